@@ -1,0 +1,189 @@
+"""CPU oracle for the fused Q4 MoE gate/up + SwiGLU (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU legs of ``bench.py``
+may import this package.  The CUDA library never imports, links or calls it,
+and it imports nothing from the CUDA library's package.
+
+The arithmetic lives in ``q4moe_oracle.c`` (plain C, f64 accumulation); this
+module compiles it with gcc on first use and marshals numpy arrays.  Every
+function cites the passage it follows in the C source.  ``group_rows``,
+``tail`` and ``gate_up_swiglu`` are pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libq4moe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_INT = ctypes.c_int
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-fPIC", "-shared", "-Wall", "-Wextra",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.q4o_bf16_rne.restype = ctypes.c_uint16
+        lib.q4o_bf16_rne.argtypes = [ctypes.c_float]
+        lib.q4o_bf16_to_f32.restype = ctypes.c_float
+        lib.q4o_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.q4o_tail.restype = None
+        lib.q4o_tail.argtypes = [ctypes.c_float, ctypes.c_float, _INT, _P]
+        lib.q4o_gate_up_swiglu.restype = _INT
+        lib.q4o_gate_up_swiglu.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I64, _INT,
+            _P, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_gate_up_swiglu_sampled.restype = _INT
+        lib.q4o_gate_up_swiglu_sampled.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I64, _INT,
+            _I64, _P, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_group_rows.restype = _INT
+        lib.q4o_group_rows.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
+        lib.q4o_max_threads.restype = _INT
+        lib.q4o_max_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_P)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return int(_load().q4o_max_threads())
+
+
+def bf16_rne(v: float) -> int:
+    """f32 -> bf16 bits, round to nearest even (page 54, trellis_bf16)."""
+    return int(_load().q4o_bf16_rne(float(np.float32(v))))
+
+
+def bf16_rne_array(a) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(a, dtype=np.float32).ravel()
+    return np.array([lib.q4o_bf16_rne(float(v)) for v in flat],
+                    dtype=np.uint16).reshape(np.shape(a))
+
+
+def tail(gate32: float, up32: float, silu_mode: int = 0):
+    """(gateT, upT, sigmoidT, siluT, out) bf16 bits for one element
+    (page 52, streamed-experts.ts, GATE_UP_SOURCE tail)."""
+    res = np.zeros(5, dtype=np.uint16)
+    _load().q4o_tail(ctypes.c_float(gate32), ctypes.c_float(up32),
+                     int(silu_mode), _ptr(res))
+    return tuple(int(v) for v in res)
+
+
+def group_rows(topk_ids, num_experts: int):
+    """Stable counting sort of (token, slot) pairs by expert.
+
+    Returns (row_offsets [E+1], token_of_row [T*k], row_of_pair [T*k])."""
+    topk = _c(topk_ids, np.int32)
+    T, k = topk.shape
+    offs = np.zeros(num_experts + 1, dtype=np.int32)
+    tok = np.zeros(T * k, dtype=np.int32)
+    rop = np.zeros(T * k, dtype=np.int32)
+    rc = _load().q4o_group_rows(_ptr(topk), T, k, num_experts, _ptr(offs),
+                                _ptr(tok), _ptr(rop))
+    if rc != 0:
+        raise ValueError(f"oracle group_rows rejected the ids (rc={rc})")
+    return offs, tok, rop
+
+
+def gate_up_swiglu(x_bits, gate_w, up_w, gate_s, up_s, row_offsets,
+                   token_of_row, silu_mode: int = 0, nthreads: int = 0,
+                   want_debug: bool = False):
+    """All M x I outputs of the grouped call.
+
+    x_bits bf16 bits [T, H] (uint16); gate_w/up_w uint32 [E, I, H/8];
+    gate_s/up_s f32 [E, I]; row_offsets int32 [E+1]; token_of_row int32 [M].
+    Returns out bits [M, I] (uint16), or with want_debug a dict that also
+    holds gate32/up32 (f32), gdot/udot (f64 unscaled dots) and gabs/uabs
+    (f64 sums of |w*x|)."""
+    x = _c(x_bits, np.uint16)
+    gw, uw = _c(gate_w, np.uint32), _c(up_w, np.uint32)
+    gs, us = _c(gate_s, np.float32), _c(up_s, np.float32)
+    offs, tok = _c(row_offsets, np.int32), _c(token_of_row, np.int32)
+    T, H = x.shape
+    E, I, _ = gw.shape
+    M = tok.shape[0]
+    out = np.zeros((M, I), dtype=np.uint16)
+    dbg = None
+    if want_debug:
+        dbg = dict(gate32=np.zeros((M, I), np.float32),
+                   up32=np.zeros((M, I), np.float32),
+                   gdot=np.zeros((M, I), np.float64),
+                   udot=np.zeros((M, I), np.float64),
+                   gabs=np.zeros((M, I), np.float64),
+                   uabs=np.zeros((M, I), np.float64))
+    g = (lambda k: _ptr(dbg[k])) if dbg else (lambda k: None)
+    rc = _load().q4o_gate_up_swiglu(
+        _ptr(x), T, H, I, E, _ptr(gw), _ptr(uw), _ptr(gs), _ptr(us),
+        _ptr(offs), _ptr(tok), M, int(silu_mode), _ptr(out), g("gate32"),
+        g("up32"), g("gdot"), g("udot"), g("gabs"), g("uabs"), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    if dbg is not None:
+        dbg["out"] = out
+        return dbg
+    return out
+
+
+def gate_up_swiglu_sampled(x_bits, gate_w, up_w, gate_s, up_s, row_offsets,
+                           token_of_row, rows, cols, silu_mode: int = 0,
+                           nthreads: int = 0):
+    """The outputs at (rows[j], cols[j]) only.  Returns a dict with out (bf16
+    bits), gate32/up32 (f32) and gabs/uabs (f64), each of length n."""
+    x = _c(x_bits, np.uint16)
+    gw, uw = _c(gate_w, np.uint32), _c(up_w, np.uint32)
+    gs, us = _c(gate_s, np.float32), _c(up_s, np.float32)
+    offs, tok = _c(row_offsets, np.int32), _c(token_of_row, np.int32)
+    r, c = _c(rows, np.int64), _c(cols, np.int64)
+    T, H = x.shape
+    E, I, _ = gw.shape
+    n = r.shape[0]
+    res = dict(out=np.zeros(n, np.uint16), gate32=np.zeros(n, np.float32),
+               up32=np.zeros(n, np.float32), gabs=np.zeros(n, np.float64),
+               uabs=np.zeros(n, np.float64))
+    rc = _load().q4o_gate_up_swiglu_sampled(
+        _ptr(x), T, H, I, E, _ptr(gw), _ptr(uw), _ptr(gs), _ptr(us),
+        _ptr(offs), _ptr(tok), tok.shape[0], int(silu_mode), n, _ptr(r),
+        _ptr(c), _ptr(res["out"]), _ptr(res["gate32"]), _ptr(res["up32"]),
+        _ptr(res["gabs"]), _ptr(res["uabs"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return res

@@ -1,0 +1,295 @@
+/*
+ * q4moe_oracle.c -- plain, slow, CPU reference of the fused Q4 MoE expert
+ * gate/up projection with SwiGLU.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * under up_swiglu_gb300/) includes, links or calls this file; only tests/,
+ * __graft_entry__.smoke() and the cpu_baseline / reference legs of bench.py
+ * load it.  It shares no code, header, table or constant with the CUDA path.
+ *
+ * Sources (all on the pages "@mlx-bun/inference 0.0.0-stage -> 1.0.0"):
+ *  - page 52, src/kernels/glm52/streamed-experts.ts, GATE_UP_SOURCE: the
+ *    per-row arithmetic (nibble p of packed word w is element 8w+p with value
+ *    ((w >> 4p) & 0xF) - 8; f32 accumulation; times the f32 row scale; gate
+ *    and up rounded to bf16; sigmoid, silu and the product each rounded to
+ *    bf16);
+ *  - page 54, src/kernels/trellis/codebook.ts, trellis_bf16: the f32 -> bf16
+ *    rounding (round to nearest, ties to even, on the bit pattern);
+ *  - page 51, src/kernels/glm52/layout.ts: the per-expert section layout
+ *    (the oracle takes the sections as separate arrays, so it never parses
+ *    a slab).
+ *
+ * Readings taken where the pages leave a step open:
+ *  - the dot product is accumulated in f64 (each product q*x is exact in
+ *    f64, so the sum is the f64 rounding of the exact dot product, far
+ *    tighter than any f32 order);
+ *  - gate32 = (float)(G * (double)scale): one rounding to f32;
+ *  - the sigmoid is the f32 chain of the page with every step correctly
+ *    rounded and no flush to zero: e = RN32(exp(-g)) (+inf on overflow),
+ *    d = RN32(1 + e), s = RN32(1 / d);  the add and the divide go through
+ *    f64, which gives the correctly rounded f32 result (double has more than
+ *    2*24+2 bits, so the double rounding is innocuous);
+ *  - silu_mode 1 keeps the sigmoid in f32 (no bf16 rounding of s), the
+ *    alternative reading of "bf16(silu(gate))"; mode 0 follows the page.
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no fast-math).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#if !defined(__STDC_IEC_559__) && !defined(__GCC_IEC_559)
+#error "the oracle needs IEEE-754 float/double semantics (Annex F)"
+#endif
+
+/* ---- bf16 <-> f32 (page 54, codebook.ts, trellis_bf16) ------------------ */
+
+/* Round an f32 to bf16, nearest with ties to even, on the bit pattern:
+ * add 0x7FFF plus the lowest kept bit, keep the upper 16 bits.  Finite inputs
+ * only (the pages' routine has no NaN case and none arises here). */
+uint16_t q4o_bf16_rne(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    u = u + 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+float q4o_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* ---- SwiGLU tail (page 52, streamed-experts.ts, GATE_UP_SOURCE tail) ---- */
+
+/* res[0..4] = gateT, upT, sigmoidT, siluT, out  (bf16 bit patterns).
+ * silu_mode 0: the page's chain (sigmoid rounded to bf16 before the product);
+ * silu_mode 1: sigmoid kept in f32 (siluT = bf16(gateT * s32)). */
+void q4o_tail(float gate32, float up32, int silu_mode, uint16_t res[5])
+{
+    const uint16_t gT = q4o_bf16_rne(gate32);
+    const uint16_t uT = q4o_bf16_rne(up32);
+    const float g = q4o_bf16_to_f32(gT);
+    const float e32 = (float)exp(-(double)g);          /* +inf past FLT_MAX */
+    const float d32 = (float)(1.0 + (double)e32);      /* RN32(1 + e)      */
+    const float s32 = (float)(1.0 / (double)d32);      /* RN32(1 / d)      */
+    const uint16_t sT = q4o_bf16_rne(s32);
+    float silu32;
+    if (silu_mode == 0)
+        silu32 = g * q4o_bf16_to_f32(sT);               /* f32 multiply    */
+    else
+        silu32 = g * s32;
+    const uint16_t siluT = q4o_bf16_rne(silu32);
+    const float o32 = q4o_bf16_to_f32(siluT) * q4o_bf16_to_f32(uT);
+    res[0] = gT;
+    res[1] = uT;
+    res[2] = sT;
+    res[3] = siluT;
+    res[4] = q4o_bf16_rne(o32);
+}
+
+/* ---- one dot product ---------------------------------------------------- */
+
+/* G = sum_k (nib(w[k>>3], k&7) - 8) * x[k] over one packed row of H/8 words
+ * (page 52, GATE_UP_SOURCE: word index = k / 8, place = k % 8, shift 4*place).
+ * Also returns sum_k |(nib - 8) * x[k]|, the scale of the rounding error any
+ * f32 summation order can make. */
+static double q4o_dot(const uint32_t *wrow, const uint16_t *xrow, int64_t H,
+                      double *absdot)
+{
+    double s = 0.0, a = 0.0;
+    for (int64_t k = 0; k < H; ++k) {
+        const uint32_t word = wrow[k >> 3];
+        const int place = (int)(k & 7);
+        const int q = (int)((word >> (4 * place)) & 0xFu) - 8;
+        const double prod = (double)q * (double)q4o_bf16_to_f32(xrow[k]);
+        s += prod;
+        a += fabs(prod);
+    }
+    *absdot = a;
+    return s;
+}
+
+/* ---- argument checks shared by the entry points below ------------------- */
+
+static int q4o_check(int64_t T, int64_t H, int64_t I, int32_t E,
+                     const int32_t *row_offsets, const int32_t *token_of_row,
+                     int64_t M)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || M < 0 || (H % 8) != 0)
+        return -1;
+    if (row_offsets[0] != 0 || row_offsets[E] != M)
+        return -2;
+    for (int32_t e = 0; e < E; ++e)
+        if (row_offsets[e + 1] < row_offsets[e])
+            return -2;
+    for (int64_t p = 0; p < M; ++p)
+        if (token_of_row[p] < 0 || token_of_row[p] >= T)
+            return -3;
+    return 0;
+}
+
+static int32_t q4o_expert_of_row(const int32_t *row_offsets, int32_t E,
+                                 int64_t p)
+{
+    for (int32_t e = 0; e < E; ++e)
+        if (p >= row_offsets[e] && p < row_offsets[e + 1])
+            return e;
+    return -1;
+}
+
+/* One output element (grouped row p, intermediate row i).  Optional outputs
+ * (any may be NULL): f32 gate/up before rounding, the f64 dot products and
+ * their absolute-value sums. */
+static void q4o_element(const uint16_t *x, int64_t H, int64_t I,
+                        const uint32_t *gate_w, const uint32_t *up_w,
+                        const float *gate_s, const float *up_s,
+                        int32_t e, int64_t t, int64_t i, int silu_mode,
+                        uint16_t *out, float *gate32, float *up32,
+                        double *gdot, double *udot, double *gabs, double *uabs)
+{
+    const int64_t words = H / 8;
+    const uint32_t *grow = gate_w + ((int64_t)e * I + i) * words;
+    const uint32_t *urow = up_w + ((int64_t)e * I + i) * words;
+    const uint16_t *xrow = x + t * H;
+    double ga, ua;
+    const double G = q4o_dot(grow, xrow, H, &ga);
+    const double U = q4o_dot(urow, xrow, H, &ua);
+    const float g32 = (float)(G * (double)gate_s[(int64_t)e * I + i]);
+    const float u32 = (float)(U * (double)up_s[(int64_t)e * I + i]);
+    uint16_t res[5];
+    q4o_tail(g32, u32, silu_mode, res);
+    *out = res[4];
+    if (gate32) *gate32 = g32;
+    if (up32) *up32 = u32;
+    if (gdot) *gdot = G;
+    if (udot) *udot = U;
+    if (gabs) *gabs = ga;
+    if (uabs) *uabs = ua;
+}
+
+/* ---- the whole grouped call ---------------------------------------------
+ * x:            bf16 bits [T, H], row-major
+ * gate_w/up_w:  uint32 [E, I, H/8]  (row i of expert e: H/8 packed words)
+ * gate_s/up_s:  f32 [E, I]
+ * row_offsets:  int32 [E+1], expert e owns grouped rows [off[e], off[e+1])
+ * token_of_row: int32 [M], the row of x that grouped row p reads
+ * out:          bf16 bits [M, I] in grouped-row order
+ * Optional (NULL to skip): gate32/up32 f32 [M, I]; gdot/udot/gabs/uabs f64
+ * [M, I].  Returns 0, or a negative code for inconsistent arguments. */
+int q4o_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                       int32_t E, const uint32_t *gate_w, const uint32_t *up_w,
+                       const float *gate_s, const float *up_s,
+                       const int32_t *row_offsets, const int32_t *token_of_row,
+                       int64_t M, int silu_mode, uint16_t *out, float *gate32,
+                       float *up32, double *gdot, double *udot, double *gabs,
+                       double *uabs, int nthreads)
+{
+    const int rc = q4o_check(T, H, I, E, row_offsets, token_of_row, M);
+    if (rc != 0)
+        return rc;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+#endif
+    for (int64_t pi = 0; pi < M * I; ++pi) {
+        const int64_t p = pi / I, i = pi % I;
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        q4o_element(x, H, I, gate_w, up_w, gate_s, up_s, e,
+                    token_of_row[p], i, silu_mode, &out[pi],
+                    gate32 ? &gate32[pi] : 0, up32 ? &up32[pi] : 0,
+                    gdot ? &gdot[pi] : 0, udot ? &udot[pi] : 0,
+                    gabs ? &gabs[pi] : 0, uabs ? &uabs[pi] : 0);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* The same arithmetic for n chosen elements (rows[j], cols[j]) only; the
+ * outputs are indexed by j.  Used where the full problem is too large. */
+int q4o_gate_up_swiglu_sampled(const uint16_t *x, int64_t T, int64_t H,
+                               int64_t I, int32_t E, const uint32_t *gate_w,
+                               const uint32_t *up_w, const float *gate_s,
+                               const float *up_s, const int32_t *row_offsets,
+                               const int32_t *token_of_row, int64_t M,
+                               int silu_mode, int64_t n, const int64_t *rows,
+                               const int64_t *cols, uint16_t *out,
+                               float *gate32, float *up32, double *gabs,
+                               double *uabs, int nthreads)
+{
+    const int rc = q4o_check(T, H, I, E, row_offsets, token_of_row, M);
+    if (rc != 0)
+        return rc;
+    for (int64_t j = 0; j < n; ++j)
+        if (rows[j] < 0 || rows[j] >= M || cols[j] < 0 || cols[j] >= I)
+            return -4;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = rows[j], i = cols[j];
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        q4o_element(x, H, I, gate_w, up_w, gate_s, up_s, e,
+                    token_of_row[p], i, silu_mode, &out[j],
+                    gate32 ? &gate32[j] : 0, up32 ? &up32[j] : 0, 0, 0,
+                    gabs ? &gabs[j] : 0, uabs ? &uabs[j] : 0);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* ---- token -> expert grouping -------------------------------------------
+ * topk: int32 [T, k], the experts each token is routed to.  Produces the
+ * per-expert row lists the gate/up call consumes: row_offsets [E+1]
+ * (counts, exclusive prefix sum), token_of_row [T*k] (the token of each
+ * grouped row) and row_of_pair [T*k] (the grouped row of pair t*k+j, for
+ * putting outputs back in token order).  Rows of one expert keep the
+ * token order (a stable counting sort).  Returns -1 on an expert id outside
+ * [0, E). */
+int q4o_group_rows(const int32_t *topk, int64_t T, int32_t k, int32_t E,
+                   int32_t *row_offsets, int32_t *token_of_row,
+                   int32_t *row_of_pair)
+{
+    if (T < 0 || k <= 0 || E <= 0)
+        return -1;
+    for (int32_t e = 0; e <= E; ++e)
+        row_offsets[e] = 0;
+    for (int64_t q = 0; q < T * k; ++q) {
+        if (topk[q] < 0 || topk[q] >= E)
+            return -1;
+        row_offsets[topk[q] + 1] += 1;
+    }
+    for (int32_t e = 0; e < E; ++e)
+        row_offsets[e + 1] += row_offsets[e];
+    for (int32_t e = 0; e < E; ++e) {
+        /* walk the pairs in order, so equal experts keep token order */
+        int32_t next = row_offsets[e];
+        for (int64_t q = 0; q < T * k; ++q) {
+            if (topk[q] != e)
+                continue;
+            token_of_row[next] = (int32_t)(q / k);
+            row_of_pair[q] = next;
+            ++next;
+        }
+    }
+    return 0;
+}
+
+int q4o_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
