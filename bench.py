@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused Q4 MoE expert gate/up + SwiGLU on one GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * grouped workloads: token->expert grouping + the fused gate/up call;
+  * the single-expert decode workload (H=4096, I=1536, one token): the call
+    repeated 1000 times (the workload's own definition), each repeat on a
+    different expert slab from a pool larger than 4x L2, captured once in a
+    CUDA graph and replayed.
+Inputs stay resident in HBM; every step streams its weights from HBM (the
+weight pool of every workload is larger than L2).  Prints one JSON line.
+
+  python bench.py [--workload NAME] [--steps K] [--warmup W] [--gpus N]
+  python bench.py --impl reference ...   (the CPU oracle, timed alone)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from up_swiglu_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = ("weight GB/s and TFLOP/s of Q4 MoE gate/up/SwiGLU; "
+          "% of HBM / tensor roofline")
+DEFAULT_WORKLOAD = "expert1_h4096_i1536_m1_x1000"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="auto",
+                    choices=["auto", "matvec", "gemm"])
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ workload math --
+
+def workload_units(w: syn.Workload, topk: np.ndarray, E_pool: int):
+    """Algorithmic work of one step: weight bytes (each touched expert's
+    packed words + f32 scales, once per call), all bytes (+ x read + out
+    written) and flops (4*H*I per routed row)."""
+    per_expert = w.I * (w.H + 8)
+    if w.repeats > 1:
+        calls = w.repeats
+        weight = calls * per_expert
+        x_bytes = calls * 2 * w.H * w.T
+        out_bytes = calls * 2 * w.I * w.routed_rows
+        flops = calls * 4 * w.H * w.I * w.routed_rows
+        touched = calls
+    else:
+        touched = int(np.unique(topk).size)
+        weight = touched * per_expert
+        x_bytes = 2 * w.H * w.T
+        out_bytes = 2 * w.I * w.routed_rows
+        flops = 4 * w.H * w.I * w.routed_rows
+    return dict(weight_bytes=weight, bytes=weight + x_bytes + out_bytes,
+                flops=flops, touched_experts=touched)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str, kernel_file: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current source of the kernel (sha256 of the .cu file)."""
+    import hashlib
+    src = os.path.join(ROOT, "up_swiglu_gb300", "csrc", kernel_file)
+    table = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(table):
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and \
+                    parts[0] == workload and parts[1] == kernel_file and \
+                    parts[2] == sha:
+                return float(parts[3])
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                                    delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}",
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(parts)
+                except ValueError:
+                    pass
+        os.unlink(self.file.name)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        power = [float(r[3]) for r in rows
+                 if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------- GPU set-up --
+
+class GpuWorkload:
+    """Device-resident inputs for one workload and the step launcher."""
+
+    def __init__(self, w: syn.Workload, kernel: str, device: int):
+        import torch
+        from up_swiglu_gb300 import q4moe as q
+        self.torch, self.q, self.w = torch, q, w
+        self.kernel = {"auto": q.KERNEL_AUTO, "matvec": q.KERNEL_MATVEC,
+                       "gemm": q.KERNEL_GEMM}[kernel]
+        self.dev = torch.device("cuda", device)
+        self.stream = torch.cuda.current_stream(self.dev)
+        L = q.q4moe_canonical_layout(w.H, w.I)
+        self.layout = L
+        if w.repeats > 1:
+            # distinct expert slabs, more than 4x L2 in total
+            pool_experts = max(8, math.ceil(4 * L2_BYTES / L.slab_bytes) + 1)
+            pool_experts = min(pool_experts, w.repeats)
+        else:
+            pool_experts = w.E
+        self.pool_experts = pool_experts
+        g = syn.generate(w, experts=pool_experts)
+        self.host = g
+        self.topk_host = g["topk"]
+        host_pool = q.pack_slab_pool(L, g["gate_w"], g["up_w"], g["gate_s"],
+                                     g["up_s"])
+        nbytes = host_pool.size
+        self._buf = torch.empty(nbytes + 4096, dtype=torch.uint8,
+                                device=self.dev)
+        off = (-self._buf.data_ptr()) % 4096
+        self.pool = self._buf[off:off + nbytes]
+        self.pool.copy_(torch.from_numpy(host_pool.reshape(-1)))
+        del host_pool
+        self.x = torch.from_numpy(g["x"].view(np.int16)).to(self.dev)
+        self.topk = torch.from_numpy(g["topk"]).to(self.dev)
+        self.M = w.routed_rows
+        self.calls = w.repeats
+        self.offs = torch.empty(w.E + 1, dtype=torch.int32, device=self.dev)
+        self.tok = torch.empty(self.M, dtype=torch.int32, device=self.dev)
+        self.rop = torch.empty(self.M, dtype=torch.int32, device=self.dev)
+        self.out = torch.empty((self.calls * self.M, w.I), dtype=torch.int16,
+                               device=self.dev)
+        if w.repeats > 1:
+            # single expert, single row: the grouping is the identity
+            self.offs.copy_(torch.tensor([0, self.M], dtype=torch.int32))
+            self.tok.zero_()
+            self.slabs = [q.make_slabs(1, L, base=self.pool.data_ptr() +
+                                       (r % pool_experts) * L.slab_bytes)
+                          for r in range(self.calls)]
+        else:
+            self.slabs = [q.make_slabs(w.E, L, base=self.pool)]
+        self.opts = q.q4moe_options_t()
+        self.opts.kernel = self.kernel
+        self.graph = None
+        self.launches_per_step = None
+
+    def _gate_up(self, r):
+        q = self.q
+        out = self.out.data_ptr() + r * self.M * self.w.I * 2
+        q.q4moe_gate_up_swiglu_ex(self.x, self.slabs[r], self.offs, self.tok,
+                                  self.M, self.w.H, self.w.I, out, self.opts,
+                                  self.stream)
+
+    def enqueue_step(self, ev=None):
+        """Queue one step; ev = (start, mid) events bracket the grouping so
+        the gate/up part can be timed on its own."""
+        q = self.q
+        if self.calls > 1:
+            if self.graph is None:
+                self._capture()
+            if ev is not None:
+                ev[0].record(self.stream)
+                ev[1].record(self.stream)
+            self.graph.replay()
+            return
+        if ev is not None:
+            ev[0].record(self.stream)
+        q.q4moe_group_rows(self.topk, self.w.T, self.w.topk, self.w.E,
+                           self.offs, self.tok, self.rop, self.stream)
+        if ev is not None:
+            ev[1].record(self.stream)
+        self._gate_up(0)
+
+    def _capture(self):
+        torch = self.torch
+        for r in range(min(3, self.calls)):      # library set-up off-capture
+            self._gate_up(r)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(self.stream)
+        n0 = self.q.q4moe_launch_count()
+        with torch.cuda.graph(g, stream=s):
+            saved = self.stream
+            self.stream = s
+            try:
+                for r in range(self.calls):
+                    self._gate_up(r)
+            finally:
+                self.stream = saved
+        self.launches_per_step = self.q.q4moe_launch_count() - n0
+        self.stream.wait_stream(s)
+        self.graph = g
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0):
+    """Time the oracle on grouped rows (all I outputs each) until about
+    budget_s seconds of work; returns (seconds per routed row, rows done,
+    threads)."""
+    import oracle
+    oracle.build()
+    topk = g["topk"]
+    E = g["gate_w"].shape[0]
+    if w.repeats > 1:
+        offs, tok = np.array([0, 1], np.int32), np.zeros(1, np.int32)
+        Ew = 1
+    else:
+        offs, tok, _ = oracle.group_rows(topk, w.E)
+        Ew = w.E
+    M = int(offs[-1])
+    rng = np.random.default_rng(0)
+    rows_done, t_total = 0, 0.0
+    order = rng.permutation(M) if M > 1 else np.zeros(1, np.int64)
+    batch = max(1, min(M, 16))
+    i = 0
+    while t_total < budget_s:
+        rows = order[i % M: i % M + batch] if M > 1 else order
+        cols = np.tile(np.arange(w.I), rows.size)
+        rr = np.repeat(rows, w.I)
+        t0 = time.perf_counter()
+        oracle.gate_up_swiglu_sampled(
+            g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
+            g["up_s"][:Ew], offs, tok, rr, cols, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        rows_done += rows.size
+        i += batch
+    del E
+    return t_total / rows_done, rows_done, oracle.max_threads()
+
+
+def cpu_value(w, units, sec_per_row):
+    """Oracle throughput scaled to the whole step: weight GB/s."""
+    rows_per_step = w.routed_rows * max(1, w.repeats)
+    t_step = sec_per_row * rows_per_step
+    return units["weight_bytes"] / t_step / 1e9, t_step
+
+
+# ------------------------------------------------------------------- main --
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle as it stands, on the host cores,
+    each step a bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return 0
+    g = syn.generate(w, experts=w.E if w.repeats == 1 else 1)
+    units = workload_units(w, g["topk"], w.E)
+    per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps +
+                                                    args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, g, per_step_budget / 4)
+    times, rows = [], 0
+    for _ in range(args.steps):
+        spr, n, threads = oracle_sample(w, g, per_step_budget)
+        times.append(spr)
+        rows += n
+    spr = statistics.mean(times)
+    value, t_step = cpu_value(w, units, spr)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4),
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded generator)",
+        "config": {"workload": w.name, "E": w.E, "H": w.H, "I": w.I,
+                   "tokens": w.T, "top_k": w.topk,
+                   "routed_rows": w.routed_rows, "repeats": w.repeats},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                         "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} routed rows x all {w.I} outputs "
+                                   f"over {args.steps} steps, scaled to the "
+                                   f"step's {w.routed_rows * w.repeats} rows"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    w = syn.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    from up_swiglu_gb300 import q4moe as q
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    q.load()
+
+    gw = GpuWorkload(w, args.kernel, local)
+    units = workload_units(w, gw.topk_host, gw.pool_experts)
+    dev = gw.dev
+    stream = gw.stream
+
+    # CPU baseline (host threads only, before the timed GPU work)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        spr, n, threads = oracle_sample(w, gw.host, args.cpu_seconds)
+        v, _ = cpu_value(w, units, spr)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} routed rows x all {w.I} outputs "
+                         f"(~{args.cpu_seconds:.0f} s), scaled to the step's "
+                         f"{w.routed_rows * w.repeats} rows"}
+
+    # warm-up
+    for _ in range(max(args.warmup, 3)):
+        gw.enqueue_step()
+    torch.cuda.synchronize(dev)
+    assert q.q4moe_device_status(stream, clear=True) == 0
+
+    # timed region: K steps, barrier + synchronize on both sides
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_end = [torch.cuda.Event(enable_timing=True)
+              for _ in range(args.steps)]
+    n0 = q.q4moe_launch_count()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_stop = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            gw.enqueue_step(ev[k])
+            ev_end[k].record(stream)
+        t_stop.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    launches = q.q4moe_launch_count() - n0
+    if gw.graph is not None:
+        launches = gw.launches_per_step * args.steps
+    total_ms = t_start.elapsed_time(t_stop)
+    gate_up_ms = [ev[k][1].elapsed_time(ev_end[k]) for k in range(args.steps)]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    world_weight = units["weight_bytes"] * args.steps * world
+    value = world_weight / (total_ms * 1e-3) / 1e9
+    tflops = units["flops"] * args.steps * world / (total_ms * 1e-3) / 1e12
+    clocks = clk.summary()
+
+    # roofline of the dominant kernel: the fused gate/up launch(es)
+    peaks, peak_src = load_peaks()
+    gu_ms = statistics.mean(gate_up_ms)
+    per_launch_ms = gu_ms / gw.calls
+    rows_per_expert = (w.routed_rows if w.repeats > 1 else
+                       w.routed_rows / units["touched_experts"])
+    decode = rows_per_expert < 64
+    if decode:
+        bytes_per_launch = units["bytes"] / gw.calls
+        achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 2),
+                "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": load_traffic(w.name, "q4moe_matvec.cu"),
+                "kernel": "q4moe_gate_up_swiglu matvec",
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    else:
+        flops_per_launch = units["flops"] / gw.calls
+        achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": load_traffic(w.name, "q4moe_gemm.cu"),
+                "kernel": "q4moe_gate_up_swiglu gemm",
+                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (activations + routing) from pinned memory, D2H of the outputs
+    x_h = torch.from_numpy(gw.host["x"].view(np.int16)).pin_memory()
+    t_h = torch.from_numpy(gw.topk_host).pin_memory()
+    o_h = torch.empty(gw.out.shape, dtype=torch.int16).pin_memory()
+    h2d = x_h.numel() * 2 + (t_h.numel() * 4 if w.repeats == 1 else 0)
+    d2h = o_h.numel() * 2
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        gw.x.copy_(x_h, non_blocking=True)
+        if w.repeats == 1:
+            gw.topk.copy_(t_h, non_blocking=True)
+        gw.enqueue_step()
+        o_h.copy_(gw.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = units["weight_bytes"] * world / (e2e_ms * 1e-3) / 1e9
+    status = q.q4moe_device_status(stream, clear=True)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": w.name, "E": w.E, "H": w.H, "I": w.I,
+                       "tokens": w.T, "top_k": w.topk,
+                       "routed_rows": w.routed_rows, "repeats": w.repeats,
+                       "touched_experts": units["touched_experts"],
+                       "weight_bytes_per_step": units["weight_bytes"],
+                       "l2": "weights larger than L2 every step "
+                             f"({gw.pool_experts} distinct expert slabs)",
+                       "kernel_choice": args.kernel,
+                       "parallelism": f"replicas x{world}" if world > 1
+                       else "single GPU"},
+            "tflops": round(tflops, 3),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches),
+            "clocks": {"sm_mhz": clocks["sm_mhz"],
+                       "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"],
+                       "samples": clocks["samples"]},
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,230 @@
+/*
+ * q4moe.h -- C ABI of the fused 4-bit MoE expert gate/up projection with
+ * SwiGLU for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation follows "@mlx-bun/inference 0.0.0-stage -> 1.0.0", page 52,
+ * src/kernels/glm52/streamed-experts.ts, GATE_UP_SOURCE (and the
+ * Glm52CanonicalMetalExecutor around it), with the expert slot layout of
+ * page 51, src/kernels/glm52/layout.ts, and the bf16 rounding of page 54,
+ * src/kernels/trellis/codebook.ts, trellis_bf16.  For every grouped row p of
+ * expert e, token t = token_to_expert_map[p], and output row i < I:
+ *
+ *   G  = sum_k (nib(gate_w[e][i][k/8], k%8) - 8) * x[t][k]      (f32 accumulate)
+ *   U  = the same over up_w
+ *   gateT = bf16(G * gate_s[e][i]),  upT = bf16(U * up_s[e][i])
+ *   sigT  = bf16(1 / (1 + exp(-gateT)))       (f32 chain, no flush to zero)
+ *   siluT = bf16(gateT * sigT)
+ *   out[p][i] = bf16(siluT * upT)
+ *
+ * where nib(w, j) = (w >> 4j) & 0xF and bf16() rounds to nearest, ties to
+ * even.  Summation order is not fixed by the pages: f32 gate/up agree with
+ * an f64 accumulation to about 1e-5 relative; with integer activations in
+ * [-8, 8] and power-of-two scales every sum is exact and the output is
+ * bit-exact.
+ *
+ * Conventions for every entry point:
+ *  - Return 0 (Q4MOE_OK) or a negative Q4MOE_ERR_* code; no C++ exception
+ *    crosses the ABI.  q4moe_last_error() gives the calling thread's message
+ *    for its last failure.
+ *  - "device" pointers are CUDA device (or managed) memory of the current
+ *    device; "host" pointers are ordinary host memory.  Every buffer is
+ *    borrowed: the caller owns it and keeps it alive until the work queued
+ *    on `stream` has completed.
+ *  - GPU entry points are asynchronous on `stream`, never synchronise the
+ *    host, and allocate no memory.  Argument errors the host can see are
+ *    returned before anything is launched.  Inconsistent data that only the
+ *    GPU can see (row offsets, token indices, expert ids, slab pointers) sets
+ *    a bit in the device status word (Q4MOE_DEV_*) and the affected rows are
+ *    skipped; read it with q4moe_device_status().  Nothing traps the GPU.
+ *  - Only sm_103 devices are accepted (Q4MOE_ERR_DEVICE otherwise).
+ */
+#ifndef Q4MOE_H_
+#define Q4MOE_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4MOE_ABI_VERSION 1
+
+/* Slab base addresses and strides must be multiples of this (the pages use
+ * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
+#define Q4MOE_SLAB_ALIGNMENT 4096
+
+/* Most experts one call accepts (row offsets are staged on chip). */
+#define Q4MOE_MAX_EXPERTS 1024
+
+/* ---- status codes ------------------------------------------------------ */
+#define Q4MOE_OK 0
+#define Q4MOE_ERR_INVALID_ARG (-1) /* null pointer, bad size or dimension  */
+#define Q4MOE_ERR_ALIGNMENT (-2)   /* slab base/stride/section misaligned  */
+#define Q4MOE_ERR_RANGE (-3)       /* a slab section lies outside the slab */
+#define Q4MOE_ERR_DEVICE (-4)      /* no usable sm_103 device              */
+#define Q4MOE_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+#define Q4MOE_ERR_DEVICE_DATA (-6) /* the device status word is nonzero    */
+
+/* ---- device status bits (see q4moe_device_status) ----------------------- */
+#define Q4MOE_DEV_BAD_ROW_OFFSETS 0x1u /* offsets not 0..M, or decreasing  */
+#define Q4MOE_DEV_BAD_TOKEN 0x2u       /* token index outside [0, T)        */
+#define Q4MOE_DEV_BAD_SLAB_PTR 0x4u    /* per-expert slab pointer misaligned */
+#define Q4MOE_DEV_BAD_EXPERT_ID 0x8u   /* routed expert id outside [0, E)    */
+#define Q4MOE_DEV_WAIT_TIMEOUT 0x10u   /* a bounded on-chip wait ran out     */
+
+/* ---- kernel selection (q4moe_options_t.kernel) -------------------------- */
+#define Q4MOE_KERNEL_AUTO 0   /* by rows per expert                          */
+#define Q4MOE_KERNEL_MATVEC 1 /* every expert on the streamed matvec         */
+#define Q4MOE_KERNEL_GEMM 2   /* every nonempty expert on the tensor-core GEMM */
+
+/*
+ * Byte layout of one expert slab (page 51, layout.ts,
+ * Glm52CanonicalMetalLayout, restricted to the sections this operation
+ * reads).  Offsets are bytes from the start of the slab.
+ *   gate_w_offset, up_w_offset: uint32 [I][H/8] row-major packed nibbles,
+ *       4-byte aligned; element k of row i is nibble k%8 (bits 4*(k%8)) of
+ *       word i*(H/8) + k/8.
+ *   gate_s_offset, up_s_offset: f32 [I] row scales, 4-byte aligned.
+ * Each section must lie inside [0, slab_bytes) (page 51, validateRange).
+ */
+typedef struct q4moe_layout {
+    int64_t hidden_size;       /* H: > 0, multiple of 8 (page 52, validateCall) */
+    int64_t intermediate_size; /* I: > 0, multiple of 4                         */
+    int64_t slab_bytes;        /* bytes of one slab                             */
+    int64_t gate_w_offset;
+    int64_t up_w_offset;
+    int64_t gate_s_offset;
+    int64_t up_s_offset;
+} q4moe_layout_t;
+
+/*
+ * Where the expert slabs live.  Expert e's slab starts at
+ *   slab_ptrs[e]                  if slab_ptrs != NULL (a device array of E
+ *                                 device pointers, e.g. a residency cache's
+ *                                 slots; each must be 4096-aligned, checked
+ *                                 on the device), else
+ *   base + e * slab_stride        (base 4096-aligned device pointer,
+ *                                 slab_stride a multiple of 4096 and
+ *                                 >= layout.slab_bytes).
+ */
+typedef struct q4moe_slabs {
+    int32_t num_experts; /* E: 1 .. Q4MOE_MAX_EXPERTS */
+    int32_t reserved0;   /* must be 0                 */
+    const void *base;
+    int64_t slab_stride;
+    const void *const *slab_ptrs;
+    q4moe_layout_t layout;
+} q4moe_slabs_t;
+
+/* Optional arguments of q4moe_gate_up_swiglu_ex (zero-initialise). */
+typedef struct q4moe_options {
+    int64_t num_tokens; /* T, rows of x; > 0 turns on the device check that
+                           every token index is in [0, T)                  */
+    float *gate_f32;    /* optional device f32 [M][I]: G * gate scale,
+                           before rounding to bf16                         */
+    float *up_f32;      /* optional device f32 [M][I]: U * up scale        */
+    int32_t kernel;     /* Q4MOE_KERNEL_*                                  */
+    int32_t reserved0;  /* must be 0                                       */
+} q4moe_options_t;
+
+/* ABI version of the loaded library (Q4MOE_ABI_VERSION). */
+int q4moe_abi_version(void);
+
+/* Message of the calling thread's last failed call ("" if none). The string
+ * is owned by the library and valid until the thread's next call. */
+const char *q4moe_last_error(void);
+
+/*
+ * Fill *layout with the canonical slab layout for (H, I): gate words at 0,
+ * up words at I*H/2, gate scales at I*H, up scales at I*H + 4*I, slab size
+ * rounded up to Q4MOE_SLAB_ALIGNMENT.  Host only.
+ */
+int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout);
+
+/* Check a layout: dimensions (page 52, validateCall), section alignment and
+ * ranges (page 51, validateRange).  Host only. */
+int q4moe_validate_layout(const q4moe_layout_t *layout);
+
+/*
+ * Copy one expert's sections into a host slab buffer of layout->slab_bytes
+ * bytes, zeroing the rest.  gate_w/up_w: host uint32 [I][H/8]; gate_s/up_s:
+ * host f32 [I]; slab_host: host buffer.  Host only (copy the slab to the
+ * device yourself).
+ */
+int q4moe_pack_slab(const q4moe_layout_t *layout, const uint32_t *gate_w,
+                    const uint32_t *up_w, const float *gate_s,
+                    const float *up_s, void *slab_host);
+
+/*
+ * Token -> expert grouping: a stable counting sort of the T*k routed
+ * (token, slot) pairs by expert id.  The pages dispatch one expert slot at a
+ * time with its rows as an [M, H] input (page 52, execute); this builds the
+ * per-expert row lists for all experts at once.
+ *   topk_ids      device int32 [T][k]: expert of slot j of token t.
+ *   row_offsets   device int32 [E+1] out: expert e owns grouped rows
+ *                 [row_offsets[e], row_offsets[e+1]); row_offsets[E] = T*k
+ *                 minus the pairs with an id outside [0, E).
+ *   token_of_row  device int32 [T*k] out: token of each grouped row, tokens
+ *                 ascending within an expert.
+ *   row_of_pair   device int32 [T*k] out: grouped row of pair t*k+j (-1 for
+ *                 a bad id), for putting outputs back in token order.
+ * An id outside [0, E) sets Q4MOE_DEV_BAD_EXPERT_ID and the pair is dropped.
+ * T >= 0, 1 <= k, 1 <= E <= Q4MOE_MAX_EXPERTS, T*k < 2^31.
+ */
+int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
+                     int32_t E, int32_t *row_offsets, int32_t *token_of_row,
+                     int32_t *row_of_pair, cudaStream_t stream);
+
+/*
+ * The fused gate/up + SwiGLU over grouped rows (the formula at the top).
+ *   x                       device bf16 [T][H], row-major, row stride H.
+ *   expert_slabs            host pointer, read during the call only.
+ *   row_offsets_per_expert  device int32 [E+1], 0 = off[0] <= ... <= off[E] = M.
+ *   token_to_expert_map     device int32 [M]: the row of x that grouped row
+ *                           p reads (a "sorted per-expert row list"; the
+ *                           name keeps the pages' wording).
+ *   M                       grouped rows (>= 0; 0 is a no-op).
+ *   H, I                    must equal the layout's.
+ *   out                     device bf16 [M][I], grouped-row order, fully
+ *                           written on success.
+ * Kernel choice per expert: up to 8 rows (and, measured, up to 48) on the
+ * HBM-streaming matvec, more on the tcgen05 tensor-core GEMM.
+ */
+int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *expert_slabs,
+                         const int32_t *row_offsets_per_expert,
+                         const int32_t *token_to_expert_map, int64_t M,
+                         int64_t H, int64_t I, void *out, cudaStream_t stream);
+
+/* q4moe_gate_up_swiglu with options (opts may be NULL). */
+int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *expert_slabs,
+                            const int32_t *row_offsets_per_expert,
+                            const int32_t *token_to_expert_map, int64_t M,
+                            int64_t H, int64_t I, void *out,
+                            const q4moe_options_t *opts, cudaStream_t stream);
+
+/*
+ * Wait for `stream`, then read the current device's status word into
+ * *flags (Q4MOE_DEV_* bits accumulated since the last clear) and clear it
+ * if `clear` is nonzero.  Returns Q4MOE_ERR_DEVICE_DATA when *flags != 0.
+ * This is the one entry point that synchronises the host.
+ */
+int q4moe_device_status(cudaStream_t stream, uint32_t *flags, int clear);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * devices, all entry points); a host-side counter for benchmarks. */
+int64_t q4moe_launch_count(void);
+
+/*
+ * Diagnostic: evaluate the device's SwiGLU tail alone.  For n elements,
+ * from bf16 gate and up values (device uint16 [n] each) write the device
+ * uint16 [n][4] results sigT, siluT, out, and gateT re-rounded (a check
+ * that it is already bf16).  Used to test the tail exhaustively.
+ */
+int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
+                     int64_t n, uint16_t *res, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4MOE_H_ */

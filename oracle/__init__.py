@@ -59,6 +59,8 @@ def _load():
         lib.q4o_bf16_to_f32.argtypes = [ctypes.c_uint16]
         lib.q4o_tail.restype = None
         lib.q4o_tail.argtypes = [ctypes.c_float, ctypes.c_float, _INT, _P]
+        lib.q4o_tail_array.restype = None
+        lib.q4o_tail_array.argtypes = [_I64, _P, _P, _INT, _P]
         lib.q4o_gate_up_swiglu.restype = _INT
         lib.q4o_gate_up_swiglu.argtypes = [
             _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I64, _INT,
@@ -106,6 +108,17 @@ def tail(gate32: float, up32: float, silu_mode: int = 0):
     _load().q4o_tail(ctypes.c_float(gate32), ctypes.c_float(up32),
                      int(silu_mode), _ptr(res))
     return tuple(int(v) for v in res)
+
+
+def tail_array(gate32, up32, silu_mode: int = 0) -> np.ndarray:
+    """tail() over arrays of f32 gate/up values; returns uint16 [n, 5]."""
+    g = _c(gate32, np.float32).ravel()
+    u = _c(up32, np.float32).ravel()
+    assert g.shape == u.shape
+    res = np.zeros((g.shape[0], 5), dtype=np.uint16)
+    _load().q4o_tail_array(g.shape[0], _ptr(g), _ptr(u), int(silu_mode),
+                           _ptr(res))
+    return res
 
 
 def group_rows(topk_ids, num_experts: int):

@@ -95,6 +95,14 @@ void q4o_tail(float gate32, float up32, int silu_mode, uint16_t res[5])
     res[4] = q4o_bf16_rne(o32);
 }
 
+/* q4o_tail over n elements: res is [n][5] (gateT, upT, sigT, siluT, out). */
+void q4o_tail_array(int64_t n, const float *gate32, const float *up32,
+                    int silu_mode, uint16_t *res)
+{
+    for (int64_t j = 0; j < n; ++j)
+        q4o_tail(gate32[j], up32[j], silu_mode, res + 5 * j);
+}
+
 /* ---- one dot product ---------------------------------------------------- */
 
 /* G = sum_k (nib(w[k>>3], k&7) - 8) * x[k] over one packed row of H/8 words

@@ -1,0 +1,179 @@
+"""Host/GPU plumbing shared by the GPU tests: build a problem from the seeded
+generator, upload it, and call the library through its C ABI binding.
+PyTorch only allocates device memory and provides the stream."""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from up_swiglu_gb300 import q4moe as q
+from up_swiglu_gb300 import synthetic as syn
+
+
+@dataclass
+class Problem:
+    x: np.ndarray         # bf16 bits [T, H]
+    gate_w: np.ndarray    # uint32 [E, I, H/8]
+    up_w: np.ndarray
+    gate_s: np.ndarray    # f32 [E, I]
+    up_s: np.ndarray
+    topk: np.ndarray      # int32 [T, k]
+
+    @property
+    def E(self):
+        return self.gate_w.shape[0]
+
+    @property
+    def I(self):
+        return self.gate_w.shape[1]
+
+    @property
+    def H(self):
+        return self.x.shape[1]
+
+    @property
+    def T(self):
+        return self.x.shape[0]
+
+    @property
+    def k(self):
+        return self.topk.shape[1]
+
+
+def random_problem(seed, E, I, H, T, k, routing="uniform", x_std=1.0):
+    x = syn.normal_x(seed, T, H, x_std)
+    gw, uw, gs, us = syn.weights(seed, E, I, H)
+    if routing == "uniform":
+        topk = syn.route_uniform(seed, T, k, E)
+    elif routing == "zipf":
+        topk = syn.route_zipf(seed, T, k, E, 1.1)
+    else:
+        raise ValueError(routing)
+    return Problem(x, gw, uw, gs, us, topk)
+
+
+def exact_problem(seed, E, I, H, T, k):
+    x, gw, uw, gs, us = syn.exact_integer_case(seed, T, H, E, I)
+    return Problem(x, gw, uw, gs, us, syn.route_uniform(seed, T, k, E))
+
+
+def problem_with_counts(seed, counts, I, H, exact=False):
+    """One token per routed row, expert e getting counts[e] rows."""
+    E = len(counts)
+    T = int(sum(counts))
+    ids = np.concatenate([np.full(c, e, np.int32)
+                          for e, c in enumerate(counts)])
+    ids = ids[np.random.default_rng(seed).permutation(T)] if T else ids
+    if exact:
+        x, gw, uw, gs, us = syn.exact_integer_case(seed, max(T, 1), H, E, I)
+        x = x[:T]
+    else:
+        x = syn.normal_x(seed, T, H)
+        gw, uw, gs, us = syn.weights(seed, E, I, H)
+    return Problem(x, gw, uw, gs, us, ids.reshape(T, 1))
+
+
+def aligned_device_buffer(nbytes, align=q.SLAB_ALIGNMENT):
+    import torch
+    buf = torch.empty(nbytes + align, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % align
+    return buf, buf[off:off + nbytes]
+
+
+@dataclass
+class DeviceProblem:
+    p: Problem
+    layout: object
+    slabs: object
+    keep: list = field(default_factory=list)
+    x: object = None
+    topk: object = None
+
+
+def upload(p: Problem, layout=None, stride_pad=0, ptr_table=False):
+    """Pack the experts into slabs (canonical layout unless given), copy them
+    into one 4096-aligned device pool, and upload x and the routing."""
+    import torch
+    L = layout or q.q4moe_canonical_layout(p.H, p.I)
+    host = q.pack_slab_pool(L, p.gate_w, p.up_w, p.gate_s, p.up_s)
+    stride = L.slab_bytes + stride_pad
+    keep = []
+    buf, pool = aligned_device_buffer(p.E * stride)
+    keep.append(buf)
+    if stride == L.slab_bytes:
+        pool.copy_(torch.from_numpy(host.reshape(-1)))
+    else:
+        for e in range(p.E):
+            pool[e * stride:e * stride + L.slab_bytes].copy_(
+                torch.from_numpy(host[e]))
+    if ptr_table:
+        # slots in a shuffled order: expert e lives in slot perm[e]
+        perm = np.random.default_rng(p.E).permutation(p.E)
+        buf2, pool2 = aligned_device_buffer(p.E * stride)
+        keep.append(buf2)
+        for e in range(p.E):
+            pool2[perm[e] * stride:perm[e] * stride + L.slab_bytes].copy_(
+                pool[e * stride:e * stride + L.slab_bytes])
+        ptrs = torch.tensor([pool2.data_ptr() + int(perm[e]) * stride
+                             for e in range(p.E)], dtype=torch.int64,
+                            device="cuda")
+        keep.append(ptrs)
+        slabs = q.make_slabs(p.E, L, slab_ptrs=ptrs)
+    else:
+        slabs = q.make_slabs(p.E, L, base=pool, slab_stride=stride)
+    d = DeviceProblem(p, L, slabs, keep)
+    d.x = torch.from_numpy(np.ascontiguousarray(p.x).view(np.int16)).cuda()
+    d.topk = torch.from_numpy(np.ascontiguousarray(p.topk)).cuda()
+    return d
+
+
+def group(d: DeviceProblem, stream=None):
+    import torch
+    n = d.p.T * d.p.k
+    offs = torch.empty(d.p.E + 1, dtype=torch.int32, device="cuda")
+    tok = torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+    rop = torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+    q.q4moe_group_rows(d.topk, d.p.T, d.p.k, d.p.E, offs, tok, rop, stream)
+    return offs, tok[:n], rop[:n]
+
+
+def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
+            stream=None, out=None):
+    """Run the fused call; returns numpy out bits [M, I] (+ gate32/up32)."""
+    import torch
+    M = int(tok.shape[0])
+    I = d.p.I
+    if out is None:
+        out = torch.full((max(M, 1), I), -1, dtype=torch.int16,
+                         device="cuda")
+    res = {}
+    if debug or kernel != q.KERNEL_AUTO:
+        g32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
+            if debug else None
+        u32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
+            if debug else None
+        o = q.q4moe_options_t()
+        o.num_tokens = d.p.T
+        o.gate_f32 = None if g32 is None else g32.data_ptr()
+        o.up_f32 = None if u32 is None else u32.data_ptr()
+        o.kernel = kernel
+        q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, offs, tok, M, d.p.H, I, out,
+                                  o, stream)
+        if debug:
+            res["gate32"] = g32[:M].cpu().numpy()
+            res["up32"] = u32[:M].cpu().numpy()
+    else:
+        q.q4moe_gate_up_swiglu(d.x, d.slabs, offs, tok, M, d.p.H, I, out,
+                               stream)
+    torch.cuda.synchronize()
+    res["out"] = out[:M].cpu().numpy().view(np.uint16)
+    return res
+
+
+def element_scales(p: Problem, offs: np.ndarray):
+    """gate/up scale of every output element [M, I] (grouped order)."""
+    M = int(offs[-1])
+    e_of_row = np.repeat(np.arange(p.E), np.diff(offs))
+    assert e_of_row.shape[0] == M
+    return p.gate_s[e_of_row], p.up_s[e_of_row]

@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA
+call (validation rules: page 52 validateCall, page 51 validateRange)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from up_swiglu_gb300 import q4moe as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "q4moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4moe_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = q.load()
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert sorted(q.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert q.q4moe_abi_version() == q.ABI_VERSION
+
+
+def test_canonical_layout():
+    L = q.q4moe_canonical_layout(5120, 1536)
+    assert (L.gate_w_offset, L.up_w_offset) == (0, 1536 * 2560)
+    assert L.gate_s_offset == 1536 * 5120
+    assert L.up_s_offset == 1536 * 5120 + 4 * 1536
+    assert L.slab_bytes == 7876608 == 1923 * 4096
+    assert q.q4moe_canonical_layout(512, 256).slab_bytes == 135168
+    assert q.q4moe_canonical_layout(4096, 1536).slab_bytes == 6303744
+    for H, I in ((0, 4), (12, 4), (8, 6), (8, 0), (-8, 4)):
+        with pytest.raises(q.Q4moeError) as ei:
+            q.q4moe_canonical_layout(H, I)
+        assert ei.value.code == q.ERR_INVALID_ARG
+
+
+def test_validate_layout_ranges_and_alignment():
+    L = q.q4moe_canonical_layout(64, 8)
+    q.q4moe_validate_layout(L)
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.up_s_offset = L.slab_bytes - 4          # runs past the slab
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_RANGE
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.gate_s_offset = -4
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_RANGE
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.gate_s_offset += 2
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_ALIGNMENT
+
+
+def test_pack_slab_places_sections():
+    H, I = 64, 8
+    L = q.q4moe_canonical_layout(H, I)
+    rng = np.random.default_rng(0)
+    gw = rng.integers(0, 2**32, size=(I, H // 8), dtype=np.uint64).astype(
+        np.uint32)
+    uw = rng.integers(0, 2**32, size=(I, H // 8), dtype=np.uint64).astype(
+        np.uint32)
+    gs = rng.random(I).astype(np.float32)
+    us = rng.random(I).astype(np.float32)
+    slab = np.full(L.slab_bytes, 0xAB, np.uint8)
+    q.q4moe_pack_slab(L, gw, uw, gs, us, slab)
+    wb = I * H // 2
+    assert np.array_equal(slab[:wb].view(np.uint32).reshape(I, -1), gw)
+    assert np.array_equal(slab[wb:2 * wb].view(np.uint32).reshape(I, -1), uw)
+    assert np.array_equal(slab[2 * wb:2 * wb + 4 * I].view(np.float32), gs)
+    assert np.array_equal(
+        slab[2 * wb + 4 * I:2 * wb + 8 * I].view(np.float32), us)
+    assert np.all(slab[2 * wb + 8 * I:] == 0)
+
+
+FAKE = 1 << 40     # an aligned address that is never dereferenced on host
+
+
+def _call(x=FAKE, slabs=None, offs=FAKE, tok=FAKE, M=4, H=64, I=8,
+          out=FAKE, opts=None):
+    lib = q.load()
+    L = q.q4moe_canonical_layout(64, 8)
+    s = slabs if slabs is not None else q.make_slabs(2, L, base=FAKE)
+    return lib.q4moe_gate_up_swiglu_ex(
+        x, ctypes.byref(s) if s is not False else None, offs, tok, M, H, I,
+        out, None if opts is None else ctypes.byref(opts), None)
+
+
+def test_host_argument_errors():
+    L = q.q4moe_canonical_layout(64, 8)
+    assert _call(slabs=False) == q.ERR_INVALID_ARG
+    assert _call(H=128) == q.ERR_INVALID_ARG               # differs from layout
+    assert _call(M=-1) == q.ERR_INVALID_ARG
+    assert _call(offs=None) == q.ERR_INVALID_ARG
+    assert _call(x=None) == q.ERR_INVALID_ARG
+    assert _call(x=FAKE + 8) == q.ERR_ALIGNMENT            # x not 16-aligned
+    assert _call(slabs=q.make_slabs(2, L, base=FAKE + 64)) == \
+        q.ERR_ALIGNMENT
+    assert _call(slabs=q.make_slabs(2, L, base=FAKE,
+                                    slab_stride=4100)) == q.ERR_ALIGNMENT
+    assert _call(slabs=q.make_slabs(0, L, base=FAKE)) == q.ERR_INVALID_ARG
+    assert _call(slabs=q.make_slabs(q.MAX_EXPERTS + 1, L, base=FAKE)) == \
+        q.ERR_INVALID_ARG
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.up_w_offset = L.slab_bytes
+    assert _call(slabs=q.make_slabs(2, bad, base=FAKE)) == q.ERR_RANGE
+    o = q.q4moe_options_t()
+    o.kernel = 7
+    assert _call(opts=o) == q.ERR_INVALID_ARG
+    assert "options" in q.q4moe_last_error()
+    lib = q.load()
+    assert lib.q4moe_group_rows(FAKE, 4, 0, 8, FAKE, FAKE, FAKE, None) == \
+        q.ERR_INVALID_ARG
+    assert lib.q4moe_group_rows(FAKE, 4, 2, q.MAX_EXPERTS + 1, FAKE, FAKE,
+                                FAKE, None) == q.ERR_INVALID_ARG
+    assert lib.q4moe_debug_tail(None, None, 4, None, None) == \
+        q.ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_device_error():
+    """A call that passes host validation needs a device: without one it
+    returns a CUDA/device error instead of computing anything."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _call()
+    assert rc in (q.ERR_CUDA, q.ERR_DEVICE)

@@ -1,0 +1,239 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every test here runs libq4moe's kernels on cuda:0 and compares with the
+oracle on the same seeded inputs (see tests/parity.py for the tolerance)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import harness as hz
+import oracle
+import parity
+from up_swiglu_gb300 import q4moe as q
+from up_swiglu_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    q.load()                 # builds if missing; raises if it cannot load
+    oracle.build()
+    q.q4moe_device_status(clear=True)
+    yield
+    assert q.q4moe_device_status(clear=True) == 0, "device status raised"
+
+
+def _oracle_full(p, offs, tok):
+    return oracle.gate_up_swiglu(p.x, p.gate_w, p.up_w, p.gate_s, p.up_s,
+                                 offs, tok, want_debug=True)
+
+
+def _run_and_compare(p, kernel=q.KERNEL_AUTO, exact=False, **upload_kw):
+    d = hz.upload(p, **upload_kw)
+    offs_d, tok_d, _ = hz.group(d)
+    offs, tok = offs_d.cpu().numpy(), tok_d.cpu().numpy()
+    o_offs, o_tok, _ = oracle.group_rows(p.topk, p.E)
+    assert np.array_equal(offs, o_offs) and np.array_equal(tok, o_tok)
+    gpu = hz.gate_up(d, offs_d, tok_d, kernel=kernel)
+    orc = _oracle_full(p, offs, tok)
+    gs, us = hz.element_scales(p, offs)
+    stats = parity.compare(gpu, orc, gs, us, p.H, exact=exact)
+    # the plain entry point (no debug outputs) writes the same bits
+    plain = hz.gate_up(d, offs_d, tok_d, kernel=kernel, debug=False)
+    assert np.array_equal(plain["out"], gpu["out"])
+    return stats
+
+
+# ----------------------------------------------------------------- grouping --
+
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (0, 8, 4), (5, 3, 7),
+                                   (1000, 8, 160), (4096, 8, 160),
+                                   (300, 2, 1024), (2047, 1, 3)])
+def test_group_rows_matches_oracle(T, k, E):
+    import torch
+    rng = np.random.default_rng(T + E)
+    topk = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    p = hz.Problem(np.zeros((T, 8), np.uint16), np.zeros((E, 4, 1), np.uint32),
+                   None, None, None, topk)
+    d = hz.DeviceProblem(p, None, None)
+    d.topk = torch.from_numpy(topk).cuda()
+    offs, tok, rop = hz.group(d)
+    o_offs, o_tok, o_rop = oracle.group_rows(topk, E)
+    assert np.array_equal(offs.cpu().numpy(), o_offs)
+    assert np.array_equal(tok.cpu().numpy(), o_tok)
+    assert np.array_equal(rop.cpu().numpy(), o_rop)
+
+
+def test_group_rows_bad_id_sets_status():
+    import torch
+    topk = np.array([[0, 5], [1, -1], [2, 0]], np.int32)
+    p = hz.Problem(np.zeros((3, 8), np.uint16), np.zeros((4, 4, 1), np.uint32),
+                   None, None, None, topk)
+    d = hz.DeviceProblem(p, None, None)
+    d.topk = torch.from_numpy(topk).cuda()
+    offs, tok, rop = hz.group(d)
+    assert q.q4moe_device_status(clear=True) & q.DEV_BAD_EXPERT_ID
+    assert list(offs.cpu().numpy()) == [0, 2, 3, 4, 4]
+    assert list(rop.cpu().numpy()) == [0, -1, 2, -1, 3, 1]
+
+
+# --------------------------------------------------------------------- tail --
+
+def test_tail_exhaustive_bf16():
+    """All 65,536 bf16 gate values (finite), several up values: the device
+    tail equals the oracle's bit for bit (sigmoid, silu and out)."""
+    import torch
+    g = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g = g[((g >> 7) & 0xFF) != 0xFF]
+    for up in (1.0, -3.0, 0.0078125, 250.0):
+        u = np.full(g.shape, syn.f32_to_bf16_bits(np.float32([up]))[0],
+                    np.uint16)
+        gd = torch.from_numpy(g.view(np.int16)).cuda()
+        ud = torch.from_numpy(u.view(np.int16)).cuda()
+        res = torch.empty((g.size, 4), dtype=torch.int16, device="cuda")
+        q.q4moe_debug_tail(gd, ud, g.size, res)
+        r = res.cpu().numpy().view(np.uint16)
+        gf = syn.bf16_bits_to_f32(g)
+        uf = syn.bf16_bits_to_f32(u)
+        t = oracle.tail_array(gf, uf)
+        assert np.array_equal(r[:, 3], g)
+        for col, name in ((0, "sigmoid"), (1, "silu"), (2, "out")):
+            bad = np.flatnonzero(r[:, col] != t[:, col + 2])
+            assert bad.size == 0, f"{name}: {bad.size} differ, e.g. gate " \
+                f"{g[bad[:4]]}"
+
+
+# ------------------------------------------------------- exact integer data --
+
+@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+@pytest.mark.parametrize("E,I,H,T,k", [(1, 256, 512, 1, 1),
+                                       (6, 128, 5120, 9, 3),
+                                       (3, 36, 24, 7, 2)])
+def test_exact_integer_bit_exact(kernel, E, I, H, T, k):
+    p = hz.exact_problem(100 + H, E, I, H, T, k)
+    _run_and_compare(p, kernel=kernel, exact=True)
+
+
+@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+def test_exact_integer_ragged_counts(kernel):
+    counts = [0, 1, 7, 8, 9, 47, 48, 49, 64, 65, 130, 0, 3]
+    p = hz.problem_with_counts(5, counts, 256, 512, exact=True)
+    _run_and_compare(p, kernel=kernel, exact=True)
+
+
+# ----------------------------------------------------- real-valued parity --
+
+def test_parity_single_expert_small_workload():
+    """The 1-expert H=512 I=256 one-token workload, seed 0, all outputs."""
+    w = syn.WORKLOADS["expert1_h512_i256_m1"]
+    g = syn.generate(w)
+    p = hz.Problem(g["x"], g["gate_w"], g["up_w"], g["gate_s"], g["up_s"],
+                   g["topk"])
+    _run_and_compare(p)
+
+
+@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+@pytest.mark.parametrize("E,T,k,routing,x_std", [
+    (16, 12, 8, "uniform", 1.0),      # grouped decode shape, fewer experts
+    (20, 40, 8, "zipf", 1.0),         # skewed verify shape
+    (4, 96, 2, "uniform", 0.5),       # prefill-like rows per expert
+])
+def test_parity_reduced_workloads(kernel, E, T, k, routing, x_std):
+    p = hz.random_problem(7 + T, E, 1536, 5120, T, k, routing, x_std)
+    _run_and_compare(p, kernel=kernel)
+
+
+@pytest.mark.parametrize("counts", [[0, 1, 7, 8, 9, 47, 48, 49, 63, 64, 65,
+                                     129, 200, 257]])
+def test_parity_ragged_rows_per_expert(counts):
+    p = hz.problem_with_counts(9, counts, 256, 512)
+    for kernel in (q.KERNEL_AUTO, q.KERNEL_MATVEC):
+        _run_and_compare(p, kernel=kernel)
+
+
+def test_parity_generic_shapes():
+    """H not a multiple of 32 and tiny I (the pages' minimum rules)."""
+    for (I, H) in ((4, 8), (12, 24), (20, 40)):
+        p = hz.random_problem(I, 3, I, H, 5, 2)
+        _run_and_compare(p)
+
+
+def test_parity_noncanonical_layout_and_pointer_table():
+    p = hz.random_problem(17, 5, 256, 512, 6, 2)
+    I, H = p.I, p.H
+    wb = I * H // 2
+    L = q.q4moe_layout_t()
+    L.hidden_size, L.intermediate_size = H, I
+    # scales first, then up, then gate, with gaps
+    L.up_s_offset = 0
+    L.gate_s_offset = 4096
+    L.up_w_offset = 8192
+    L.gate_w_offset = 8192 + wb + 256
+    L.slab_bytes = (L.gate_w_offset + wb + 4095) // 4096 * 4096
+    _run_and_compare(p, layout=L, stride_pad=8192)
+    _run_and_compare(p, ptr_table=True)
+
+
+def test_max_experts_and_empty_call():
+    import torch
+    p = hz.random_problem(3, q.MAX_EXPERTS, 8, 64, 70, 3)
+    _run_and_compare(p)
+    d = hz.upload(p)
+    offs = torch.zeros(p.E + 1, dtype=torch.int32, device="cuda")
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")[:0]
+    out = torch.full((1, p.I), 7, dtype=torch.int16, device="cuda")
+    q.q4moe_gate_up_swiglu(d.x, d.slabs, offs, tok, 0, p.H, p.I, out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7)          # M = 0 writes nothing
+
+
+# ------------------------------------------------------ device-side checks --
+
+def test_bad_offsets_and_tokens_raise_status():
+    import torch
+    p = hz.random_problem(4, 3, 16, 64, 4, 2)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    q.q4moe_device_status(clear=True)
+    bad = offs.clone()
+    bad[1] = bad[2] + 1                     # decreasing
+    out = torch.full((8, p.I), 5, dtype=torch.int16, device="cuda")
+    q.q4moe_gate_up_swiglu(d.x, d.slabs, bad, tok, 8, p.H, p.I, out)
+    assert q.q4moe_device_status(clear=True) == q.DEV_BAD_ROW_OFFSETS
+    assert torch.all(out == 5)              # nothing written
+    badtok = tok.clone()
+    badtok[3] = p.T + 5
+    hz.gate_up(d, offs, badtok)             # num_tokens = T: checked
+    assert q.q4moe_device_status(clear=True) == q.DEV_BAD_TOKEN
+
+
+def test_misaligned_slab_pointer_raises_status():
+    import torch
+    p = hz.random_problem(8, 2, 16, 64, 3, 1)
+    d = hz.upload(p, ptr_table=True)
+    ptrs = d.keep[-1]
+    ptrs[1] += 64                            # no longer 4096-aligned
+    offs, tok, _ = hz.group(d)
+    hz.gate_up(d, offs, tok)
+    assert q.q4moe_device_status(clear=True) & q.DEV_BAD_SLAB_PTR
+    del torch
+
+
+# ------------------------------------------------------ stream, determinism --
+
+def test_side_stream_and_repeatability():
+    import torch
+    p = hz.random_problem(12, 8, 256, 1024, 20, 4)
+    d = hz.upload(p)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        offs, tok, _ = hz.group(d, stream=s)
+        a = hz.gate_up(d, offs, tok, stream=s)
+        b = hz.gate_up(d, offs, tok, stream=s)
+    assert np.array_equal(a["out"], b["out"])
+    assert np.array_equal(a["gate32"], b["gate32"])

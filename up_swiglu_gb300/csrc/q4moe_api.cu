@@ -1,0 +1,394 @@
+// q4moe_api.cu -- the C ABI: argument validation, the device status word and
+// kernel dispatch.  Validation rules follow the pages' host checks (page 52,
+// streamed-experts.ts, validateCall; page 51, layout.ts, validateRange).
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "q4moe_internal.cuh"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int ok() {
+    t_last_error.clear();
+    return Q4MOE_OK;
+}
+
+int cuda_fail(cudaError_t err, const char *what) {
+    return fail(Q4MOE_ERR_CUDA, "%s: %s (%d)", what, cudaGetErrorString(err),
+                (int)err);
+}
+
+// Device status word: Q4MOE_DEV_* bits raised by kernels that meet
+// inconsistent device-side data.  One per device (a __device__ variable
+// exists once in every device context that loads the library).
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    char why[160] = {0};
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+// Per-device set-up, done on the first call that needs it with that device
+// current: the compute capability check and the status word's address.
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(Q4MOE_ERR_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((err = cudaDeviceGetAttribute(
+                 &major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+                cudaSuccess ||
+            (err = cudaDeviceGetAttribute(
+                 &minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+                cudaSuccess ||
+            (err = cudaDeviceGetAttribute(
+                 &sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(err, "cudaDeviceGetAttribute");
+        d.num_sms = sms;
+        d.supported = (major == 10 && minor == 3);
+        if (!d.supported) {
+            snprintf(d.why, sizeof d.why,
+                     "device %d is sm_%d%d; this library is built for sm_103",
+                     dev, major, minor);
+        } else {
+            void *p = nullptr;
+            err = cudaGetSymbolAddress(&p, g_status_word);
+            if (err != cudaSuccess)
+                return cuda_fail(err, "cudaGetSymbolAddress(status word)");
+            d.status = static_cast<unsigned int *>(p);
+        }
+        d.ready = true;
+    }
+    if (!d.supported)
+        return fail(Q4MOE_ERR_DEVICE, "%s", d.why);
+    *out = &d;
+    return Q4MOE_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+int check_range(int64_t off, int64_t len, int64_t slab_bytes,
+                const char *what) {
+    if (off < 0)
+        return fail(Q4MOE_ERR_RANGE, "%s offset must be non-negative", what);
+    if (len < 0 || off > slab_bytes || len > slab_bytes - off)
+        return fail(Q4MOE_ERR_RANGE, "%s exceed the expert slab", what);
+    return Q4MOE_OK;
+}
+
+int validate_layout(const q4moe_layout_t *L) {
+    if (L == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
+    const int64_t H = L->hidden_size, I = L->intermediate_size;
+    if (H <= 0 || I <= 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "hidden and intermediate sizes must be positive");
+    if (H % 8 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "Q4 hidden size must be divisible by 8");
+    if (I % 4 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "intermediate size must be divisible by 4");
+    if (H > (INT64_C(1) << 24) || I > (INT64_C(1) << 24))
+        return fail(Q4MOE_ERR_INVALID_ARG, "dimensions above 2^24");
+    if (L->slab_bytes <= 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "slab bytes must be positive");
+    int rc;
+    const int64_t wbytes = I * (H / 2), sbytes = I * 4;
+    if ((rc = check_range(L->gate_w_offset, wbytes, L->slab_bytes,
+                          "gate weights")) ||
+        (rc = check_range(L->up_w_offset, wbytes, L->slab_bytes,
+                          "up weights")) ||
+        (rc = check_range(L->gate_s_offset, sbytes, L->slab_bytes,
+                          "gate scales")) ||
+        (rc = check_range(L->up_s_offset, sbytes, L->slab_bytes,
+                          "up scales")))
+        return rc;
+    if ((L->gate_w_offset | L->up_w_offset | L->gate_s_offset |
+         L->up_s_offset) % 4 != 0)
+        return fail(Q4MOE_ERR_ALIGNMENT,
+                    "slab sections must start on 4-byte boundaries");
+    return Q4MOE_OK;
+}
+
+std::atomic<int64_t> g_launches{0};
+
+}  // namespace
+
+namespace q4moe {
+void count_launches(int n) { g_launches.fetch_add(n); }
+}  // namespace q4moe
+
+extern "C" {
+
+int64_t q4moe_launch_count(void) { return g_launches.load(); }
+
+int q4moe_abi_version(void) { return Q4MOE_ABI_VERSION; }
+
+const char *q4moe_last_error(void) { return t_last_error.c_str(); }
+
+int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout) {
+    if (layout == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
+    q4moe_layout_t L{};
+    L.hidden_size = H;
+    L.intermediate_size = I;
+    if (H <= 0 || I <= 0 || H % 8 != 0 || I % 4 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "need H > 0, H %% 8 == 0, I > 0, I %% 4 == 0");
+    if (H > (INT64_C(1) << 24) || I > (INT64_C(1) << 24))
+        return fail(Q4MOE_ERR_INVALID_ARG, "dimensions above 2^24");
+    const int64_t wbytes = I * (H / 2);
+    L.gate_w_offset = 0;
+    L.up_w_offset = wbytes;
+    L.gate_s_offset = 2 * wbytes;
+    L.up_s_offset = 2 * wbytes + 4 * I;
+    const int64_t used = 2 * wbytes + 8 * I;
+    L.slab_bytes = (used + Q4MOE_SLAB_ALIGNMENT - 1) /
+                   Q4MOE_SLAB_ALIGNMENT * Q4MOE_SLAB_ALIGNMENT;
+    *layout = L;
+    return ok();
+}
+
+int q4moe_validate_layout(const q4moe_layout_t *layout) {
+    const int rc = validate_layout(layout);
+    return rc ? rc : ok();
+}
+
+int q4moe_pack_slab(const q4moe_layout_t *L, const uint32_t *gate_w,
+                    const uint32_t *up_w, const float *gate_s,
+                    const float *up_s, void *slab_host) {
+    int rc = validate_layout(L);
+    if (rc)
+        return rc;
+    if (!gate_w || !up_w || !gate_s || !up_s || !slab_host)
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    const int64_t H = L->hidden_size, I = L->intermediate_size;
+    uint8_t *s = static_cast<uint8_t *>(slab_host);
+    memset(s, 0, (size_t)L->slab_bytes);
+    memcpy(s + L->gate_w_offset, gate_w, (size_t)(I * (H / 2)));
+    memcpy(s + L->up_w_offset, up_w, (size_t)(I * (H / 2)));
+    memcpy(s + L->gate_s_offset, gate_s, (size_t)(I * 4));
+    memcpy(s + L->up_s_offset, up_s, (size_t)(I * 4));
+    return ok();
+}
+
+int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
+                     int32_t E, int32_t *row_offsets, int32_t *token_of_row,
+                     int32_t *row_of_pair, cudaStream_t stream) {
+    if (T < 0 || k <= 0 || E <= 0 || E > Q4MOE_MAX_EXPERTS)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "need T >= 0, k >= 1, 1 <= E <= %d", Q4MOE_MAX_EXPERTS);
+    if (T > (int64_t)(INT32_MAX - 1024) / k)
+        return fail(Q4MOE_ERR_INVALID_ARG, "T*k must stay below 2^31");
+    if (row_offsets == nullptr || (T > 0 && (!topk_ids || !token_of_row ||
+                                             !row_of_pair)))
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc)
+        return rc;
+    cudaError_t err =
+        q4moe::launch_group_rows(topk_ids, T * k, k, E, row_offsets,
+                                 token_of_row, row_of_pair, d->status, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "group_rows launch");
+    return ok();
+}
+
+int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
+                            const int32_t *row_offsets,
+                            const int32_t *token_of_row, int64_t M, int64_t H,
+                            int64_t I, void *out, const q4moe_options_t *opts,
+                            cudaStream_t stream) {
+    if (slabs == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "expert_slabs is null");
+    int rc = validate_layout(&slabs->layout);
+    if (rc)
+        return rc;
+    const q4moe_layout_t &L = slabs->layout;
+    if (H != L.hidden_size || I != L.intermediate_size)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "H, I (%lld, %lld) differ from the slab layout's "
+                    "(%lld, %lld)", (long long)H, (long long)I,
+                    (long long)L.hidden_size,
+                    (long long)L.intermediate_size);
+    if (slabs->num_experts <= 0 || slabs->num_experts > Q4MOE_MAX_EXPERTS)
+        return fail(Q4MOE_ERR_INVALID_ARG, "num_experts must be in 1..%d",
+                    Q4MOE_MAX_EXPERTS);
+    if (slabs->reserved0 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "reserved field must be 0");
+    if (M < 0 || M > INT32_MAX)
+        return fail(Q4MOE_ERR_INVALID_ARG, "M must be in 0..2^31-1");
+    if (M > 0 && M * I > (INT64_C(1) << 40))
+        return fail(Q4MOE_ERR_INVALID_ARG, "output too large");
+    if (row_offsets == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "row_offsets_per_expert is null");
+    if (M > 0 && (x == nullptr || token_of_row == nullptr || out == nullptr))
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(x, 16))
+        return fail(Q4MOE_ERR_ALIGNMENT, "x must be 16-byte aligned");
+    if (!aligned(out, 2))
+        return fail(Q4MOE_ERR_ALIGNMENT, "out must be 2-byte aligned");
+    if (slabs->slab_ptrs == nullptr) {
+        if (slabs->base == nullptr)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "slab base is null and no pointer table given");
+        if (!aligned(slabs->base, Q4MOE_SLAB_ALIGNMENT))
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab base must be %d-byte aligned",
+                        Q4MOE_SLAB_ALIGNMENT);
+        if (slabs->slab_stride % Q4MOE_SLAB_ALIGNMENT != 0 ||
+            (slabs->num_experts > 1 && slabs->slab_stride < L.slab_bytes) ||
+            slabs->slab_stride < 0)
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab stride must be a multiple of %d and at least "
+                        "the slab size", Q4MOE_SLAB_ALIGNMENT);
+    } else if (!aligned(slabs->slab_ptrs, 8)) {
+        return fail(Q4MOE_ERR_ALIGNMENT, "slab pointer table misaligned");
+    }
+    q4moe_options_t o{};
+    if (opts != nullptr)
+        o = *opts;
+    if (o.reserved0 != 0 || o.kernel < Q4MOE_KERNEL_AUTO ||
+        o.kernel > Q4MOE_KERNEL_GEMM || o.num_tokens < 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
+    if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
+        return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
+                                         "aligned");
+
+    DeviceInfo *d = nullptr;
+    rc = device_info(&d);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return ok();
+
+    q4moe::GateUpArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.base = static_cast<const uint8_t *>(slabs->base);
+    a.stride = slabs->slab_stride;
+    a.slab_ptrs = reinterpret_cast<const uint8_t *const *>(slabs->slab_ptrs);
+    a.gate_w_off = L.gate_w_offset;
+    a.up_w_off = L.up_w_offset;
+    a.gate_s_off = L.gate_s_offset;
+    a.up_s_off = L.up_s_offset;
+    a.row_offsets = row_offsets;
+    a.token_of_row = token_of_row;
+    a.M = M;
+    a.H = H;
+    a.I = I;
+    a.T = o.num_tokens;
+    a.E = slabs->num_experts;
+    a.out = static_cast<uint16_t *>(out);
+    a.gate_f32 = o.gate_f32;
+    a.up_f32 = o.up_f32;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
+
+    const bool gemm_ok = q4moe::gemm_supported(H, I, a);
+    int32_t matvec_max = INT32_MAX;
+    if (o.kernel == Q4MOE_KERNEL_GEMM) {
+        if (!gemm_ok)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "the tensor-core GEMM needs H %% 64 == 0, I %% 128 "
+                        "== 0 and 16-byte aligned slab sections");
+        matvec_max = 0;
+    } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
+        matvec_max = 48;
+    }
+    a.matvec_max_rows = matvec_max;
+
+    cudaError_t err = cudaSuccess;
+    if (matvec_max > 0 && (err = q4moe::launch_matvec(a, stream)) !=
+                              cudaSuccess)
+        return cuda_fail(err, "matvec launch");
+    // every expert has at most M rows: no GEMM work when M <= matvec_max
+    if (matvec_max < M && (err = q4moe::launch_gemm(a, stream)) !=
+                              cudaSuccess)
+        return cuda_fail(err, "gemm launch");
+    return ok();
+}
+
+int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *slabs,
+                         const int32_t *row_offsets,
+                         const int32_t *token_of_row, int64_t M, int64_t H,
+                         int64_t I, void *out, cudaStream_t stream) {
+    return q4moe_gate_up_swiglu_ex(x, slabs, row_offsets, token_of_row, M, H,
+                                   I, out, nullptr, stream);
+}
+
+int q4moe_device_status(cudaStream_t stream, uint32_t *flags, int clear) {
+    if (flags == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "flags is null");
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc)
+        return rc;
+    cudaError_t err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "cudaStreamSynchronize");
+    unsigned int v = 0;
+    err = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "reading the status word");
+    if (clear) {
+        const unsigned int zero = 0;
+        err = cudaMemcpy(d->status, &zero, sizeof zero,
+                         cudaMemcpyHostToDevice);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "clearing the status word");
+    }
+    *flags = v;
+    if (v != 0)
+        return fail(Q4MOE_ERR_DEVICE_DATA, "device status 0x%x", v);
+    return ok();
+}
+
+int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
+                     int64_t n, uint16_t *res, cudaStream_t stream) {
+    if (n < 0 || (n > 0 && (!gate_bf16 || !up_bf16 || !res)))
+        return fail(Q4MOE_ERR_INVALID_ARG, "bad arguments");
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc)
+        return rc;
+    cudaError_t err = q4moe::launch_debug_tail(gate_bf16, up_bf16, n, res,
+                                               stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "debug tail launch");
+    return ok();
+}
+
+}  // extern "C"

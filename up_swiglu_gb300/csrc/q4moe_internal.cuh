@@ -1,0 +1,142 @@
+// q4moe_internal.cuh -- launch arguments and device helpers shared by the
+// CUDA translation units of libq4moe (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "q4moe.h"
+
+namespace q4moe {
+
+// Everything a gate/up kernel needs, resolved and validated on the host.
+struct GateUpArgs {
+    const uint16_t *x;           // bf16 [T][H]
+    const uint8_t *base;         // slab of expert e at base + e * stride ...
+    int64_t stride;
+    const uint8_t *const *slab_ptrs;  // ... or at slab_ptrs[e] when non-null
+    int64_t gate_w_off, up_w_off, gate_s_off, up_s_off;
+    const int32_t *row_offsets;  // [E+1]
+    const int32_t *token_of_row; // [M]
+    int64_t M, H, I, T;          // T <= 0: token indices unchecked
+    int32_t E;
+    uint16_t *out;               // bf16 [M][I]
+    float *gate_f32;             // optional [M][I]
+    float *up_f32;               // optional [M][I]
+    unsigned int *status;        // device status word (Q4MOE_DEV_* bits)
+    int32_t matvec_max_rows;     // experts with more rows go to the GEMM
+    int32_t num_sms;
+};
+
+// Host-side count of kernel launches (q4moe_launch_count).
+void count_launches(int n);
+
+cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s);
+cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
+bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);
+cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
+                              int32_t E, int32_t *row_offsets,
+                              int32_t *token_of_row, int32_t *row_of_pair,
+                              unsigned int *status, cudaStream_t s);
+cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
+                              int64_t n, uint16_t *res, cudaStream_t s);
+
+// ------------------------------------------------------------------------
+// bf16 helpers.  Rounding: nearest, ties to even, on the f32 bit pattern
+// (page 54, codebook.ts, trellis_bf16); every value reaching it is finite.
+__device__ __forceinline__ uint16_t bf16_rne(float v) {
+    uint32_t u = __float_as_uint(v);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float bf16_f32(uint32_t b16) {
+    return __uint_as_float(b16 << 16);
+}
+
+// The page's f32 sigmoid chain 1 / (1 + exp(-g)) for a bf16 value g
+// (page 52, GATE_UP_SOURCE tail), with IEEE add and divide and no flush to
+// zero.  expf is within 2 ulp of exp; the result can only round to a
+// different bf16 than the correctly rounded chain when it lies within a few
+// f32 ulp of a bf16 rounding midpoint, and there the chain is recomputed
+// from the double-precision exponential.
+__device__ __forceinline__ float sigmoid_chain(float g) {
+    float e = expf(-g);
+    float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+    const int lo = (int)(__float_as_uint(s) & 0xFFFFu);
+    if (abs(lo - 0x8000) <= 32) {
+        e = __double2float_rn(exp(-(double)g));
+        s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+    }
+    return s;
+}
+
+// gateT, upT -> out (bf16 bits).  sig and silu are also returned.
+__device__ __forceinline__ uint16_t swiglu_tail_bits(uint16_t gT, uint16_t uT,
+                                                     uint16_t *sigT,
+                                                     uint16_t *siluT) {
+    const float g = bf16_f32(gT);
+    const uint16_t s = bf16_rne(sigmoid_chain(g));
+    const uint16_t si = bf16_rne(__fmul_rn(g, bf16_f32(s)));
+    *sigT = s;
+    *siluT = si;
+    return bf16_rne(__fmul_rn(bf16_f32(si), bf16_f32(uT)));
+}
+
+__device__ __forceinline__ uint16_t swiglu_out(float gate32, float up32) {
+    uint16_t s, si;
+    return swiglu_tail_bits(bf16_rne(gate32), bf16_rne(up32), &s, &si);
+}
+
+// Slab of expert e; null (and a status bit) for a misaligned table entry.
+__device__ __forceinline__ const uint8_t *expert_slab(const GateUpArgs &a,
+                                                      int e) {
+    if (a.slab_ptrs == nullptr)
+        return a.base + (int64_t)e * a.stride;
+    const uint8_t *p = a.slab_ptrs[e];
+    if (p == nullptr ||
+        (reinterpret_cast<uintptr_t>(p) & (Q4MOE_SLAB_ALIGNMENT - 1)) != 0) {
+        atomicOr(a.status, Q4MOE_DEV_BAD_SLAB_PTR);
+        return nullptr;
+    }
+    return p;
+}
+
+// Stage row_offsets[0..E] in shared memory and check them (0 first, M last,
+// never decreasing).  Every thread of the block must call it; returns false
+// (and block 0 raises the status bit) when they are inconsistent.
+__device__ __forceinline__ bool stage_row_offsets(const GateUpArgs &a,
+                                                  int32_t *s_off) {
+    __shared__ int s_bad;
+    if (threadIdx.x == 0)
+        s_bad = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) {
+        const int32_t v = a.row_offsets[e];
+        s_off[e] = v;
+        bool bad = (e == 0 && v != 0) || (e == a.E && v != a.M) || v < 0 ||
+                   v > a.M;
+        if (e > 0 && a.row_offsets[e - 1] > v)
+            bad = true;
+        if (bad)
+            s_bad = 1;
+    }
+    __syncthreads();
+    const bool ok = s_bad == 0;
+    if (!ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+        blockIdx.z == 0)
+        atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
+    return ok;
+}
+
+// Token of grouped row p, or -1 (and a status bit) when out of range.
+__device__ __forceinline__ int64_t row_token(const GateUpArgs &a, int64_t p) {
+    const int32_t t = a.token_of_row[p];
+    if (t < 0 || (a.T > 0 && t >= a.T)) {
+        atomicOr(a.status, Q4MOE_DEV_BAD_TOKEN);
+        return -1;
+    }
+    return t;
+}
+
+}  // namespace q4moe

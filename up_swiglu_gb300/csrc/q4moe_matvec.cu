@@ -1,0 +1,139 @@
+// q4moe_matvec.cu -- grouped Q4 gate/up + SwiGLU matvec for experts with few
+// rows (decode / speculative verify widths).
+//
+// Generic version: any H % 8 == 0, I % 4 == 0.  One warp owns one output
+// row i of one expert and up to 8 of the expert's grouped rows at a time,
+// so every packed word it loads serves all of them (the shared-row idea of
+// the pages' trellis GATEUP_SHARED_M_SOURCE, page 57, gate-up.ts); lanes
+// stride over the row's words as the page's GATE_UP_SOURCE does (page 52),
+// accumulate gate and up in f32, and meet in a shuffle reduction.
+#include "q4moe_internal.cuh"
+
+namespace q4moe {
+namespace {
+
+constexpr int kWarpsPerBlock = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerBlock = kWarpsPerBlock * kRowsPerWarp;
+constexpr int kChunk = 8;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+matvec_generic_kernel(GateUpArgs a) {
+    __shared__ int32_t s_off[Q4MOE_MAX_EXPERTS + 1];
+    if (!stage_row_offsets(a, s_off))
+        return;
+    const int e = blockIdx.y;
+    const int32_t r0 = s_off[e], r1 = s_off[e + 1];
+    const int32_t rows = r1 - r0;
+    if (rows == 0 || rows > a.matvec_max_rows)
+        return;
+    const uint8_t *slab = expert_slab(a, e);
+    if (slab == nullptr)
+        return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t words = a.H / 8;
+    const float *gs = reinterpret_cast<const float *>(slab + a.gate_s_off);
+    const float *us = reinterpret_cast<const float *>(slab + a.up_s_off);
+
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int64_t i = (int64_t)blockIdx.x * kRowsPerBlock +
+                          warp * kRowsPerWarp + rr;
+        if (i >= a.I)
+            break;
+        const uint32_t *gw = reinterpret_cast<const uint32_t *>(
+                                 slab + a.gate_w_off) + i * words;
+        const uint32_t *uw = reinterpret_cast<const uint32_t *>(
+                                 slab + a.up_w_off) + i * words;
+        for (int32_t p0 = r0; p0 < r1; p0 += kChunk) {
+            const int nt = min(kChunk, r1 - p0);
+            int64_t tok[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j)
+                tok[j] = j < nt ? row_token(a, p0 + j) : -1;
+            float ag[kChunk], au[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j)
+                ag[j] = au[j] = 0.0f;
+            for (int64_t w = lane; w < words; w += 32) {
+                const uint32_t g = gw[w], u = uw[w];
+#pragma unroll
+                for (int j = 0; j < kChunk; ++j) {
+                    if (tok[j] < 0)
+                        continue;
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(
+                        a.x + tok[j] * a.H + w * 8);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int place = 0; place < 8; ++place) {
+                        const float xf = bf16_f32(
+                            (xw[place >> 1] >> (16 * (place & 1))) & 0xFFFFu);
+                        const float wg =
+                            (float)((int)((g >> (4 * place)) & 0xFu) - 8);
+                        const float wu =
+                            (float)((int)((u >> (4 * place)) & 0xFu) - 8);
+                        ag[j] = __fmaf_rn(wg, xf, ag[j]);
+                        au[j] = __fmaf_rn(wu, xf, au[j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const float G = warp_sum(ag[j]);
+                const float U = warp_sum(au[j]);
+                if (lane == j && tok[j] >= 0) {
+                    const float g32 = __fmul_rn(G, gs[i]);
+                    const float u32 = __fmul_rn(U, us[i]);
+                    const int64_t o = (int64_t)(p0 + j) * a.I + i;
+                    a.out[o] = swiglu_out(g32, u32);
+                    if (a.gate_f32)
+                        a.gate_f32[o] = g32;
+                    if (a.up_f32)
+                        a.up_f32[o] = u32;
+                }
+            }
+        }
+    }
+}
+
+__global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
+                                  int64_t n, uint16_t *res) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const uint16_t gT = bf16_rne(bf16_f32(g[j]));
+        uint16_t s, si;
+        const uint16_t o = swiglu_tail_bits(gT, u[j], &s, &si);
+        res[4 * j + 0] = s;
+        res[4 * j + 1] = si;
+        res[4 * j + 2] = o;
+        res[4 * j + 3] = gT;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
+    const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),
+                    (unsigned)a.E);
+    matvec_generic_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
+                              uint16_t *res, cudaStream_t s) {
+    if (n == 0)
+        return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+    debug_tail_kernel<<<blocks, 256, 0, s>>>(g, u, n, res);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace q4moe
