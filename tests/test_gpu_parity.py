@@ -110,16 +110,24 @@ def test_tail_exhaustive_bf16():
 
 # ------------------------------------------------------- exact integer data --
 
-@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+KERNELS = [q.KERNEL_AUTO, q.KERNEL_MATVEC, q.KERNEL_GEMM]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("E,I,H,T,k", [(1, 256, 512, 1, 1),
                                        (6, 128, 5120, 9, 3),
+                                       (2, 384, 1024, 300, 2),
                                        (3, 36, 24, 7, 2)])
 def test_exact_integer_bit_exact(kernel, E, I, H, T, k):
     p = hz.exact_problem(100 + H, E, I, H, T, k)
+    if kernel == q.KERNEL_GEMM and (H % 64 or I % 128):
+        with pytest.raises(q.Q4moeError):
+            _run_and_compare(p, kernel=kernel, exact=True)
+        return
     _run_and_compare(p, kernel=kernel, exact=True)
 
 
-@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_exact_integer_ragged_counts(kernel):
     counts = [0, 1, 7, 8, 9, 47, 48, 49, 64, 65, 130, 0, 3]
     p = hz.problem_with_counts(5, counts, 256, 512, exact=True)
@@ -137,7 +145,7 @@ def test_parity_single_expert_small_workload():
     _run_and_compare(p)
 
 
-@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("E,T,k,routing,x_std", [
     (16, 12, 8, "uniform", 1.0),      # grouped decode shape, fewer experts
     (20, 40, 8, "zipf", 1.0),         # skewed verify shape
@@ -152,7 +160,7 @@ def test_parity_reduced_workloads(kernel, E, T, k, routing, x_std):
                                      129, 200, 257]])
 def test_parity_ragged_rows_per_expert(counts):
     p = hz.problem_with_counts(9, counts, 256, 512)
-    for kernel in (q.KERNEL_AUTO, q.KERNEL_MATVEC):
+    for kernel in KERNELS:
         _run_and_compare(p, kernel=kernel)
 
 
@@ -177,6 +185,8 @@ def test_parity_noncanonical_layout_and_pointer_table():
     L.slab_bytes = (L.gate_w_offset + wb + 4095) // 4096 * 4096
     _run_and_compare(p, layout=L, stride_pad=8192)
     _run_and_compare(p, ptr_table=True)
+    _run_and_compare(p, kernel=q.KERNEL_GEMM, layout=L, stride_pad=8192)
+    _run_and_compare(p, kernel=q.KERNEL_GEMM, ptr_table=True)
 
 
 def test_max_experts_and_empty_call():

@@ -1,14 +1,508 @@
-// q4moe_gemm.cu -- tensor-core grouped GEMM for experts with many rows
-// (placeholder until the tcgen05 kernel lands: reports itself unsupported,
-// so every expert runs on the matvec).
+// q4moe_gemm.cu -- grouped Q4 gate/up + SwiGLU on the tcgen05 tensor core,
+// for experts with many rows (prefill).
+//
+// The pages give the fused gate/up/SwiGLU as a matvec (page 52,
+// streamed-experts.ts, GATE_UP_SOURCE) and as an 8x8 simdgroup-matrix form
+// for up to 8 rows (page 57, trellis/gate-up-mma.ts); this is the
+// large-batch form of the same arithmetic for sm_103a:
+//
+//  tile   = 128 intermediate rows (i) of one expert x up to 256 of the
+//           expert's grouped rows (tokens); both projections of the tile
+//           share the token operand;
+//  A      = the gate (and the up) weights of the tile's rows, dequantised
+//           (nibble - 8, exact in bf16) into shared memory in the 128-byte
+//           swizzled K-major layout, 64 K per pipeline stage;
+//  B      = the tile's token rows of x, gathered row by row with cp.async
+//           into the same layout;
+//  D      = two f32 accumulators in tensor memory (gate: columns 0..N-1,
+//           up: columns 256..256+N-1), lane = intermediate row;
+//  tail   = row scales, bf16 rounding and the SwiGLU chain, per element, as
+//           in the matvec.
+//
+// Warp roles (512 threads, one CTA per SM, persistent over tiles):
+//   0-7   epilogue (warp w reads TMEM lanes 32*(w%4)..; w/4 picks the
+//         16-column chunks it handles)
+//   8     TMEM allocation and the single thread that issues the MMAs
+//   9-12  weight dequantisation (one A row of gate and of up per thread)
+//   13-15 token gather (cp.async)
+// Every wait on an mbarrier is bounded; on time-out the CTA raises
+// Q4MOE_DEV_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include "q4moe_internal.cuh"
+#include "q4moe_sm100.cuh"
 
 namespace q4moe {
+namespace {
 
-bool gemm_supported(int64_t, int64_t, const GateUpArgs &) { return false; }
+using namespace sm100;
 
-cudaError_t launch_gemm(const GateUpArgs &, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int BM = 128;                      // intermediate rows per tile
+constexpr int BK = 64;                       // K per stage
+constexpr int NMAX = 256;                    // token rows per tile
+constexpr int STAGES = 3;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = NMAX * BK * 2;       // 32 KB
+constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr int kThreads = 512;
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kDeqWarp0 = 9;
+constexpr int kDeqWarps = 4;
+constexpr int kGatWarp0 = 13;
+constexpr int kGatWarps = 3;
+constexpr int kGatThreads = kGatWarps * 32;
+constexpr int kGatItems = (NMAX * 8 + kGatThreads - 1) / kGatThreads;
+constexpr int kPrefetch = 4;                 // k-blocks of weights in flight
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kUpCol = 256;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+
+struct Ctl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full;
+    uint64_t tmem_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int bad_offsets;
+};
+
+constexpr size_t smem_bytes(int E) {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl) +
+           2 * sizeof(int32_t) * (size_t)(E + 1) + 16;
+}
+
+struct Tile {
+    int e;          // expert
+    int iblk;       // block of 128 intermediate rows
+    int row0;       // first grouped row of the tile
+    int nvalid;     // grouped rows in the tile
+    int n;          // nvalid rounded up to 16 (the MMA's N)
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Rows of expert e are split into ceil(n/256) chunks of equal size rounded
+// up to 16.
+__device__ __forceinline__ int chunk_rows(int n_e) {
+    const int nch = ceil_div(n_e, NMAX);
+    return ceil_div(ceil_div(n_e, nch), 16) * 16;
+}
+
+__device__ __forceinline__ Tile tile_of(int t, const int32_t *off,
+                                        const int32_t *pre, int E, int IB) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    Tile ti;
+    ti.e = lo;
+    const int local = t - pre[lo];
+    const int chunk = local / IB;
+    ti.iblk = local - chunk * IB;
+    const int n_e = off[lo + 1] - off[lo];
+    const int cs = chunk_rows(n_e);
+    ti.row0 = off[lo] + chunk * cs;
+    ti.nvalid = min(cs, n_e - chunk * cs);
+    ti.n = ceil_div(ti.nvalid, 16) * 16;
+    return ti;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and, the first time,
+// raises the status bit) once the CTA has aborted or the wait ran out.
+__device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
+                                        volatile int *abort,
+                                        unsigned int *status) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (globaltimer_ns() - t0 > kTimeoutNs) {
+                if (atomicExch((int *)abort, 1) == 0)
+                    atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// One packed word (8 nibbles, K order) -> 8 bf16 (nibble - 8) in K order:
+// each output pair (2j, 2j+1) is byte j of the word split into its two
+// nibbles, placed in the low mantissa bits of 128.0 (0x4300) and then
+// reduced by 136 (exact: the results are the integers -8..7).
+__device__ __forceinline__ uint4 dequant_word(uint32_t w) {
+    const uint32_t ws = w >> 4;
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t v =
+            (__byte_perm(w, ws, (uint32_t)(j | ((4 + j) << 8))) &
+             0x000F000Fu) | 0x43004300u;
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v);
+        const __nv_bfloat162 k136 =
+            __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x4308),
+                               __ushort_as_bfloat16((unsigned short)0x4308));
+        b = __hsub2(b, k136);
+        r[j] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
+// K-major tile.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tcgen05_kernel(GateUpArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)STAGES * STAGE_BYTES);
+    int32_t *s_off = reinterpret_cast<int32_t *>(ctl + 1);
+    int32_t *s_pre = s_off + (a.E + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = a.E;
+    const int IB = (int)(a.I / BM);
+    const int KB = (int)(a.H / BK);
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&ctl->full[s], kDeqWarps + kGatWarps);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->tmem_full, 1);
+        mbar_init(&ctl->tmem_empty, kEpiWarps);
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        ctl->bad_offsets = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    // stage and check the row offsets
+    for (int e = tid; e <= E; e += kThreads) {
+        const int32_t v = a.row_offsets[e];
+        s_off[e] = v;
+        if ((e == 0 && v != 0) || (e == E && v != a.M) || v < 0 || v > a.M ||
+            (e > 0 && a.row_offsets[e - 1] > v))
+            ctl->bad_offsets = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool offsets_ok = ctl->bad_offsets == 0;
+    if (!offsets_ok && tid == 0 && blockIdx.x == 0)
+        atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
+    // tiles per expert (experts above the matvec's row limit), prefix sums
+    if (warp == 0 && offsets_ok) {
+        const int per = ceil_div(E, 32);
+        const int e0 = lane * per;
+        int sum = 0;
+        for (int e = e0; e < min(E, e0 + per); ++e) {
+            const int n_e = s_off[e + 1] - s_off[e];
+            sum += (n_e > a.matvec_max_rows && n_e > 0)
+                       ? IB * ceil_div(n_e, NMAX) : 0;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += v;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < min(E, e0 + per); ++e) {
+            s_pre[e] = run;
+            const int n_e = s_off[e + 1] - s_off[e];
+            run += (n_e > a.matvec_max_rows && n_e > 0)
+                       ? IB * ceil_div(n_e, NMAX) : 0;
+        }
+        if (lane == 31)
+            s_pre[E] = incl;
+    }
+    __syncthreads();
+    const int ntiles = offsets_ok ? s_pre[E] : 0;
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort = &ctl->abort;
+    const uint32_t stage0 = smem_u32(stages);
+
+    if (warp >= kGatWarp0) {
+        // ---------------------------------------------------- token gather
+        const int j = tid - kGatWarp0 * 32;
+        uint32_t g = 0;
+        bool pending = false;
+        for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+            const Tile ti = tile_of(t, s_off, s_pre, E, IB);
+            // per item: token row (>= 0), -1 zero fill, -2 nothing to copy
+            int32_t tokm[kGatItems];
+#pragma unroll
+            for (int m = 0; m < kGatItems; ++m) {
+                const int f = j + kGatThreads * m;
+                const int n = f >> 3;
+                tokm[m] = -2;
+                if (n < ti.n) {
+                    tokm[m] = -1;
+                    if (n < ti.nvalid) {
+                        const int64_t tok = row_token(a, ti.row0 + n);
+                        if (tok >= 0)
+                            tokm[m] = (int32_t)tok;
+                    }
+                }
+            }
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb, ++g) {
+                const uint32_t s = g % STAGES;
+                if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1, abort,
+                                a.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bdst = stage0 + s * STAGE_BYTES + 2 * A_BYTES;
+#pragma unroll
+                for (int m = 0; m < kGatItems; ++m) {
+                    if (tokm[m] == -2)
+                        continue;
+                    const int f = j + kGatThreads * m;
+                    const uint32_t dst = bdst + sw128_offset(f >> 3, f & 7);
+                    if (tokm[m] >= 0)
+                        cp_async_16(dst,
+                                    a.x + (int64_t)tokm[m] * a.H + (f & 7) * 8 +
+                                        kb * BK,
+                                    16);
+                    else
+                        cp_async_16(dst, a.x, 0);
+                }
+                cp_async_commit();
+                if (pending) {
+                    cp_async_wait<1>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&ctl->full[(g - 1) % STAGES]);
+                }
+                pending = true;
+            }
+            if (!ok)
+                break;
+        }
+        cp_async_wait<0>();
+        if (pending && !*abort) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ctl->full[(g - 1) % STAGES]);
+        }
+    } else if (warp >= kDeqWarp0) {
+        // ------------------------------------------- weight dequantisation
+        const int r = tid - kDeqWarp0 * 32;          // A row 0..127
+        uint32_t g = 0;
+        for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+            const Tile ti = tile_of(t, s_off, s_pre, E, IB);
+            const uint8_t *slab = expert_slab(a, ti.e);
+            const int64_t row = (int64_t)ti.iblk * BM + r;
+            const uint4 *gp = slab ? reinterpret_cast<const uint4 *>(
+                                         slab + a.gate_w_off + row * (a.H / 2))
+                                   : nullptr;
+            const uint4 *up = slab ? reinterpret_cast<const uint4 *>(
+                                         slab + a.up_w_off + row * (a.H / 2))
+                                   : nullptr;
+            uint4 ring[kPrefetch][4];
+#pragma unroll
+            for (int d = 0; d < kPrefetch; ++d) {
+                if (d < KB && slab) {
+                    ring[d][0] = __ldg(gp + 2 * d);
+                    ring[d][1] = __ldg(gp + 2 * d + 1);
+                    ring[d][2] = __ldg(up + 2 * d);
+                    ring[d][3] = __ldg(up + 2 * d + 1);
+                } else {
+                    ring[d][0] = ring[d][1] = ring[d][2] = ring[d][3] =
+                        make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
+                                   0x88888888u);
+                }
+            }
+            bool ok = true;
+            for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+#pragma unroll
+                for (int d = 0; d < kPrefetch; ++d) {
+                    const int kb = kb0 + d;
+                    if (kb >= KB)
+                        break;
+                    const uint32_t s = g % STAGES;
+                    if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1,
+                                    abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *ag = stages + (size_t)s * STAGE_BYTES;
+                    uint8_t *au = ag + A_BYTES;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t wg =
+                            reinterpret_cast<const uint32_t *>(
+                                &ring[d][c >> 2])[c & 3];
+                        const uint32_t wu =
+                            reinterpret_cast<const uint32_t *>(
+                                &ring[d][2 + (c >> 2)])[c & 3];
+                        *reinterpret_cast<uint4 *>(ag + sw128_offset(r, c)) =
+                            dequant_word(wg);
+                        *reinterpret_cast<uint4 *>(au + sw128_offset(r, c)) =
+                            dequant_word(wu);
+                    }
+                    const int kn = kb + kPrefetch;
+                    if (kn < KB && slab) {
+                        ring[d][0] = __ldg(gp + 2 * kn);
+                        ring[d][1] = __ldg(gp + 2 * kn + 1);
+                        ring[d][2] = __ldg(up + 2 * kn);
+                        ring[d][3] = __ldg(up + 2 * kn + 1);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&ctl->full[s]);
+                    ++g;
+                }
+            }
+            if (!ok)
+                break;
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            uint32_t g = 0, it = 0;
+            bool issued = false;
+            for (int t = blockIdx.x; t < ntiles && !*abort;
+                 t += gridDim.x, ++it) {
+                const Tile ti = tile_of(t, s_off, s_pre, E, IB);
+                const uint32_t idesc = idesc_bf16_m128((uint32_t)ti.n);
+                if (!wait_phase(&ctl->tmem_empty, (it & 1) ^ 1, abort,
+                                a.status))
+                    break;
+                tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const uint32_t s = g % STAGES;
+                    if (!wait_phase(&ctl->full[s], (g / STAGES) & 1, abort,
+                                    a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ag = stage0 + s * STAGE_BYTES;
+                    const uint32_t au = ag + A_BYTES;
+                    const uint32_t bb = ag + 2 * A_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+                        const uint64_t bd = sw128_kmajor_desc(bb + ks * 32);
+                        umma_bf16(tmem, sw128_kmajor_desc(ag + ks * 32), bd,
+                                  idesc, acc);
+                        umma_bf16(tmem + kUpCol,
+                                  sw128_kmajor_desc(au + ks * 32), bd, idesc,
+                                  acc);
+                    }
+                    umma_commit(&ctl->empty[s]);
+                    issued = true;
+                }
+                if (!ok)
+                    break;
+                umma_commit(&ctl->tmem_full);
+            }
+            if (issued) {
+                umma_commit(&ctl->drain);
+                uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&ctl->drain, 0) &&
+                       globaltimer_ns() - t0 < kTimeoutNs) {
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int quad = warp & 3, half = warp >> 2;
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < ntiles && !*abort;
+             t += gridDim.x, ++it) {
+            const Tile ti = tile_of(t, s_off, s_pre, E, IB);
+            if (!wait_phase(&ctl->tmem_full, it & 1, abort, a.status))
+                break;
+            tc_fence_after();
+            const uint8_t *slab = expert_slab(a, ti.e);
+            const int64_t i = (int64_t)ti.iblk * BM + quad * 32 + lane;
+            float sg = 0.0f, su = 0.0f;
+            if (slab) {
+                sg = reinterpret_cast<const float *>(slab + a.gate_s_off)[i];
+                su = reinterpret_cast<const float *>(slab + a.up_s_off)[i];
+            }
+            const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+            for (int c0 = half * 16; c0 < ti.n; c0 += 32) {
+                uint32_t gv[16], uv[16];
+                tmem_ld16(tl + (uint32_t)c0, gv);
+                tmem_ld16(tl + kUpCol + (uint32_t)c0, uv);
+                tmem_ld_wait();
+                if (!slab)
+                    continue;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int n = c0 + jj;
+                    if (n >= ti.nvalid)
+                        break;
+                    const int64_t o = (int64_t)(ti.row0 + n) * a.I + i;
+                    const float g32 = __fmul_rn(__uint_as_float(gv[jj]), sg);
+                    const float u32 = __fmul_rn(__uint_as_float(uv[jj]), su);
+                    a.out[o] = swiglu_out(g32, u32);
+                    if (a.gate_f32)
+                        a.gate_f32[o] = g32;
+                    if (a.up_f32)
+                        a.up_f32[o] = u32;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ctl->tmem_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a) {
+    return H % BK == 0 && I % BM == 0 && a.gate_w_off % 16 == 0 &&
+           a.up_w_off % 16 == 0 && a.E <= Q4MOE_MAX_EXPERTS;
+}
+
+cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
+    const size_t smem = smem_bytes(a.E);
+    cudaError_t err = cudaFuncSetAttribute(
+        gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    gemm_tcgen05_kernel<<<a.num_sms, kThreads, smem, s>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace q4moe
