@@ -24,7 +24,8 @@
 //         16-column chunks it handles)
 //   8     TMEM allocation and the single thread that issues the MMAs
 //   9-12  weight dequantisation (one A row of gate and of up per thread)
-//   13-15 token gather (cp.async)
+//   13-15 token gather (cp.async; each thread's copies count as its arrival
+//         on the stage barrier when they land)
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // Q4MOE_DEV_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include "q4moe_internal.cuh"
@@ -180,7 +181,7 @@ gemm_tcgen05_kernel(GateUpArgs a) {
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->full[s], kDeqWarps + kGatWarps);
+            mbar_init(&ctl->full[s], kDeqWarps + kGatThreads);
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->tmem_full, 1);
@@ -244,8 +245,8 @@ gemm_tcgen05_kernel(GateUpArgs a) {
     if (warp >= kGatWarp0) {
         // ---------------------------------------------------- token gather
         const int j = tid - kGatWarp0 * 32;
+        const uint64_t keep = l2_policy_evict_last();
         uint32_t g = 0;
-        bool pending = false;
         for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
             const Tile ti = tile_of(t, s_off, s_pre, E, IB);
             // per item: token row (>= 0), -1 zero fill, -2 nothing to copy
@@ -280,33 +281,20 @@ gemm_tcgen05_kernel(GateUpArgs a) {
                     const int f = j + kGatThreads * m;
                     const uint32_t dst = bdst + sw128_offset(f >> 3, f & 7);
                     if (tokm[m] >= 0)
-                        cp_async_16(dst,
-                                    a.x + (int64_t)tokm[m] * a.H + (f & 7) * 8 +
-                                        kb * BK,
-                                    16);
+                        cp_async_16_hint(dst,
+                                         a.x + (int64_t)tokm[m] * a.H +
+                                             (f & 7) * 8 + kb * BK,
+                                         16, keep);
                     else
                         cp_async_16(dst, a.x, 0);
                 }
-                cp_async_commit();
-                if (pending) {
-                    cp_async_wait<1>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&ctl->full[(g - 1) % STAGES]);
-                }
-                pending = true;
+                // counted as this thread's arrival once its copies landed
+                cp_async_arrive_noinc(&ctl->full[s]);
             }
             if (!ok)
                 break;
         }
         cp_async_wait<0>();
-        if (pending && !*abort) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ctl->full[(g - 1) % STAGES]);
-        }
     } else if (warp >= kDeqWarp0) {
         // ------------------------------------------- weight dequantisation
         const int r = tid - kDeqWarp0 * 32;          // A row 0..127
@@ -401,6 +389,9 @@ gemm_tcgen05_kernel(GateUpArgs a) {
                         ok = false;
                         break;
                     }
+                    // the token rows arrived through cp.async (generic
+                    // proxy); order them before the tensor core's reads
+                    fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t ag = stage0 + s * STAGE_BYTES;
                     const uint32_t au = ag + A_BYTES;

@@ -3,13 +3,16 @@
 //
 // The pages hand each expert slot its own [M, H] row block (page 52,
 // streamed-experts.ts, Glm52CanonicalMetalExecutor.execute); this kernel
-// builds those row lists for every expert in one pass:
-//   1. histogram of expert ids in shared memory;
-//   2. exclusive scan -> row_offsets;
-//   3. pairs taken 1024 at a time in order; within a chunk each pair's rank
-//      among equal ids is (pairs of that id in earlier warps) + (earlier
-//      lanes of its own warp with that id, from __match_any_sync), so rows
-//      of one expert keep the token order.
+// builds those row lists for every expert in one pass over the pairs:
+//   1. each warp owns one contiguous segment of the pairs and counts its
+//      experts 32 pairs at a time (__match_any_sync groups equal ids; the
+//      lowest lane of a group adds the group's size);
+//   2. per expert, an exclusive scan over the warps, then over the experts,
+//      turns the counts into each warp's first row for that expert and into
+//      row_offsets;
+//   3. each warp walks its segment again, giving a pair the row
+//      base + (earlier lanes with the same id); segments are in pair order,
+//      so rows of one expert keep the token order.
 #include "q4moe_internal.cuh"
 
 namespace q4moe {
@@ -25,31 +28,52 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
                   int32_t *__restrict__ row_of_pair,
                   unsigned int *__restrict__ status) {
     extern __shared__ int32_t smem[];
-    int32_t *s_base = smem;             // [E]   next free row of expert e
-    int32_t *s_warp = smem + E;         // [kWarps][E] per-warp counts/bases
+    int32_t *s_cnt = smem;              // [kWarps][E] counts, then bases
+    int32_t *s_tot = smem + kWarps * E; // [E] first row of each expert
     __shared__ int32_t s_warp_sums[kWarps];
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = tid; e < E; e += kThreads)
-        s_base[e] = 0;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int j = tid; j < kWarps * E; j += kThreads)
+        s_cnt[j] = 0;
     if (tid == 0)
         s_bad = 0;
     __syncthreads();
 
-    // 1. histogram
-    for (int32_t q = tid; q < pairs; q += kThreads) {
-        const int32_t e = topk[q];
-        if (e >= 0 && e < E)
-            atomicAdd(&s_base[e], 1);
-        else
-            s_bad = 1;
+    const int32_t seg = (pairs + kWarps - 1) / kWarps;
+    const int32_t q0 = min(pairs, warp * seg), q1 = min(pairs, q0 + seg);
+    int32_t *cnt = s_cnt + warp * E;
+
+    // 1. per-warp counts
+    for (int32_t b = q0; b < q1; b += 32) {
+        const int32_t q = b + lane;
+        int32_t e = -1;
+        if (q < q1) {
+            e = topk[q];
+            if (e < 0 || e >= E) {
+                e = -1;
+                s_bad = 1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt_mask) == 0)
+            cnt[e] += __popc(peers);
+        __syncwarp();
     }
     __syncthreads();
 
-    // 2. exclusive scan over E <= kThreads counts (one per thread)
-    const int32_t c = tid < E ? s_base[tid] : 0;
-    int32_t incl = c;
+    // 2. per expert: each warp's first row (scan over warps), then the
+    //    offsets (scan over experts; E <= kThreads, one per thread)
+    int32_t tot = 0;
+    if (tid < E) {
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t n = s_cnt[w * E + tid];
+            s_cnt[w * E + tid] = tot;
+            tot += n;
+        }
+    }
+    int32_t incl = tot;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
@@ -60,7 +84,7 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
         s_warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int32_t w = s_warp_sums[lane];
+        const int32_t w = s_warp_sums[lane];
         int32_t wi = w;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -71,55 +95,40 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
         s_warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
     }
     __syncthreads();
-    const int32_t excl = s_warp_sums[warp] + incl - c;
+    const int32_t excl = s_warp_sums[warp] + incl - tot;
     if (tid < E) {
-        s_base[tid] = excl;
+        s_tot[tid] = excl;
         row_offsets[tid] = excl;
+        if (tid == E - 1)
+            row_offsets[E] = excl + tot;
     }
-    if (tid == E - 1 || (E == 0 && tid == 0))
-        row_offsets[E] = excl + c;
     if (tid == 0 && s_bad)
         atomicOr(status, Q4MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
 
-    // 3. stable scatter, one chunk of kThreads pairs at a time
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int32_t c0 = 0; c0 < pairs; c0 += kThreads) {
-        for (int j = tid; j < kWarps * E; j += kThreads)
-            s_warp[j] = 0;
-        __syncthreads();
-        const int32_t q = c0 + tid;
+    // 3. stable scatter
+    for (int32_t b = q0; b < q1; b += 32) {
+        const int32_t q = b + lane;
         int32_t e = -1;
-        if (q < pairs) {
+        if (q < q1) {
             e = topk[q];
             if (e < 0 || e >= E)
                 e = -1;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
+        int32_t row = -1;
+        if (e >= 0)
+            row = s_tot[e] + cnt[e] + rank;
+        __syncwarp();
         if (e >= 0 && rank == 0)
-            s_warp[warp * E + e] = __popc(peers);
-        __syncthreads();
-        for (int ee = tid; ee < E; ee += kThreads) {
-            int32_t run = s_base[ee];
-            for (int w = 0; w < kWarps; ++w) {
-                const int32_t n = s_warp[w * E + ee];
-                s_warp[w * E + ee] = run;
-                run += n;
-            }
-            s_base[ee] = run;
-        }
-        __syncthreads();
-        if (q < pairs) {
-            if (e >= 0) {
-                const int32_t row = s_warp[warp * E + e] + rank;
+            cnt[e] += __popc(peers);
+        __syncwarp();
+        if (q < q1) {
+            row_of_pair[q] = row;
+            if (row >= 0)
                 token_of_row[row] = q / k;
-                row_of_pair[q] = row;
-            } else {
-                row_of_pair[q] = -1;
-            }
         }
-        __syncthreads();
     }
 }
 

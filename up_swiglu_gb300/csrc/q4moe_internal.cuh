@@ -43,24 +43,23 @@ cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
                               int64_t n, uint16_t *res, cudaStream_t s);
 
 // ------------------------------------------------------------------------
-// bf16 helpers.  Rounding: nearest, ties to even, on the f32 bit pattern
-// (page 54, codebook.ts, trellis_bf16); every value reaching it is finite.
+// bf16 helpers.  Rounding: nearest, ties to even (page 54, codebook.ts,
+// trellis_bf16), done by the hardware conversion (subnormals kept); every
+// value reaching it is finite.
 __device__ __forceinline__ uint16_t bf16_rne(float v) {
-    uint32_t u = __float_as_uint(v);
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return (uint16_t)(u >> 16);
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 __device__ __forceinline__ float bf16_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
 }
 
-// The page's f32 sigmoid chain 1 / (1 + exp(-g)) for a bf16 value g
-// (page 52, GATE_UP_SOURCE tail), with IEEE add and divide and no flush to
-// zero.  expf is within 2 ulp of exp; the result can only round to a
-// different bf16 than the correctly rounded chain when it lies within a few
-// f32 ulp of a bf16 rounding midpoint, and there the chain is recomputed
-// from the double-precision exponential.
+// The page's f32 sigmoid chain 1 / (1 + exp(-g)) (page 52, GATE_UP_SOURCE
+// tail) with IEEE add and divide and no flush to zero.  expf is within 2 ulp
+// of exp; the result can only round to a different bf16 than the correctly
+// rounded chain when it lies within a few f32 ulp of a bf16 rounding
+// midpoint, and there the chain is recomputed from the double-precision
+// exponential.
 __device__ __forceinline__ float sigmoid_chain(float g) {
     float e = expf(-g);
     float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
@@ -72,12 +71,46 @@ __device__ __forceinline__ float sigmoid_chain(float g) {
     return s;
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// bf16 sigmoid of a bf16 value g, equal to bf16(sigmoid_chain(g)).
+// For |g| < 16 the sigmoid is first formed as 1 / (1 + 2^(-g log2 e)) with
+// the hardware approximations; its error against the chain stays below
+// 40 f32 ulp (argument rounding 1.6e-6 relative, ex2 and rcp about 2 ulp),
+// so whenever it lies more than 96 ulp from a bf16 rounding midpoint both
+// round to the same bf16.  For g >= 16, 1 - sigmoid < 2^-9 (it is below
+// 2^-23), so the bf16 result is 1.0.  Everything else takes the exact
+// chain.  (sigmoidT depends on the 16-bit g only; all 65,536 cases are
+// tested against the oracle.)
+__device__ __forceinline__ uint16_t sigmoid_bf16(float g) {
+    if (fabsf(g) < 16.0f) {
+        const float s =
+            rcp_approx(1.0f + ex2_approx(g * -1.44269504088896341f));
+        const int lo = (int)(__float_as_uint(s) & 0xFFFFu);
+        if (abs(lo - 0x8000) > 96)
+            return bf16_rne(s);
+    } else if (g >= 16.0f) {
+        return 0x3F80;
+    }
+    return bf16_rne(sigmoid_chain(g));
+}
+
 // gateT, upT -> out (bf16 bits).  sig and silu are also returned.
 __device__ __forceinline__ uint16_t swiglu_tail_bits(uint16_t gT, uint16_t uT,
                                                      uint16_t *sigT,
                                                      uint16_t *siluT) {
     const float g = bf16_f32(gT);
-    const uint16_t s = bf16_rne(sigmoid_chain(g));
+    const uint16_t s = sigmoid_bf16(g);
     const uint16_t si = bf16_rne(__fmul_rn(g, bf16_f32(s)));
     *sigT = s;
     *siluT = si;

@@ -61,6 +61,34 @@ __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// The same copy with an L2 cache policy (l2_policy_evict_last).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src,
+                                                 uint32_t src_bytes,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+            dst),
+        "l"(src), "r"(src_bytes), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data that many CTAs re-read (the activations): keep it
+// resident while the weights stream through.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
+                 : "=l"(p));
+    return p;
+}
+
+// Arrive on *bar (counted as one of its expected arrivals) once every
+// cp.async this thread issued so far has landed in shared memory.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
