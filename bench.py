@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default="auto",
                     choices=["auto", "matvec", "gemm"])
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="call without the scratch workspace")
     return ap.parse_args()
 
 
@@ -183,7 +185,8 @@ class ClockSampler:
 class GpuWorkload:
     """Device-resident inputs for one workload and the step launcher."""
 
-    def __init__(self, w: syn.Workload, kernel: str, device: int):
+    def __init__(self, w: syn.Workload, kernel: str, device: int,
+                 use_workspace: bool = True):
         import torch
         from up_swiglu_gb300 import q4moe as q
         self.torch, self.q, self.w = torch, q, w
@@ -232,6 +235,14 @@ class GpuWorkload:
             self.slabs = [q.make_slabs(w.E, L, base=self.pool)]
         self.opts = q.q4moe_options_t()
         self.opts.kernel = self.kernel
+        if use_workspace:
+            # scratch for the grouped activations the tensor-core GEMM reads
+            nbytes = q.q4moe_workspace_bytes(self.M, w.H)
+            self._ws = torch.empty(nbytes + 256, dtype=torch.uint8,
+                                   device=self.dev)
+            off = (-self._ws.data_ptr()) % 256
+            self.opts.workspace = self._ws.data_ptr() + off
+            self.opts.workspace_bytes = nbytes
         self.graph = None
         self.launches_per_step = None
 
@@ -390,7 +401,8 @@ def main():
         dist.init_process_group("nccl")
     q.load()
 
-    gw = GpuWorkload(w, args.kernel, local)
+    gw = GpuWorkload(w, args.kernel, local,
+                     use_workspace=not args.no_workspace)
     units = workload_units(w, gw.topk_host, gw.pool_experts)
     dev = gw.dev
     stream = gw.stream
@@ -514,6 +526,7 @@ def main():
                        "l2": "weights larger than L2 every step "
                              f"({gw.pool_experts} distinct expert slabs)",
                        "kernel_choice": args.kernel,
+                       "workspace": not args.no_workspace,
                        "parallelism": f"replicas x{world}" if world > 1
                        else "single GPU"},
             "tflops": round(tflops, 3),

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 1
+#define Q4MOE_ABI_VERSION 2
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -126,7 +126,21 @@ typedef struct q4moe_options {
     float *up_f32;      /* optional device f32 [M][I]: U * up scale        */
     int32_t kernel;     /* Q4MOE_KERNEL_*                                  */
     int32_t reserved0;  /* must be 0                                       */
+    void *workspace;    /* optional device scratch of at least
+                           q4moe_workspace_bytes(M, H) bytes, 256-byte
+                           aligned, not overlapping any other argument.
+                           With it the tensor-core GEMM reads the routed
+                           activations once, grouped, through TMA; without
+                           it the GEMM gathers them row by row.  Contents
+                           are undefined after the call; calls that share a
+                           workspace must be ordered on one stream.       */
+    int64_t workspace_bytes; /* size of workspace                         */
 } q4moe_options_t;
+
+/* Bytes of the optional workspace (q4moe_options_t.workspace) for M grouped
+ * rows of hidden size H: the routed activations in grouped order, bf16
+ * [M][H].  Host only; returns a negative code for negative arguments. */
+int64_t q4moe_workspace_bytes(int64_t M, int64_t H);
 
 /* ABI version of the loaded library (Q4MOE_ABI_VERSION). */
 int q4moe_abi_version(void);

@@ -139,8 +139,10 @@ def group(d: DeviceProblem, stream=None):
 
 
 def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
-            stream=None, out=None):
-    """Run the fused call; returns numpy out bits [M, I] (+ gate32/up32)."""
+            stream=None, out=None, workspace=False):
+    """Run the fused call; returns numpy out bits [M, I] (+ gate32/up32).
+    workspace=True hands the call a scratch buffer (grouped activations
+    for the tensor-core GEMM)."""
     import torch
     M = int(tok.shape[0])
     I = d.p.I
@@ -148,7 +150,7 @@ def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
         out = torch.full((max(M, 1), I), -1, dtype=torch.int16,
                          device="cuda")
     res = {}
-    if debug or kernel != q.KERNEL_AUTO:
+    if debug or kernel != q.KERNEL_AUTO or workspace:
         g32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
             if debug else None
         u32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
@@ -158,6 +160,13 @@ def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
         o.gate_f32 = None if g32 is None else g32.data_ptr()
         o.up_f32 = None if u32 is None else u32.data_ptr()
         o.kernel = kernel
+        if workspace:
+            nbytes = q.q4moe_workspace_bytes(M, d.p.H)
+            wbuf, ws = aligned_device_buffer(max(nbytes, 256), 256)
+            ws.fill_(0xFF)                      # stale contents must not matter
+            d.keep.append(wbuf)
+            o.workspace = ws.data_ptr()
+            o.workspace_bytes = nbytes
         q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, offs, tok, M, d.p.H, I, out,
                                   o, stream)
         if debug:

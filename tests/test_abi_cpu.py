@@ -121,6 +121,15 @@ def test_host_argument_errors():
     o.kernel = 7
     assert _call(opts=o) == q.ERR_INVALID_ARG
     assert "options" in q.q4moe_last_error()
+    o = q.q4moe_options_t()
+    o.workspace = FAKE
+    o.workspace_bytes = q.q4moe_workspace_bytes(4, 64) - 1
+    assert _call(opts=o) == q.ERR_INVALID_ARG       # workspace too small
+    o.workspace = FAKE + 16
+    o.workspace_bytes = 1 << 20
+    assert _call(opts=o) == q.ERR_ALIGNMENT         # not 256-aligned
+    assert q.q4moe_workspace_bytes(4, 64) == 512
+    assert q.q4moe_workspace_bytes(3, 8) == 256
     lib = q.load()
     assert lib.q4moe_group_rows(FAKE, 4, 0, 8, FAKE, FAKE, FAKE, None) == \
         q.ERR_INVALID_ARG

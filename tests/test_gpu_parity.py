@@ -46,6 +46,11 @@ def _run_and_compare(p, kernel=q.KERNEL_AUTO, exact=False, **upload_kw):
     # the plain entry point (no debug outputs) writes the same bits
     plain = hz.gate_up(d, offs_d, tok_d, kernel=kernel, debug=False)
     assert np.array_equal(plain["out"], gpu["out"])
+    # with a workspace the GEMM reads the grouped rows through TMA: same bits
+    ws = hz.gate_up(d, offs_d, tok_d, kernel=kernel, workspace=True)
+    assert np.array_equal(ws["out"], gpu["out"])
+    assert np.array_equal(ws["gate32"].view(np.uint32),
+                          gpu["gate32"].view(np.uint32))
     return stats
 
 

@@ -91,6 +91,9 @@ def test_full_size_sampled(name):
     gs_el, us_el = hz.element_scales(p, offs)
     sel = {k: gpu[k][rows, cols] for k in ("out", "gate32", "up32")}
     parity.compare(sel, orc, gs_el[rows, cols], us_el[rows, cols], p.H)
-    # the plain entry point gives the same bits as the debug one
+    # the plain entry point gives the same bits as the debug one, and so
+    # does the call with a workspace (the benchmark's configuration)
     plain = hz.gate_up(d, offs_d, tok_d, debug=False)
     assert np.array_equal(plain["out"], gpu["out"])
+    ws = hz.gate_up(d, offs_d, tok_d, debug=False, workspace=True)
+    assert np.array_equal(ws["out"], gpu["out"])

@@ -158,6 +158,12 @@ int q4moe_abi_version(void) { return Q4MOE_ABI_VERSION; }
 
 const char *q4moe_last_error(void) { return t_last_error.c_str(); }
 
+int64_t q4moe_workspace_bytes(int64_t M, int64_t H) {
+    if (M < 0 || H < 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "negative size");
+    return (M * H * 2 + 255) / 256 * 256;
+}
+
 int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout) {
     if (layout == nullptr)
         return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
@@ -287,6 +293,16 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
         return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
                                          "aligned");
+    if (o.workspace != nullptr) {
+        if (!aligned(o.workspace, 256))
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "workspace must be 256-byte aligned");
+        if (o.workspace_bytes < q4moe_workspace_bytes(M, H))
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "workspace of %lld bytes is smaller than the %lld "
+                        "this call needs", (long long)o.workspace_bytes,
+                        (long long)q4moe_workspace_bytes(M, H));
+    }
 
     DeviceInfo *d = nullptr;
     rc = device_info(&d);
@@ -314,6 +330,7 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     a.out = static_cast<uint16_t *>(out);
     a.gate_f32 = o.gate_f32;
     a.up_f32 = o.up_f32;
+    a.xg = static_cast<uint16_t *>(o.workspace);
     a.status = d->status;
     a.num_sms = d->num_sms;
 

@@ -12,8 +12,10 @@
 //  A      = the gate (and the up) weights of the tile's rows, dequantised
 //           (nibble - 8, exact in bf16) into shared memory in the 128-byte
 //           swizzled K-major layout, 64 K per pipeline stage;
-//  B      = the tile's token rows of x, gathered row by row with cp.async
-//           into the same layout;
+//  B      = the tile's token rows of x in the same layout: with a
+//           workspace, the rows are first copied once into grouped order
+//           and each stage is a few TMA boxes of 16 rows; without one,
+//           they are gathered row by row with cp.async;
 //  D      = two f32 accumulators in tensor memory (gate: columns 0..N-1,
 //           up: columns 256..256+N-1), lane = intermediate row;
 //  tail   = row scales, bf16 rounding and the SwiGLU chain, per element, as
@@ -24,10 +26,18 @@
 //         16-column chunks it handles)
 //   8     TMEM allocation and the single thread that issues the MMAs
 //   9-12  weight dequantisation (one A row of gate and of up per thread)
-//   13-15 token gather (cp.async; each thread's copies count as its arrival
-//         on the stage barrier when they land)
+//   13-15 token rows: one thread issuing TMA boxes (workspace), or all
+//         three warps gathering with cp.async, each thread's copies
+//         counting as its arrival on the stage barrier when they land
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // Q4MOE_DEV_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
 #include "q4moe_internal.cuh"
 #include "q4moe_sm100.cuh"
 
@@ -56,6 +66,8 @@ constexpr int kPrefetch = 4;                 // k-blocks of weights in flight
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kUpCol = 256;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr int kBoxRows = 16;                 // rows per TMA box of x
+constexpr uint32_t kBoxBytes = kBoxRows * BK * 2;
 
 struct Ctl {
     uint64_t full[STAGES];
@@ -164,8 +176,31 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Bounded wait that ignores the abort flag, used while draining copies
+// before exit (they land within microseconds; 0.2 s is ample).
+__device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity) &&
+           globaltimer_ns() - t0 < 200000000ull) {
+    }
+}
+
+// Copy each grouped row's activations into the workspace (bf16 [M][H]).
+__global__ void __launch_bounds__(128)
+gather_rows_kernel(GateUpArgs a) {
+    const int64_t chunks = a.H / 8;
+    for (int64_t p = blockIdx.x; p < a.M; p += gridDim.x) {
+        const int64_t t = row_token(a, p);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.xg + p * a.H);
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * a.H);
+        for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
+            dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <bool kTma>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tcgen05_kernel(GateUpArgs a) {
+gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -181,7 +216,7 @@ gemm_tcgen05_kernel(GateUpArgs a) {
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->full[s], kDeqWarps + kGatThreads);
+            mbar_init(&ctl->full[s], kDeqWarps + (kTma ? 1 : kGatThreads));
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->tmem_full, 1);
@@ -242,7 +277,36 @@ gemm_tcgen05_kernel(GateUpArgs a) {
     volatile int *abort = &ctl->abort;
     const uint32_t stage0 = smem_u32(stages);
 
-    if (warp >= kGatWarp0) {
+    if (kTma && warp >= kGatWarp0) {
+        // ------------------------------------------- token rows via TMA
+        if (warp == kGatWarp0 && lane == 0) {
+            uint32_t g = 0;
+            for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+                const Tile ti = tile_of(t, s_off, s_pre, E, IB);
+                const int boxes = ti.n / kBoxRows;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const uint32_t s = g % STAGES;
+                    if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1,
+                                    abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ctl->full[s], boxes * kBoxBytes);
+                    const uint32_t bdst =
+                        stage0 + s * STAGE_BYTES + 2 * A_BYTES;
+                    for (int b = 0; b < boxes; ++b)
+                        tma_load_2d(bdst + b * kBoxBytes, &tmap_xg, kb * BK,
+                                    ti.row0 + b * kBoxRows, &ctl->full[s]);
+                }
+                if (!ok)
+                    break;
+            }
+            // let the boxes still in flight land before the CTA exits
+            for (uint32_t gg = g > STAGES ? g - STAGES : 0; gg < g; ++gg)
+                drain_phase(&ctl->full[gg % STAGES], (gg / STAGES) & 1);
+        }
+    } else if (warp >= kGatWarp0) {
         // ---------------------------------------------------- token gather
         const int j = tid - kGatWarp0 * 32;
         const uint64_t keep = l2_policy_evict_last();
@@ -389,9 +453,10 @@ gemm_tcgen05_kernel(GateUpArgs a) {
                         ok = false;
                         break;
                     }
-                    // the token rows arrived through cp.async (generic
-                    // proxy); order them before the tensor core's reads
-                    fence_proxy_async_smem();
+                    // token rows that arrived through cp.async (generic
+                    // proxy) are ordered before the tensor core's reads
+                    if (!kTma)
+                        fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t ag = stage0 + s * STAGE_BYTES;
                     const uint32_t au = ag + A_BYTES;
@@ -484,16 +549,73 @@ bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a) {
            a.up_w_off % 16 == 0 && a.E <= Q4MOE_MAX_EXPERTS;
 }
 
-cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p,
+                                             12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tensor map of the grouped activations bf16 [M][H]: boxes of 64 columns
+// (128 bytes, the swizzle span) x 16 rows, 128-byte swizzle, rows past M
+// read as zero.
+cudaError_t encode_xg_map(const GateUpArgs &a, CUtensorMap *map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)kBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.xg,
+                           dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool kTma>
+cudaError_t launch_gemm_kernel(const GateUpArgs &a, const CUtensorMap &map,
+                               cudaStream_t s) {
     const size_t smem = smem_bytes(a.E);
     cudaError_t err = cudaFuncSetAttribute(
-        gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        gemm_tcgen05_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)smem);
     if (err != cudaSuccess)
         return err;
-    gemm_tcgen05_kernel<<<a.num_sms, kThreads, smem, s>>>(a);
+    gemm_tcgen05_kernel<kTma><<<a.num_sms, kThreads, smem, s>>>(a, map);
     count_launches(1);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
+    CUtensorMap map;
+    memset(&map, 0, sizeof map);
+    if (a.xg == nullptr)
+        return launch_gemm_kernel<false>(a, map, s);
+    cudaError_t err = encode_xg_map(a, &map);
+    if (err != cudaSuccess)
+        return err;
+    const int blocks = (int)std::min<int64_t>(a.M, (int64_t)a.num_sms * 16);
+    gather_rows_kernel<<<blocks, 128, 0, s>>>(a);
+    count_launches(1);
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
+    return launch_gemm_kernel<true>(a, map, s);
 }
 
 }  // namespace q4moe

@@ -24,6 +24,8 @@ struct GateUpArgs {
     uint16_t *out;               // bf16 [M][I]
     float *gate_f32;             // optional [M][I]
     float *up_f32;               // optional [M][I]
+    uint16_t *xg;                // optional workspace: bf16 [M][H], the
+                                 // routed activations in grouped order
     unsigned int *status;        // device status word (Q4MOE_DEV_* bits)
     int32_t matvec_max_rows;     // experts with more rows go to the GEMM
     int32_t num_sms;

@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -40,7 +40,7 @@ EXPORTS = (
     "q4moe_abi_version", "q4moe_last_error", "q4moe_canonical_layout",
     "q4moe_validate_layout", "q4moe_pack_slab", "q4moe_group_rows",
     "q4moe_gate_up_swiglu", "q4moe_gate_up_swiglu_ex", "q4moe_device_status",
-    "q4moe_debug_tail", "q4moe_launch_count",
+    "q4moe_debug_tail", "q4moe_launch_count", "q4moe_workspace_bytes",
 )
 
 
@@ -74,7 +74,9 @@ class q4moe_options_t(ctypes.Structure):
                 ("gate_f32", ctypes.c_void_p),
                 ("up_f32", ctypes.c_void_p),
                 ("kernel", ctypes.c_int32),
-                ("reserved0", ctypes.c_int32)]
+                ("reserved0", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -121,6 +123,7 @@ def load(build_if_missing: bool = True):
                                      ctypes.c_int]),
             "q4moe_debug_tail": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
             "q4moe_launch_count": (ctypes.c_int64, []),
+            "q4moe_workspace_bytes": (ctypes.c_int64, [_I64, _I64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -218,6 +221,13 @@ def q4moe_device_status(stream=None, clear: bool = True) -> int:
     if rc not in (OK, ERR_DEVICE_DATA):
         _check(rc)
     return int(flags.value)
+
+
+def q4moe_workspace_bytes(M: int, H: int) -> int:
+    n = int(load().q4moe_workspace_bytes(M, H))
+    if n < 0:
+        _check(n)
+    return n
 
 
 def q4moe_launch_count() -> int:
