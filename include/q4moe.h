@@ -137,6 +137,32 @@ typedef struct q4moe_options {
     int64_t workspace_bytes; /* size of workspace                         */
 } q4moe_options_t;
 
+/*
+ * q4moe_gate_up_swiglu for callers that cannot allocate device memory (a
+ * plugin inside a host engine that owns all GPU memory through its own pool,
+ * code held to a fixed memory budget, a latency-critical loop that must not
+ * risk the device synchronisation an allocation can bring).  The pages have
+ * no counterpart: this is a library convenience.  Same arguments and result
+ * as q4moe_gate_up_swiglu with a workspace, but the scratch is a fixed array
+ * inside the library, Q4MOE_NOALLOC_SCRATCH_BYTES on every GPU that loads
+ * it, held until the process exits; the call allocates nothing.
+ *  - Limit: M * H * 2 bytes (q4moe_workspace_bytes) must not exceed
+ *    Q4MOE_NOALLOC_SCRATCH_BYTES, else Q4MOE_ERR_INVALID_ARG with a message.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and overwrites what it needs before
+ *    reading it (nothing has to start at zero); calls that overlap on the
+ *    GPU, on different streams, race on it.
+ */
+#define Q4MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
+int q4moe_gate_up_swiglu_noalloc(const void *x,
+                                 const q4moe_slabs_t *expert_slabs,
+                                 const int32_t *row_offsets_per_expert,
+                                 const int32_t *token_to_expert_map,
+                                 int64_t M, int64_t H, int64_t I, void *out,
+                                 cudaStream_t stream);
+
 /* Bytes of the optional workspace (q4moe_options_t.workspace) for M grouped
  * rows of hidden size H: the routed activations in grouped order, bf16
  * [M][H].  Host only; returns a negative code for negative arguments. */

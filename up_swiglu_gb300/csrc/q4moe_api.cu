@@ -148,6 +148,9 @@ std::atomic<int64_t> g_launches{0};
 
 namespace q4moe {
 void count_launches(int n) { g_launches.fetch_add(n); }
+int report_error(int code, const char *message) {
+    return fail(code, "%s", message);
+}
 }  // namespace q4moe
 
 extern "C" {

@@ -34,6 +34,9 @@ struct GateUpArgs {
 // Host-side count of kernel launches (q4moe_launch_count).
 void count_launches(int n);
 
+// Record `message` as the calling thread's last error; returns `code`.
+int report_error(int code, const char *message);
+
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
 bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);

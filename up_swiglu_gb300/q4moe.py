@@ -41,7 +41,11 @@ EXPORTS = (
     "q4moe_validate_layout", "q4moe_pack_slab", "q4moe_group_rows",
     "q4moe_gate_up_swiglu", "q4moe_gate_up_swiglu_ex", "q4moe_device_status",
     "q4moe_debug_tail", "q4moe_launch_count", "q4moe_workspace_bytes",
+    "q4moe_gate_up_swiglu_noalloc",
 )
+
+# Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class Q4moeError(RuntimeError):
@@ -124,6 +128,9 @@ def load(build_if_missing: bool = True):
             "q4moe_debug_tail": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
             "q4moe_launch_count": (ctypes.c_int64, []),
             "q4moe_workspace_bytes": (ctypes.c_int64, [_I64, _I64]),
+            "q4moe_gate_up_swiglu_noalloc": (ctypes.c_int,
+                                             [_P, _P, _P, _P, _I64, _I64,
+                                              _I64, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -211,6 +218,18 @@ def q4moe_gate_up_swiglu_ex(x, expert_slabs, row_offsets_per_expert,
         _ptr(x), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
         _ptr(token_to_expert_map), M, H, I, _ptr(out),
         None if opts is None else ctypes.byref(opts), _stream(stream)))
+
+
+def q4moe_gate_up_swiglu_noalloc(x, expert_slabs, row_offsets_per_expert,
+                                 token_to_expert_map, M, H, I, out,
+                                 stream=None) -> None:
+    """The fused call without any device allocation: for callers that have
+    no way to hand over scratch memory (see include/q4moe.h).  The scratch
+    is a fixed array inside the library; M * H * 2 bytes must fit in
+    NOALLOC_SCRATCH_BYTES."""
+    _check(load().q4moe_gate_up_swiglu_noalloc(
+        _ptr(x), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
+        _ptr(token_to_expert_map), M, H, I, _ptr(out), _stream(stream)))
 
 
 def q4moe_device_status(stream=None, clear: bool = True) -> int:
