@@ -511,19 +511,41 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                 tmem_ld_wait();
                 if (!slab)
                     continue;
+                // all 16 columns branch-free (independent chains the
+                // scheduler can interleave); the rare exact sigmoids after
+                float gT[16], uT[16], sT[16];
+                uint32_t slow = 0;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    const int n = c0 + jj;
-                    if (n >= ti.nvalid)
-                        break;
-                    const int64_t o = (int64_t)(ti.row0 + n) * a.I + i;
                     const float g32 = __fmul_rn(__uint_as_float(gv[jj]), sg);
                     const float u32 = __fmul_rn(__uint_as_float(uv[jj]), su);
-                    a.out[o] = swiglu_out(g32, u32);
-                    if (a.gate_f32)
-                        a.gate_f32[o] = g32;
-                    if (a.up_f32)
-                        a.up_f32[o] = u32;
+                    gv[jj] = __float_as_uint(g32);
+                    uv[jj] = __float_as_uint(u32);
+                    gT[jj] = bf16_round(g32);
+                    uT[jj] = bf16_round(u32);
+                    bool ok;
+                    sT[jj] = sigmoid_bf16_fast_f(gT[jj], &ok);
+                    slow |= (ok ? 0u : 1u) << jj;
+                }
+                if (slow) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        if (slow & (1u << jj))
+                            sT[jj] = bf16_f32(sigmoid_bf16_exact(gT[jj]));
+                }
+                const int64_t o0 = (int64_t)(ti.row0 + c0) * a.I + i;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float si = bf16_round(__fmul_rn(gT[jj], sT[jj]));
+                    const uint16_t o = bf16_bits(__fmul_rn(si, uT[jj]));
+                    if (c0 + jj < ti.nvalid) {
+                        const int64_t oi = o0 + (int64_t)jj * a.I;
+                        a.out[oi] = o;
+                        if (a.gate_f32)
+                            a.gate_f32[oi] = __uint_as_float(gv[jj]);
+                        if (a.up_f32)
+                            a.up_f32[oi] = __uint_as_float(uv[jj]);
+                    }
                 }
             }
             tc_fence_before();

@@ -59,6 +59,21 @@ __device__ __forceinline__ float bf16_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
 }
 
+// The same rounding done on the bit pattern with integer operations (the
+// page's own formulation: add 0x7FFF plus the lowest kept bit, drop the low
+// 16 bits), returning the rounded value as an f32 (bf16_round) or its bf16
+// bits (bf16_bits).  Used on hot paths, where the integer unit is faster
+// than the conversion unit.
+__device__ __forceinline__ float bf16_round(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return __uint_as_float((u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
 // The page's f32 sigmoid chain 1 / (1 + exp(-g)) (page 52, GATE_UP_SOURCE
 // tail) with IEEE add and divide and no flush to zero.  expf is within 2 ulp
 // of exp; the result can only round to a different bf16 than the correctly
@@ -88,26 +103,45 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
-// bf16 sigmoid of a bf16 value g, equal to bf16(sigmoid_chain(g)).
-// For |g| < 16 the sigmoid is first formed as 1 / (1 + 2^(-g log2 e)) with
-// the hardware approximations; its error against the chain stays below
-// 40 f32 ulp (argument rounding 1.6e-6 relative, ex2 and rcp about 2 ulp),
-// so whenever it lies more than 96 ulp from a bf16 rounding midpoint both
-// round to the same bf16.  For g >= 16, 1 - sigmoid < 2^-9 (it is below
-// 2^-23), so the bf16 result is 1.0.  Everything else takes the exact
-// chain.  (sigmoidT depends on the 16-bit g only; all 65,536 cases are
-// tested against the oracle.)
-__device__ __forceinline__ uint16_t sigmoid_bf16(float g) {
-    if (fabsf(g) < 16.0f) {
-        const float s =
-            rcp_approx(1.0f + ex2_approx(g * -1.44269504088896341f));
-        const int lo = (int)(__float_as_uint(s) & 0xFFFFu);
-        if (abs(lo - 0x8000) > 96)
-            return bf16_rne(s);
-    } else if (g >= 16.0f) {
-        return 0x3F80;
-    }
+// bf16 sigmoid of a bf16 value g, in two parts so that callers can run the
+// first on many values at once.  sigmoid_bf16_fast_f forms
+// exp(-g) = 2^(-g log2 e) with the hardware ex2 approximation, carrying the
+// rounding error of the argument: log2 e is split into a float head and
+// tail, t = -g * head is rounded, and the exact remainder
+// fma(-g, head, -t) - g * tail multiplies the result as 1 + r ln 2 (its
+// square is below 2^-40).  Then sigmoid = rcp(1 + e).  For g > -16 its error
+// against the page's f32 chain is a few f32 ulp (ex2 and rcp about 2 ulp
+// each), so when it lies more than 16 ulp from a bf16 rounding midpoint both
+// round to the same bf16 and *ok is set; otherwise sigmoid_bf16_exact runs
+// the chain itself.  (sigmoidT depends on the 16-bit g only; all 65,536
+// cases are tested against the oracle.)
+__device__ __forceinline__ float sigmoid_bf16_fast_f(float g, bool *ok) {
+    const float kHead = 1.44269502162933349609375f;  // float(log2 e)
+    const float kTail = 1.925963033500011e-08f;      // log2 e - kHead
+    const float kLn2 = 0.693147180559945309f;
+    const float a = -fminf(g, 16.0f);  // sigmoidT is 1.0 for every g >= 16
+    const float t = a * kHead;
+    const float r = __fmaf_rn(a, kHead, -t) + a * kTail;
+    const float p = ex2_approx(t);
+    const float e = __fmaf_rn(p, r * kLn2, p);
+    const float s = rcp_approx(1.0f + e);
+    const int lo = (int)(__float_as_uint(s) & 0xFFFFu);
+    *ok = (g > -16.0f) && (abs(lo - 0x8000) > 16);
+    return bf16_round(s);
+}
+
+__device__ __forceinline__ uint16_t sigmoid_bf16_fast(float g, bool *ok) {
+    return (uint16_t)(__float_as_uint(sigmoid_bf16_fast_f(g, ok)) >> 16);
+}
+
+static __device__ __noinline__ uint16_t sigmoid_bf16_exact(float g) {
     return bf16_rne(sigmoid_chain(g));
+}
+
+__device__ __forceinline__ uint16_t sigmoid_bf16(float g) {
+    bool ok;
+    const uint16_t s = sigmoid_bf16_fast(g, &ok);
+    return ok ? s : sigmoid_bf16_exact(g);
 }
 
 // gateT, upT -> out (bf16 bits).  sig and silu are also returned.

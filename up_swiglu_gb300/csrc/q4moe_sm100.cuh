@@ -125,6 +125,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Prefetch one box of a tiled 2-D tensor into L2 (no shared memory write,
+// no completion to track).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0,
+                                                int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05 --
 // TMEM allocation (whole warp): the base address is written to *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
