@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "q4moe.h"
@@ -38,6 +39,8 @@ void count_launches(int n);
 int report_error(int code, const char *message);
 
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s);
+bool matvec_mma_supported(const GateUpArgs &a);
+cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
 bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);
 cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,

@@ -1,0 +1,470 @@
+// q4moe_matvec_mma.cu -- grouped Q4 gate/up + SwiGLU for experts with few
+// rows (decode, speculative verify), on the warp-level tensor core path.
+//
+// Same arithmetic as the pages' GATE_UP_SOURCE (page 52, streamed-experts.ts):
+// every packed word is read from HBM once per call and serves all of the
+// expert's rows in the chunk (the shared-row idea of page 57's
+// GATEUP_SHARED_M_SOURCE), the dot products accumulate in f32.
+//
+// Task = (expert, chunk of up to 8 grouped rows, block of 8 intermediate
+// rows).  A CTA of 8 warps owns one task at a time and splits its K range:
+// warp w takes the 128-wide K steps w, w+8, ...  For one K step a thread
+// (group g = lane/4, quad member t = lane%4) holds 16 bytes (32 nibbles) of
+// gate row g and of up row g and issues eight mma.sync.m16n8k16 (bf16 in,
+// f32 accumulate) with
+//   A rows 0-7  = gate rows, A rows 8-15 = up rows of the same 8 i,
+//   B columns   = the chunk's 8 grouped rows (tokens),
+// so the C fragment of a thread already pairs gate and up of one i.
+// Weights are dequantised straight into registers: word w gives the four
+// bf16x2 {n_j, n_j+4} (j = 0..3) as (w >> 4j) & 0x000F000F placed in the
+// mantissa of 128.0 and reduced by 136 (exact).  The K order inside each
+// MMA follows that pairing; the activations are staged once per chunk in
+// shared memory in the matching order ((0,4,1,5,2,6,3,7) within each group
+// of 8) and bank-swizzled so that the B fragments load without conflicts.
+// Each warp prefetches the weights of its next K steps into registers while
+// it multiplies the current ones.  Partial sums meet in shared memory in a
+// fixed warp order (deterministic, and a row's bits do not depend on the
+// other rows of its chunk); warp 0 applies the scales and the tail.
+#include "q4moe_internal.cuh"
+
+namespace q4moe {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerTask = 16;    // intermediate rows (two MMA row tiles)
+constexpr int kTok = 8;             // grouped rows per chunk
+constexpr int kStepK = 128;         // K per step (16 words per row)
+
+struct Task {
+    int e, chunk, blk;
+    int p0, nt;                     // first grouped row, rows in the chunk
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int groups_of(int n_e, int max_rows, int GB) {
+    return (n_e > 0 && n_e <= max_rows) ? ceil_div(n_e, kTok) * GB : 0;
+}
+
+// Group t (in expert-major, chunk-major order) -> expert, chunk, group
+// index within the chunk (returned in blk).
+__device__ __forceinline__ Task group_of(int t, const int32_t *off,
+                                         const int32_t *pre, int E, int GB) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    Task k;
+    k.e = lo;
+    const int local = t - pre[lo];
+    k.chunk = local / GB;
+    k.blk = local - k.chunk * GB;
+    k.p0 = off[lo] + k.chunk * kTok;
+    k.nt = min(kTok, off[lo + 1] - k.p0);
+    return k;
+}
+
+// Physical 16-byte chunk of logical chunk q of token row n in the staged
+// activations (bank swizzle for the B-fragment loads).
+__device__ __forceinline__ int xs_chunk(int q, int n) {
+    return (q & ~7) | ((q & 7) ^ ((q >> 3) & 1) ^ ((n & 1) << 1));
+}
+
+// 8 consecutive 16-bit values (uint4) -> K order (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ uint4 permute8(uint4 v) {
+    return make_uint4(__byte_perm(v.x, v.z, 0x5410),
+                      __byte_perm(v.x, v.z, 0x7632),
+                      __byte_perm(v.y, v.w, 0x5410),
+                      __byte_perm(v.y, v.w, 0x7632));
+}
+
+// bf16 value -> f16 bits, and whether the conversion is exact (zero, or
+// 2^-17 <= |x| <= 65504: eight significant bits fit f16 there).
+__device__ __forceinline__ uint32_t bf16_to_f16_exact(uint32_t b, bool *ok) {
+    const uint32_t ex = (b >> 7) & 0xFFu;
+    *ok = ((b & 0x7FFFu) == 0) || (ex >= 110u && ex <= 142u);
+    return __half_as_ushort(__float2half_rn(__uint_as_float(b << 16)));
+}
+
+// The four pairs {n_j - 8, n_{j+4} - 8}, j = 0..3, of one packed word, as
+// bf16x2 (nibble in the mantissa of 128.0, minus 136) ...
+__device__ __forceinline__ void word_pairs_bf16(uint32_t w, uint32_t (&r)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v);
+        b = __hsub2(b, __halves2bfloat162(__ushort_as_bfloat16(0x4308),
+                                          __ushort_as_bfloat16(0x4308)));
+        r[j] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+}
+
+// ... or as f16x2: the low nibble of a byte lands in the mantissa of 1024.0
+// (minus 1032), the high one in the mantissa at 16x (times 1/16, minus 72);
+// all exact.
+__device__ __forceinline__ void word_pairs_f16(uint32_t w, uint32_t (&r)[4]) {
+    const uint32_t ws = w >> 8;
+    const uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u;
+    const uint32_t v1 = (w & 0x00F000F0u) | 0x64006400u;
+    const uint32_t v2 = (ws & 0x000F000Fu) | 0x64006400u;
+    const uint32_t v3 = (ws & 0x00F000F0u) | 0x64006400u;
+    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408),
+                                         __ushort_as_half(0x6408));
+    const __half2 k16 = __halves2half2(__ushort_as_half(0x2C00),
+                                       __ushort_as_half(0x2C00));
+    const __half2 km72 = __halves2half2(__ushort_as_half(0xD480),
+                                        __ushort_as_half(0xD480));
+    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2 *>(&v0), k1032);
+    const __half2 h1 = __hfma2(*reinterpret_cast<const __half2 *>(&v1), k16,
+                               km72);
+    const __half2 h2 = __hsub2(*reinterpret_cast<const __half2 *>(&v2), k1032);
+    const __half2 h3 = __hfma2(*reinterpret_cast<const __half2 *>(&v3), k16,
+                               km72);
+    r[0] = *reinterpret_cast<const uint32_t *>(&h0);
+    r[1] = *reinterpret_cast<const uint32_t *>(&h1);
+    r[2] = *reinterpret_cast<const uint32_t *>(&h2);
+    r[3] = *reinterpret_cast<const uint32_t *>(&h3);
+}
+
+template <bool kF16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0,
+                                          uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+    if (kF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One K step of one warp: w[0..3] = 16 bytes of gate row g, up row g,
+// gate row 8+g, up row 8+g; xb = the four 16-byte activation chunks.
+template <bool kF16>
+__device__ __forceinline__ void step_mma(float (&acc)[2][4],
+                                         const uint4 (&w)[4],
+                                         const uint4 (&xb)[4]) {
+    const uint32_t *wg0 = reinterpret_cast<const uint32_t *>(&w[0]);
+    const uint32_t *wu0 = reinterpret_cast<const uint32_t *>(&w[1]);
+    const uint32_t *wg1 = reinterpret_cast<const uint32_t *>(&w[2]);
+    const uint32_t *wu1 = reinterpret_cast<const uint32_t *>(&w[3]);
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        uint32_t g0[4], u0[4], g1[4], u1[4];
+        if (kF16) {
+            word_pairs_f16(wg0[wd], g0);
+            word_pairs_f16(wu0[wd], u0);
+            word_pairs_f16(wg1[wd], g1);
+            word_pairs_f16(wu1[wd], u1);
+        } else {
+            word_pairs_bf16(wg0[wd], g0);
+            word_pairs_bf16(wu0[wd], u0);
+            word_pairs_bf16(wg1[wd], g1);
+            word_pairs_bf16(wu1[wd], u1);
+        }
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xb[wd]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mma_16816<kF16>(acc[0], g0[2 * h], u0[2 * h], g0[2 * h + 1],
+                            u0[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
+            mma_16816<kF16>(acc[1], g1[2 * h], u1[2 * h], g1[2 * h + 1],
+                            u1[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
+        }
+    }
+}
+
+// Work is handed out in groups: a group is 8/S consecutive blocks of 16
+// intermediate rows of one (expert, chunk), one task per slot of S warps;
+// the S warps of a slot split the task's K steps (warp kpart takes steps
+// kpart, kpart+S, ...).  S = 1 streams whole rows per warp with no barrier
+// inside a group; S = 8 spreads the few tasks of a tiny call over all warps.
+template <int S>
+__global__ void __launch_bounds__(kThreads, 2)
+matvec_mma_kernel(GateUpArgs a, int tok_cap) {
+    constexpr int kSlots = kWarps / S;
+    constexpr int D = 3;                          // K steps in flight
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int E = a.E;
+    const int H = (int)a.H;
+    float4 *red = reinterpret_cast<float4 *>(smem);          // [8][32][2]
+    int32_t *s_off = reinterpret_cast<int32_t *>(red + kWarps * 32 * 2);
+    int32_t *s_pre = s_off + (E + 1);
+    int *s_flag = s_pre + (E + 1);
+    uint8_t *xs = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(s_flag + 1) + 127) &
+        ~uintptr_t(127));                                     // [tok_cap][H]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int slot = warp / S, kpart = warp - slot * S;
+    const int IBk = (int)(a.I / kRowsPerTask);
+    const int GB = ceil_div(IBk, kSlots);          // groups per chunk
+    const int steps = H / kStepK;                  // K steps in a row
+    const int spw = ceil_div(steps, S);            // steps per warp per task
+
+    if (!stage_row_offsets(a, s_off))
+        return;
+    if (warp == 0) {
+        const int per = ceil_div(E, 32);
+        const int e0 = lane * per;
+        int sum = 0;
+        for (int e = e0; e < min(E, e0 + per); ++e)
+            sum += groups_of(s_off[e + 1] - s_off[e], a.matvec_max_rows, GB);
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += v;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < min(E, e0 + per); ++e) {
+            s_pre[e] = run;
+            run += groups_of(s_off[e + 1] - s_off[e], a.matvec_max_rows, GB);
+        }
+        if (lane == 31)
+            s_pre[E] = incl;
+    }
+    __syncthreads();
+    const int ngroups = s_pre[E];
+    const int gr_begin = (int)((int64_t)ngroups * blockIdx.x / gridDim.x);
+    const int gr_end = (int)((int64_t)ngroups * (blockIdx.x + 1) / gridDim.x);
+    if (gr_begin >= gr_end)
+        return;
+    const int ngr = gr_end - gr_begin;
+    const int total = ngr * spw;                   // this warp's K steps
+
+    auto task_at = [&](int gi) {
+        Task k = group_of(gr_begin + gi, s_off, s_pre, E, GB);
+        k.blk = k.blk * kSlots + slot;             // this slot's block
+        return k;
+    };
+
+    // --- load cursor: runs D steps ahead of the multiply
+    const int64_t row_bytes = a.H / 2;
+    int lgi = 0, lm = 0;
+    Task lt = task_at(0);
+    const uint8_t *lslab = expert_slab(a, lt.e);
+    auto load_next = [&](uint4 (&r)[4]) {
+        r[0] = r[1] = r[2] = r[3] = make_uint4(0, 0, 0, 0);
+        if (lgi < ngr) {
+            const int kc = kpart + S * lm;
+            if (kc < steps && lt.blk < IBk && lslab != nullptr) {
+                const int64_t off =
+                    ((int64_t)lt.blk * kRowsPerTask + g) * row_bytes +
+                    kc * 64 + tq * 16;
+                const uint8_t *gp = lslab + a.gate_w_off + off;
+                const uint8_t *up = lslab + a.up_w_off + off;
+                r[0] = __ldg(reinterpret_cast<const uint4 *>(gp));
+                r[1] = __ldg(reinterpret_cast<const uint4 *>(up));
+                r[2] = __ldg(reinterpret_cast<const uint4 *>(gp + 8 * row_bytes));
+                r[3] = __ldg(reinterpret_cast<const uint4 *>(up + 8 * row_bytes));
+            }
+            if (++lm == spw) {
+                lm = 0;
+                if (++lgi < ngr) {
+                    lt = task_at(lgi);
+                    lslab = expert_slab(a, lt.e);
+                }
+            }
+        }
+    };
+
+    uint4 ring[D][4];
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+        load_next(ring[d]);
+
+    float acc[2][4];
+    int staged_e = -1, staged_chunk = -1;
+    bool f16 = false;
+    Task k{};
+    int gi = 0, m = 0;
+
+    for (int j0 = 0; j0 < total; j0 += D) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            if (j0 + d >= total)
+                break;
+            if (m == 0) {
+                k = task_at(gi);
+                if (k.e != staged_e || k.chunk != staged_chunk) {
+                    __syncthreads();      // everyone is done with the old x
+                    if (tid == 0)
+                        *s_flag = 0;
+                    __syncthreads();
+                    // stage the chunk: f16 when every value converts exactly
+                    const int qn = H / 8;
+                    bool exact = true;
+                    for (int idx = tid; idx < k.nt * qn; idx += kThreads) {
+                        const int n = idx / qn, q = idx - n * qn;
+                        const int64_t tok = row_token(a, k.p0 + n);
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (tok >= 0)
+                            v = __ldg(reinterpret_cast<const uint4 *>(
+                                          a.x + tok * a.H) + q);
+                        bool e0, e1, e2, e3, e4, e5, e6, e7;
+                        const uint4 hv = make_uint4(
+                            bf16_to_f16_exact(v.x & 0xFFFFu, &e0) |
+                                (bf16_to_f16_exact(v.x >> 16, &e1) << 16),
+                            bf16_to_f16_exact(v.y & 0xFFFFu, &e2) |
+                                (bf16_to_f16_exact(v.y >> 16, &e3) << 16),
+                            bf16_to_f16_exact(v.z & 0xFFFFu, &e4) |
+                                (bf16_to_f16_exact(v.z >> 16, &e5) << 16),
+                            bf16_to_f16_exact(v.w & 0xFFFFu, &e6) |
+                                (bf16_to_f16_exact(v.w >> 16, &e7) << 16));
+                        exact = exact && e0 && e1 && e2 && e3 && e4 && e5 &&
+                                e6 && e7;
+                        uint8_t *dst = xs + (int64_t)n * H * 2 +
+                                       xs_chunk(q, n) * 16;
+                        *reinterpret_cast<uint4 *>(dst) = permute8(hv);
+                    }
+                    if (!exact)
+                        *s_flag = 1;
+                    __syncthreads();
+                    f16 = (*s_flag == 0);
+                    if (!f16) {
+                        // some value is not exact in f16: keep bf16
+                        for (int idx = tid; idx < k.nt * qn; idx += kThreads) {
+                            const int n = idx / qn, q = idx - n * qn;
+                            const int64_t tok = row_token(a, k.p0 + n);
+                            uint4 v = make_uint4(0, 0, 0, 0);
+                            if (tok >= 0)
+                                v = __ldg(reinterpret_cast<const uint4 *>(
+                                              a.x + tok * a.H) + q);
+                            *reinterpret_cast<uint4 *>(
+                                xs + (int64_t)n * H * 2 +
+                                xs_chunk(q, n) * 16) = permute8(v);
+                        }
+                        __syncthreads();
+                    }
+                    staged_e = k.e;
+                    staged_chunk = k.chunk;
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.0f;
+            }
+            const int kc = kpart + S * m;
+            if (kc < steps && k.blk < IBk) {
+                uint4 xb[4];
+                const uint8_t *xrow = xs + (int64_t)g * H * 2;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int q = kc * 16 + tq * 4 + q4;
+                    xb[q4] = g < k.nt ? *reinterpret_cast<const uint4 *>(
+                                            xrow + xs_chunk(q, g) * 16)
+                                      : make_uint4(0, 0, 0, 0);
+                }
+                if (f16)
+                    step_mma<true>(acc, ring[d], xb);
+                else
+                    step_mma<false>(acc, ring[d], xb);
+            }
+            load_next(ring[d]);
+            if (m == spw - 1) {
+                // the task is complete: sum over the slot's warps
+                if (S > 1) {
+                    red[(warp * 32 + lane) * 2] = make_float4(
+                        acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+                    red[(warp * 32 + lane) * 2 + 1] = make_float4(
+                        acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+                    __syncthreads();
+                    if (kpart == 0) {
+                        for (int w = 1; w < S; ++w) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const float4 v =
+                                    red[((warp + w) * 32 + lane) * 2 + r];
+                                acc[r][0] += v.x;
+                                acc[r][1] += v.y;
+                                acc[r][2] += v.z;
+                                acc[r][3] += v.w;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+                const uint8_t *slab = expert_slab(a, k.e);
+                if (kpart == 0 && k.blk < IBk && slab != nullptr) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int64_t i =
+                            (int64_t)k.blk * kRowsPerTask + 8 * r + g;
+                        const float sg = reinterpret_cast<const float *>(
+                            slab + a.gate_s_off)[i];
+                        const float su = reinterpret_cast<const float *>(
+                            slab + a.up_s_off)[i];
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int n = 2 * tq + jj;
+                            if (n < k.nt) {
+                                const float g32 = __fmul_rn(acc[r][jj], sg);
+                                const float u32 =
+                                    __fmul_rn(acc[r][2 + jj], su);
+                                const int64_t o =
+                                    (int64_t)(k.p0 + n) * a.I + i;
+                                a.out[o] = swiglu_out(g32, u32);
+                                if (a.gate_f32)
+                                    a.gate_f32[o] = g32;
+                                if (a.up_f32)
+                                    a.up_f32[o] = u32;
+                            }
+                        }
+                    }
+                }
+            }
+            if (++m == spw) {
+                m = 0;
+                ++gi;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+bool matvec_mma_supported(const GateUpArgs &a) {
+    return a.H % kStepK == 0 && a.I % kRowsPerTask == 0 &&
+           a.gate_w_off % 16 == 0 && a.up_w_off % 16 == 0 &&
+           a.H <= 16384;
+}
+
+template <int S>
+cudaError_t launch_split(const GateUpArgs &a, size_t smem, int tok_cap,
+                         cudaStream_t s) {
+    cudaError_t err = cudaFuncSetAttribute(
+        matvec_mma_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    matvec_mma_kernel<S><<<2 * a.num_sms, kThreads, smem, s>>>(a, tok_cap);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Few grouped rows (a tiny call) -> split K over all 8 warps; otherwise
+// whole tasks per warp.
+cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s) {
+    const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
+    const size_t smem = sizeof(float4) * kWarps * 32 * 2 +
+                        sizeof(int32_t) * (2 * (size_t)(a.E + 1) + 1) + 128 +
+                        (size_t)tok_cap * (size_t)a.H * 2;
+    if (a.M < 16)
+        return launch_split<8>(a, smem, tok_cap, s);
+    return launch_split<1>(a, smem, tok_cap, s);
+}
+
+}  // namespace q4moe
