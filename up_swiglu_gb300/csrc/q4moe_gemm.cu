@@ -185,11 +185,22 @@ __device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity) {
     }
 }
 
-// Copy each grouped row's activations into the workspace (bf16 [M][H]).
+// Copy the activations of each grouped row that the GEMM will read (rows of
+// experts above the matvec's row limit) into the workspace, bf16 [M][H].
 __global__ void __launch_bounds__(128)
 gather_rows_kernel(GateUpArgs a) {
     const int64_t chunks = a.H / 8;
     for (int64_t p = blockIdx.x; p < a.M; p += gridDim.x) {
+        int lo = 0, hi = a.E;         // expert e with off[e] <= p < off[e+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.row_offsets[mid] <= p)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        if (a.row_offsets[lo + 1] - a.row_offsets[lo] <= a.matvec_max_rows)
+            continue;
         const int64_t t = row_token(a, p);
         uint4 *dst = reinterpret_cast<uint4 *>(a.xg + p * a.H);
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * a.H);

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 16;   // ids each lane loads at once
 
 __global__ void __launch_bounds__(kThreads, 1)
 group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
@@ -45,21 +46,27 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
     const int32_t q0 = min(pairs, warp * seg), q1 = min(pairs, q0 + seg);
     int32_t *cnt = s_cnt + warp * E;
 
-    // 1. per-warp counts
-    for (int32_t b = q0; b < q1; b += 32) {
-        const int32_t q = b + lane;
-        int32_t e = -1;
-        if (q < q1) {
-            e = topk[q];
-            if (e < 0 || e >= E) {
+    // 1. per-warp counts; each lane loads kBatch ids before using any, so a
+    //    warp waits for one memory latency per 32*kBatch pairs
+    for (int32_t b0 = q0; b0 < q1; b0 += 32 * kBatch) {
+        int32_t ids[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int32_t q = b0 + i * 32 + lane;
+            ids[i] = q < q1 ? topk[q] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            int32_t e = ids[i];
+            if (b0 + i * 32 + lane < q1 && (e < 0 || e >= E)) {
                 e = -1;
                 s_bad = 1;
             }
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && (peers & lt_mask) == 0)
+                cnt[e] += __popc(peers);
+            __syncwarp();
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & lt_mask) == 0)
-            cnt[e] += __popc(peers);
-        __syncwarp();
     }
     __syncthreads();
 
@@ -106,28 +113,34 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs, int32_t k,
         atomicOr(status, Q4MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
 
-    // 3. stable scatter
-    for (int32_t b = q0; b < q1; b += 32) {
-        const int32_t q = b + lane;
-        int32_t e = -1;
-        if (q < q1) {
-            e = topk[q];
+    // 3. stable scatter (the ids are read again, kBatch per lane at once)
+    for (int32_t b0 = q0; b0 < q1; b0 += 32 * kBatch) {
+        int32_t ids[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int32_t q = b0 + i * 32 + lane;
+            ids[i] = q < q1 ? topk[q] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int32_t q = b0 + i * 32 + lane;
+            int32_t e = ids[i];
             if (e < 0 || e >= E)
                 e = -1;
-        }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & lt_mask);
-        int32_t row = -1;
-        if (e >= 0)
-            row = s_tot[e] + cnt[e] + rank;
-        __syncwarp();
-        if (e >= 0 && rank == 0)
-            cnt[e] += __popc(peers);
-        __syncwarp();
-        if (q < q1) {
-            row_of_pair[q] = row;
-            if (row >= 0)
-                token_of_row[row] = q / k;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & lt_mask);
+            int32_t row = -1;
+            if (e >= 0)
+                row = s_tot[e] + cnt[e] + rank;
+            __syncwarp();
+            if (e >= 0 && rank == 0)
+                cnt[e] += __popc(peers);
+            __syncwarp();
+            if (q < q1) {
+                row_of_pair[q] = row;
+                if (row >= 0)
+                    token_of_row[row] = q / k;
+            }
         }
     }
 }

@@ -83,14 +83,6 @@ __device__ __forceinline__ uint4 permute8(uint4 v) {
                       __byte_perm(v.y, v.w, 0x7632));
 }
 
-// bf16 value -> f16 bits, and whether the conversion is exact (zero, or
-// 2^-17 <= |x| <= 65504: eight significant bits fit f16 there).
-__device__ __forceinline__ uint32_t bf16_to_f16_exact(uint32_t b, bool *ok) {
-    const uint32_t ex = (b >> 7) & 0xFFu;
-    *ok = ((b & 0x7FFFu) == 0) || (ex >= 110u && ex <= 142u);
-    return __half_as_ushort(__float2half_rn(__uint_as_float(b << 16)));
-}
-
 // The four pairs {n_j - 8, n_{j+4} - 8}, j = 0..3, of one packed word, as
 // bf16x2 (nibble in the mantissa of 128.0, minus 136) ...
 __device__ __forceinline__ void word_pairs_bf16(uint32_t w, uint32_t (&r)[4]) {
@@ -104,55 +96,19 @@ __device__ __forceinline__ void word_pairs_bf16(uint32_t w, uint32_t (&r)[4]) {
     }
 }
 
-// ... or as f16x2: the low nibble of a byte lands in the mantissa of 1024.0
-// (minus 1032), the high one in the mantissa at 16x (times 1/16, minus 72);
-// all exact.
-__device__ __forceinline__ void word_pairs_f16(uint32_t w, uint32_t (&r)[4]) {
-    const uint32_t ws = w >> 8;
-    const uint32_t v0 = (w & 0x000F000Fu) | 0x64006400u;
-    const uint32_t v1 = (w & 0x00F000F0u) | 0x64006400u;
-    const uint32_t v2 = (ws & 0x000F000Fu) | 0x64006400u;
-    const uint32_t v3 = (ws & 0x00F000F0u) | 0x64006400u;
-    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408),
-                                         __ushort_as_half(0x6408));
-    const __half2 k16 = __halves2half2(__ushort_as_half(0x2C00),
-                                       __ushort_as_half(0x2C00));
-    const __half2 km72 = __halves2half2(__ushort_as_half(0xD480),
-                                        __ushort_as_half(0xD480));
-    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2 *>(&v0), k1032);
-    const __half2 h1 = __hfma2(*reinterpret_cast<const __half2 *>(&v1), k16,
-                               km72);
-    const __half2 h2 = __hsub2(*reinterpret_cast<const __half2 *>(&v2), k1032);
-    const __half2 h3 = __hfma2(*reinterpret_cast<const __half2 *>(&v3), k16,
-                               km72);
-    r[0] = *reinterpret_cast<const uint32_t *>(&h0);
-    r[1] = *reinterpret_cast<const uint32_t *>(&h1);
-    r[2] = *reinterpret_cast<const uint32_t *>(&h2);
-    r[3] = *reinterpret_cast<const uint32_t *>(&h3);
-}
-
-template <bool kF16>
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0,
                                           uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0,
                                           uint32_t b1) {
-    if (kF16)
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    else
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // One K step of one warp: w[0..3] = 16 bytes of gate row g, up row g,
 // gate row 8+g, up row 8+g; xb = the four 16-byte activation chunks.
-template <bool kF16>
 __device__ __forceinline__ void step_mma(float (&acc)[2][4],
                                          const uint4 (&w)[4],
                                          const uint4 (&xb)[4]) {
@@ -163,24 +119,17 @@ __device__ __forceinline__ void step_mma(float (&acc)[2][4],
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
         uint32_t g0[4], u0[4], g1[4], u1[4];
-        if (kF16) {
-            word_pairs_f16(wg0[wd], g0);
-            word_pairs_f16(wu0[wd], u0);
-            word_pairs_f16(wg1[wd], g1);
-            word_pairs_f16(wu1[wd], u1);
-        } else {
-            word_pairs_bf16(wg0[wd], g0);
-            word_pairs_bf16(wu0[wd], u0);
-            word_pairs_bf16(wg1[wd], g1);
-            word_pairs_bf16(wu1[wd], u1);
-        }
+        word_pairs_bf16(wg0[wd], g0);
+        word_pairs_bf16(wu0[wd], u0);
+        word_pairs_bf16(wg1[wd], g1);
+        word_pairs_bf16(wu1[wd], u1);
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xb[wd]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            mma_16816<kF16>(acc[0], g0[2 * h], u0[2 * h], g0[2 * h + 1],
-                            u0[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
-            mma_16816<kF16>(acc[1], g1[2 * h], u1[2 * h], g1[2 * h + 1],
-                            u1[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
+            mma_16816(acc[0], g0[2 * h], u0[2 * h], g0[2 * h + 1],
+                      u0[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
+            mma_16816(acc[1], g1[2 * h], u1[2 * h], g1[2 * h + 1],
+                      u1[2 * h + 1], xw[2 * h], xw[2 * h + 1]);
         }
     }
 }
@@ -194,16 +143,15 @@ template <int S>
 __global__ void __launch_bounds__(kThreads, 2)
 matvec_mma_kernel(GateUpArgs a, int tok_cap) {
     constexpr int kSlots = kWarps / S;
-    constexpr int D = 3;                          // K steps in flight
+    constexpr int D = 2;                          // K steps in flight
     extern __shared__ __align__(16) uint8_t smem[];
     const int E = a.E;
     const int H = (int)a.H;
     float4 *red = reinterpret_cast<float4 *>(smem);          // [8][32][2]
     int32_t *s_off = reinterpret_cast<int32_t *>(red + kWarps * 32 * 2);
     int32_t *s_pre = s_off + (E + 1);
-    int *s_flag = s_pre + (E + 1);
     uint8_t *xs = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(s_flag + 1) + 127) &
+        (reinterpret_cast<uintptr_t>(s_pre + (E + 1)) + 127) &
         ~uintptr_t(127));                                     // [tok_cap][H]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -252,35 +200,53 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
         return k;
     };
 
-    // --- load cursor: runs D steps ahead of the multiply
+    // --- load cursor: runs D steps ahead of the multiply; the row pointers
+    //     of the cursor's task are formed once per task
     const int64_t row_bytes = a.H / 2;
     int lgi = 0, lm = 0;
-    Task lt = task_at(0);
-    const uint8_t *lslab = expert_slab(a, lt.e);
+    const uint8_t *lg = nullptr, *lu = nullptr;    // gate / up rows of lane
+    auto set_load_task = [&](int gi) {
+        const Task t = task_at(gi);
+        const uint8_t *slab = expert_slab(a, t.e);
+        lg = lu = nullptr;
+        if (slab != nullptr && t.blk < IBk) {
+            const int64_t off =
+                ((int64_t)t.blk * kRowsPerTask + g) * row_bytes + tq * 16 +
+                (int64_t)kpart * 64;
+            lg = slab + a.gate_w_off + off;
+            lu = slab + a.up_w_off + off;
+        }
+    };
+    set_load_task(0);
     auto load_next = [&](uint4 (&r)[4]) {
         r[0] = r[1] = r[2] = r[3] = make_uint4(0, 0, 0, 0);
         if (lgi < ngr) {
-            const int kc = kpart + S * lm;
-            if (kc < steps && lt.blk < IBk && lslab != nullptr) {
-                const int64_t off =
-                    ((int64_t)lt.blk * kRowsPerTask + g) * row_bytes +
-                    kc * 64 + tq * 16;
-                const uint8_t *gp = lslab + a.gate_w_off + off;
-                const uint8_t *up = lslab + a.up_w_off + off;
-                r[0] = __ldg(reinterpret_cast<const uint4 *>(gp));
-                r[1] = __ldg(reinterpret_cast<const uint4 *>(up));
-                r[2] = __ldg(reinterpret_cast<const uint4 *>(gp + 8 * row_bytes));
-                r[3] = __ldg(reinterpret_cast<const uint4 *>(up + 8 * row_bytes));
+            if (lg != nullptr && kpart + S * lm < steps) {
+                const int64_t o = (int64_t)lm * (S * 64);
+                r[0] = __ldg(reinterpret_cast<const uint4 *>(lg + o));
+                r[1] = __ldg(reinterpret_cast<const uint4 *>(lu + o));
+                r[2] = __ldg(reinterpret_cast<const uint4 *>(
+                    lg + o + 8 * row_bytes));
+                r[3] = __ldg(reinterpret_cast<const uint4 *>(
+                    lu + o + 8 * row_bytes));
             }
             if (++lm == spw) {
                 lm = 0;
-                if (++lgi < ngr) {
-                    lt = task_at(lgi);
-                    lslab = expert_slab(a, lt.e);
-                }
+                if (++lgi < ngr)
+                    set_load_task(lgi);
             }
         }
     };
+
+    // byte offsets (within the staged activations) of this thread's four
+    // B-fragment chunks at K step 0; step kc adds kc * 256
+    const int xrow = min(g, tok_cap - 1);
+    int xoff[4];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+        xoff[q4] = xrow * H * 2 +
+                   ((tq >> 1) * 8 +
+                    (((tq & 1) * 4 + q4) ^ (tq >> 1) ^ ((xrow & 1) << 1))) * 16;
 
     uint4 ring[D][4];
 #pragma unroll
@@ -289,7 +255,6 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
 
     float acc[2][4];
     int staged_e = -1, staged_chunk = -1;
-    bool f16 = false;
     Task k{};
     int gi = 0, m = 0;
 
@@ -302,12 +267,8 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                 k = task_at(gi);
                 if (k.e != staged_e || k.chunk != staged_chunk) {
                     __syncthreads();      // everyone is done with the old x
-                    if (tid == 0)
-                        *s_flag = 0;
-                    __syncthreads();
-                    // stage the chunk: f16 when every value converts exactly
+                    // stage the chunk's activations: permuted, swizzled
                     const int qn = H / 8;
-                    bool exact = true;
                     for (int idx = tid; idx < k.nt * qn; idx += kThreads) {
                         const int n = idx / qn, q = idx - n * qn;
                         const int64_t tok = row_token(a, k.p0 + n);
@@ -315,41 +276,11 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                         if (tok >= 0)
                             v = __ldg(reinterpret_cast<const uint4 *>(
                                           a.x + tok * a.H) + q);
-                        bool e0, e1, e2, e3, e4, e5, e6, e7;
-                        const uint4 hv = make_uint4(
-                            bf16_to_f16_exact(v.x & 0xFFFFu, &e0) |
-                                (bf16_to_f16_exact(v.x >> 16, &e1) << 16),
-                            bf16_to_f16_exact(v.y & 0xFFFFu, &e2) |
-                                (bf16_to_f16_exact(v.y >> 16, &e3) << 16),
-                            bf16_to_f16_exact(v.z & 0xFFFFu, &e4) |
-                                (bf16_to_f16_exact(v.z >> 16, &e5) << 16),
-                            bf16_to_f16_exact(v.w & 0xFFFFu, &e6) |
-                                (bf16_to_f16_exact(v.w >> 16, &e7) << 16));
-                        exact = exact && e0 && e1 && e2 && e3 && e4 && e5 &&
-                                e6 && e7;
-                        uint8_t *dst = xs + (int64_t)n * H * 2 +
-                                       xs_chunk(q, n) * 16;
-                        *reinterpret_cast<uint4 *>(dst) = permute8(hv);
+                        *reinterpret_cast<uint4 *>(
+                            xs + (int64_t)n * H * 2 + xs_chunk(q, n) * 16) =
+                            permute8(v);
                     }
-                    if (!exact)
-                        *s_flag = 1;
                     __syncthreads();
-                    f16 = (*s_flag == 0);
-                    if (!f16) {
-                        // some value is not exact in f16: keep bf16
-                        for (int idx = tid; idx < k.nt * qn; idx += kThreads) {
-                            const int n = idx / qn, q = idx - n * qn;
-                            const int64_t tok = row_token(a, k.p0 + n);
-                            uint4 v = make_uint4(0, 0, 0, 0);
-                            if (tok >= 0)
-                                v = __ldg(reinterpret_cast<const uint4 *>(
-                                              a.x + tok * a.H) + q);
-                            *reinterpret_cast<uint4 *>(
-                                xs + (int64_t)n * H * 2 +
-                                xs_chunk(q, n) * 16) = permute8(v);
-                        }
-                        __syncthreads();
-                    }
                     staged_e = k.e;
                     staged_chunk = k.chunk;
                 }
@@ -359,19 +290,14 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
             }
             const int kc = kpart + S * m;
             if (kc < steps && k.blk < IBk) {
+                // B fragments: rows past the chunk read a stale in-bounds
+                // row; those output columns are never stored
                 uint4 xb[4];
-                const uint8_t *xrow = xs + (int64_t)g * H * 2;
+                const uint8_t *xk = xs + kc * 256;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int q = kc * 16 + tq * 4 + q4;
-                    xb[q4] = g < k.nt ? *reinterpret_cast<const uint4 *>(
-                                            xrow + xs_chunk(q, g) * 16)
-                                      : make_uint4(0, 0, 0, 0);
-                }
-                if (f16)
-                    step_mma<true>(acc, ring[d], xb);
-                else
-                    step_mma<false>(acc, ring[d], xb);
+                for (int q4 = 0; q4 < 4; ++q4)
+                    xb[q4] = *reinterpret_cast<const uint4 *>(xk + xoff[q4]);
+                step_mma(acc, ring[d], xb);
             }
             load_next(ring[d]);
             if (m == spw - 1) {
@@ -460,7 +386,7 @@ cudaError_t launch_split(const GateUpArgs &a, size_t smem, int tok_cap,
 cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s) {
     const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
     const size_t smem = sizeof(float4) * kWarps * 32 * 2 +
-                        sizeof(int32_t) * (2 * (size_t)(a.E + 1) + 1) + 128 +
+                        sizeof(int32_t) * 2 * (size_t)(a.E + 1) + 128 +
                         (size_t)tok_cap * (size_t)a.H * 2;
     if (a.M < 16)
         return launch_split<8>(a, smem, tok_cap, s);
