@@ -6,12 +6,10 @@
 // expert's rows in the chunk (the shared-row idea of page 57's
 // GATEUP_SHARED_M_SOURCE), the dot products accumulate in f32.
 //
-// Task = (expert, chunk of up to 8 grouped rows, block of 8 intermediate
-// rows).  A CTA of 8 warps owns one task at a time and splits its K range:
-// warp w takes the 128-wide K steps w, w+8, ...  For one K step a thread
-// (group g = lane/4, quad member t = lane%4) holds 16 bytes (32 nibbles) of
-// gate row g and of up row g and issues eight mma.sync.m16n8k16 (bf16 in,
-// f32 accumulate) with
+// Task = (expert, chunk of up to 8 grouped rows, block of 16 intermediate
+// rows).  For one 128-wide K step a thread (group g = lane/4, quad member
+// t = lane%4) holds 16 bytes (32 nibbles) of gate and up rows g and 8+g and
+// issues sixteen mma.sync.m16n8k16 (bf16 in, f32 accumulate) with
 //   A rows 0-7  = gate rows, A rows 8-15 = up rows of the same 8 i,
 //   B columns   = the chunk's 8 grouped rows (tokens),
 // so the C fragment of a thread already pairs gate and up of one i.
@@ -21,16 +19,17 @@
 // MMA follows that pairing; the activations are staged once per chunk in
 // shared memory in the matching order ((0,4,1,5,2,6,3,7) within each group
 // of 8) and bank-swizzled so that the B fragments load without conflicts.
-// Each warp prefetches the weights of its next K steps into registers while
-// it multiplies the current ones.  Partial sums meet in shared memory in a
-// fixed warp order (deterministic, and a row's bits do not depend on the
-// other rows of its chunk); warp 0 applies the scales and the tail.
+// Each thread keeps the weights of its next K steps in flight through a
+// shared-memory ring (cp.async) while it multiplies the current ones.  When
+// warps split a task's K, their partial sums meet in shared memory in a fixed
+// warp order; results are deterministic and a row's bits do not depend on
+// the other rows of its chunk.
 #include "q4moe_internal.cuh"
 
 namespace q4moe {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerTask = 16;    // intermediate rows (two MMA row tiles)
 constexpr int kTok = 8;             // grouped rows per chunk
@@ -134,25 +133,43 @@ __device__ __forceinline__ void step_mma(float (&acc)[2][4],
     }
 }
 
-// Work is handed out in groups: a group is 8/S consecutive blocks of 16
+// cp.async of 16 bytes global -> shared (bypassing L1) and its waits.
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Work is handed out in groups: a group is 16/S consecutive blocks of 16
 // intermediate rows of one (expert, chunk), one task per slot of S warps;
 // the S warps of a slot split the task's K steps (warp kpart takes steps
 // kpart, kpart+S, ...).  S = 1 streams whole rows per warp with no barrier
-// inside a group; S = 8 spreads the few tasks of a tiny call over all warps.
-template <int S>
-__global__ void __launch_bounds__(kThreads, 2)
+// inside a group; S = 16 spreads the few tasks of a tiny call over all
+// warps.  Each thread copies its own weight bytes for the next R steps into
+// a shared-memory ring with cp.async and reads back only those bytes, so its
+// own cp.async.wait_group is all the synchronisation the ring needs.
+template <int S, int R>
+__global__ void __launch_bounds__(kThreads, 1)
 matvec_mma_kernel(GateUpArgs a, int tok_cap) {
     constexpr int kSlots = kWarps / S;
-    constexpr int D = 2;                          // K steps in flight
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     const int E = a.E;
     const int H = (int)a.H;
-    float4 *red = reinterpret_cast<float4 *>(smem);          // [8][32][2]
-    int32_t *s_off = reinterpret_cast<int32_t *>(red + kWarps * 32 * 2);
+    // [kWarps][R][4][32] x 16 B weight ring, then the staged activations,
+    // the reduction buffer (S > 1) and the row offsets
+    uint8_t *ring = smem;
+    uint8_t *xs = ring + (size_t)kWarps * R * 4 * 32 * 16;
+    float4 *red = reinterpret_cast<float4 *>(xs + (size_t)tok_cap * H * 2);
+    int32_t *s_off = reinterpret_cast<int32_t *>(
+        red + (S > 1 ? kWarps * 32 * 2 : 0));
     int32_t *s_pre = s_off + (E + 1);
-    uint8_t *xs = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(s_pre + (E + 1)) + 127) &
-        ~uintptr_t(127));                                     // [tok_cap][H]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
@@ -200,12 +217,11 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
         return k;
     };
 
-    // --- load cursor: runs D steps ahead of the multiply; the row pointers
-    //     of the cursor's task are formed once per task
+    // --- copy cursor: R steps ahead of the multiply
     const int64_t row_bytes = a.H / 2;
     int lgi = 0, lm = 0;
     const uint8_t *lg = nullptr, *lu = nullptr;    // gate / up rows of lane
-    auto set_load_task = [&](int gi) {
+    auto set_copy_task = [&](int gi) {
         const Task t = task_at(gi);
         const uint8_t *slab = expert_slab(a, t.e);
         lg = lu = nullptr;
@@ -217,57 +233,60 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
             lu = slab + a.up_w_off + off;
         }
     };
-    set_load_task(0);
-    auto load_next = [&](uint4 (&r)[4]) {
-        r[0] = r[1] = r[2] = r[3] = make_uint4(0, 0, 0, 0);
+    const uint32_t ring0 =
+        static_cast<uint32_t>(__cvta_generic_to_shared(ring)) +
+        (uint32_t)(warp * R * 4 * 32 + lane) * 16;
+    auto copy_next = [&](int r) {                  // into ring slot r
         if (lgi < ngr) {
             if (lg != nullptr && kpart + S * lm < steps) {
                 const int64_t o = (int64_t)lm * (S * 64);
-                r[0] = __ldg(reinterpret_cast<const uint4 *>(lg + o));
-                r[1] = __ldg(reinterpret_cast<const uint4 *>(lu + o));
-                r[2] = __ldg(reinterpret_cast<const uint4 *>(
-                    lg + o + 8 * row_bytes));
-                r[3] = __ldg(reinterpret_cast<const uint4 *>(
-                    lu + o + 8 * row_bytes));
+                const uint32_t dst = ring0 + (uint32_t)(r * 4 * 32) * 16;
+                cp16(dst, lg + o);
+                cp16(dst + 32 * 16, lu + o);
+                cp16(dst + 64 * 16, lg + o + 8 * row_bytes);
+                cp16(dst + 96 * 16, lu + o + 8 * row_bytes);
             }
             if (++lm == spw) {
                 lm = 0;
                 if (++lgi < ngr)
-                    set_load_task(lgi);
+                    set_copy_task(lgi);
             }
         }
+        cp_commit();                               // one group per step
     };
+    set_copy_task(0);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        copy_next(r);
 
     // byte offsets (within the staged activations) of this thread's four
-    // B-fragment chunks at K step 0; step kc adds kc * 256
+    // B-fragment chunks at K step 0 (step kc adds kc * 256); rows past the
+    // chunk read a stale in-bounds row whose output columns are not stored
     const int xrow = min(g, tok_cap - 1);
     int xoff[4];
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4)
         xoff[q4] = xrow * H * 2 +
                    ((tq >> 1) * 8 +
-                    (((tq & 1) * 4 + q4) ^ (tq >> 1) ^ ((xrow & 1) << 1))) * 16;
-
-    uint4 ring[D][4];
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-        load_next(ring[d]);
+                    (((tq & 1) * 4 + q4) ^ (tq >> 1) ^ ((xrow & 1) << 1))) *
+                       16;
 
     float acc[2][4];
     int staged_e = -1, staged_chunk = -1;
     Task k{};
     int gi = 0, m = 0;
+    const uint4 *myring = reinterpret_cast<const uint4 *>(ring) +
+                          (warp * R * 4 * 32 + lane);
 
-    for (int j0 = 0; j0 < total; j0 += D) {
+    for (int j0 = 0; j0 < total; j0 += R) {
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-            if (j0 + d >= total)
+        for (int r = 0; r < R; ++r) {
+            if (j0 + r >= total)
                 break;
             if (m == 0) {
                 k = task_at(gi);
                 if (k.e != staged_e || k.chunk != staged_chunk) {
                     __syncthreads();      // everyone is done with the old x
-                    // stage the chunk's activations: permuted, swizzled
                     const int qn = H / 8;
                     for (int idx = tid; idx < k.nt * qn; idx += kThreads) {
                         const int n = idx / qn, q = idx - n * qn;
@@ -280,26 +299,28 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                             xs + (int64_t)n * H * 2 + xs_chunk(q, n) * 16) =
                             permute8(v);
                     }
-                    __syncthreads();
                     staged_e = k.e;
                     staged_chunk = k.chunk;
+                    __syncthreads();
                 }
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.0f;
+                for (int i = 0; i < 2; ++i)
+                    acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
             }
+            cp_wait<R - 1>();             // this step's copies have landed
             const int kc = kpart + S * m;
             if (kc < steps && k.blk < IBk) {
-                // B fragments: rows past the chunk read a stale in-bounds
-                // row; those output columns are never stored
-                uint4 xb[4];
+                uint4 w[4], xb[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    w[c] = myring[(r * 4 + c) * 32];
                 const uint8_t *xk = xs + kc * 256;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     xb[q4] = *reinterpret_cast<const uint4 *>(xk + xoff[q4]);
-                step_mma(acc, ring[d], xb);
+                step_mma(acc, w, xb);
             }
-            load_next(ring[d]);
+            copy_next(r);
             if (m == spw - 1) {
                 // the task is complete: sum over the slot's warps
                 if (S > 1) {
@@ -311,13 +332,13 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                     if (kpart == 0) {
                         for (int w = 1; w < S; ++w) {
 #pragma unroll
-                            for (int r = 0; r < 2; ++r) {
+                            for (int i = 0; i < 2; ++i) {
                                 const float4 v =
-                                    red[((warp + w) * 32 + lane) * 2 + r];
-                                acc[r][0] += v.x;
-                                acc[r][1] += v.y;
-                                acc[r][2] += v.z;
-                                acc[r][3] += v.w;
+                                    red[((warp + w) * 32 + lane) * 2 + i];
+                                acc[i][0] += v.x;
+                                acc[i][1] += v.y;
+                                acc[i][2] += v.z;
+                                acc[i][3] += v.w;
                             }
                         }
                     }
@@ -326,22 +347,22 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                 const uint8_t *slab = expert_slab(a, k.e);
                 if (kpart == 0 && k.blk < IBk && slab != nullptr) {
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int64_t i =
-                            (int64_t)k.blk * kRowsPerTask + 8 * r + g;
+                    for (int i = 0; i < 2; ++i) {
+                        const int64_t row =
+                            (int64_t)k.blk * kRowsPerTask + 8 * i + g;
                         const float sg = reinterpret_cast<const float *>(
-                            slab + a.gate_s_off)[i];
+                            slab + a.gate_s_off)[row];
                         const float su = reinterpret_cast<const float *>(
-                            slab + a.up_s_off)[i];
+                            slab + a.up_s_off)[row];
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             const int n = 2 * tq + jj;
                             if (n < k.nt) {
-                                const float g32 = __fmul_rn(acc[r][jj], sg);
+                                const float g32 = __fmul_rn(acc[i][jj], sg);
                                 const float u32 =
-                                    __fmul_rn(acc[r][2 + jj], su);
+                                    __fmul_rn(acc[i][2 + jj], su);
                                 const int64_t o =
-                                    (int64_t)(k.p0 + n) * a.I + i;
+                                    (int64_t)(k.p0 + n) * a.I + row;
                                 a.out[o] = swiglu_out(g32, u32);
                                 if (a.gate_f32)
                                     a.gate_f32[o] = g32;
@@ -358,39 +379,56 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
             }
         }
     }
+    cp_wait<0>();
 }
 
-}  // namespace
-
-bool matvec_mma_supported(const GateUpArgs &a) {
-    return a.H % kStepK == 0 && a.I % kRowsPerTask == 0 &&
-           a.gate_w_off % 16 == 0 && a.up_w_off % 16 == 0 &&
-           a.H <= 16384;
-}
-
-template <int S>
+template <int S, int R>
 cudaError_t launch_split(const GateUpArgs &a, size_t smem, int tok_cap,
                          cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(
-        matvec_mma_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        matvec_mma_kernel<S, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)smem);
     if (err != cudaSuccess)
         return err;
-    matvec_mma_kernel<S><<<2 * a.num_sms, kThreads, smem, s>>>(a, tok_cap);
+    matvec_mma_kernel<S, R><<<a.num_sms, kThreads, smem, s>>>(a, tok_cap);
     count_launches(1);
     return cudaGetLastError();
 }
 
-// Few grouped rows (a tiny call) -> split K over all 8 warps; otherwise
-// whole tasks per warp.
+size_t matvec_smem(const GateUpArgs &a, int S, int R, int tok_cap) {
+    return (size_t)kWarps * R * 4 * 32 * 16 + (size_t)tok_cap * a.H * 2 +
+           (S > 1 ? sizeof(float4) * kWarps * 32 * 2 : 0) +
+           sizeof(int32_t) * 2 * (size_t)(a.E + 1);
+}
+
+constexpr size_t kSmemLimit = 227 * 1024 - 1024;  // room for static smem
+
+}  // namespace
+
+bool matvec_mma_supported(const GateUpArgs &a) {
+    const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
+    return a.H % kStepK == 0 && a.I % kRowsPerTask == 0 &&
+           a.gate_w_off % 16 == 0 && a.up_w_off % 16 == 0 &&
+           matvec_smem(a, 16, 2, tok_cap) <= kSmemLimit &&
+           matvec_smem(a, 1, 2, tok_cap) <= kSmemLimit;
+}
+
+// Few grouped rows (a tiny call) -> split K over all 16 warps; otherwise
+// whole tasks per warp.  The ring is 4 steps deep when shared memory
+// allows, else 2.
 cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s) {
     const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
-    const size_t smem = sizeof(float4) * kWarps * 32 * 2 +
-                        sizeof(int32_t) * 2 * (size_t)(a.E + 1) + 128 +
-                        (size_t)tok_cap * (size_t)a.H * 2;
-    if (a.M < 16)
-        return launch_split<8>(a, smem, tok_cap, s);
-    return launch_split<1>(a, smem, tok_cap, s);
+    if (a.M < 16) {
+        if (matvec_smem(a, 16, 4, tok_cap) <= kSmemLimit)
+            return launch_split<16, 4>(a, matvec_smem(a, 16, 4, tok_cap),
+                                       tok_cap, s);
+        return launch_split<16, 2>(a, matvec_smem(a, 16, 2, tok_cap),
+                                   tok_cap, s);
+    }
+    if (matvec_smem(a, 1, 4, tok_cap) <= kSmemLimit)
+        return launch_split<1, 4>(a, matvec_smem(a, 1, 4, tok_cap), tok_cap,
+                                  s);
+    return launch_split<1, 2>(a, matvec_smem(a, 1, 2, tok_cap), tok_cap, s);
 }
 
 }  // namespace q4moe
