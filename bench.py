@@ -55,6 +55,9 @@ def parse_args():
                     choices=["auto", "matvec", "gemm"])
     ap.add_argument("--no-workspace", action="store_true",
                     help="call without the scratch workspace")
+    ap.add_argument("--matvec-tile", type=int, default=0,
+                    choices=[0, 16, 32, 64, 128],
+                    help="unit height of the TMA matvec (0: per call)")
     return ap.parse_args()
 
 
@@ -186,7 +189,7 @@ class GpuWorkload:
     """Device-resident inputs for one workload and the step launcher."""
 
     def __init__(self, w: syn.Workload, kernel: str, device: int,
-                 use_workspace: bool = True):
+                 use_workspace: bool = True, matvec_tile: int = 0):
         import torch
         from up_swiglu_gb300 import q4moe as q
         self.torch, self.q, self.w = torch, q, w
@@ -235,6 +238,7 @@ class GpuWorkload:
             self.slabs = [q.make_slabs(w.E, L, base=self.pool)]
         self.opts = q.q4moe_options_t()
         self.opts.kernel = self.kernel
+        self.opts.matvec_tile = matvec_tile
         if use_workspace:
             # scratch for the grouped activations the tensor-core GEMM reads
             nbytes = q.q4moe_workspace_bytes(self.M, w.H)
@@ -402,7 +406,8 @@ def main():
     q.load()
 
     gw = GpuWorkload(w, args.kernel, local,
-                     use_workspace=not args.no_workspace)
+                     use_workspace=not args.no_workspace,
+                     matvec_tile=args.matvec_tile)
     units = workload_units(w, gw.topk_host, gw.pool_experts)
     dev = gw.dev
     stream = gw.stream
@@ -527,6 +532,7 @@ def main():
                              f"({gw.pool_experts} distinct expert slabs)",
                        "kernel_choice": args.kernel,
                        "workspace": not args.no_workspace,
+                       "matvec_tile": args.matvec_tile or "per call",
                        "parallelism": f"replicas x{world}" if world > 1
                        else "single GPU"},
             "tflops": round(tflops, 3),

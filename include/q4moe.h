@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 2
+#define Q4MOE_ABI_VERSION 3
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -125,7 +125,14 @@ typedef struct q4moe_options {
                            before rounding to bf16                         */
     float *up_f32;      /* optional device f32 [M][I]: U * up scale        */
     int32_t kernel;     /* Q4MOE_KERNEL_*                                  */
-    int32_t reserved0;  /* must be 0                                       */
+    int32_t matvec_tile; /* 0: chosen per call; else the height, in
+                            intermediate rows, of the work unit of the
+                            TMA-fed matvec (16, 32, 64 or 128; taller
+                            units split K over fewer warps).  It changes
+                            only the f32 summation order: every height
+                            meets the same accuracy bound, and inputs
+                            whose sums are exact give identical bits.
+                            The other matvec versions ignore it.         */
     void *workspace;    /* optional device scratch of at least
                            q4moe_workspace_bytes(M, H) bytes, 256-byte
                            aligned, not overlapping any other argument.

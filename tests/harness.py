@@ -139,10 +139,11 @@ def group(d: DeviceProblem, stream=None):
 
 
 def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
-            stream=None, out=None, workspace=False):
+            stream=None, out=None, workspace=False, matvec_tile=0):
     """Run the fused call; returns numpy out bits [M, I] (+ gate32/up32).
     workspace=True hands the call a scratch buffer (grouped activations
-    for the tensor-core GEMM)."""
+    for the tensor-core GEMM); matvec_tile fixes the TMA matvec's unit
+    height."""
     import torch
     M = int(tok.shape[0])
     I = d.p.I
@@ -150,7 +151,7 @@ def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
         out = torch.full((max(M, 1), I), -1, dtype=torch.int16,
                          device="cuda")
     res = {}
-    if debug or kernel != q.KERNEL_AUTO or workspace:
+    if debug or kernel != q.KERNEL_AUTO or workspace or matvec_tile:
         g32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
             if debug else None
         u32 = torch.full((max(M, 1), I), float("nan"), device="cuda") \
@@ -160,6 +161,7 @@ def gate_up(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO, debug=True,
         o.gate_f32 = None if g32 is None else g32.data_ptr()
         o.up_f32 = None if u32 is None else u32.data_ptr()
         o.kernel = kernel
+        o.matvec_tile = matvec_tile
         if workspace:
             nbytes = q.q4moe_workspace_bytes(M, d.p.H)
             wbuf, ws = aligned_device_buffer(max(nbytes, 256), 256)

@@ -33,21 +33,33 @@ def _oracle_full(p, offs, tok):
                                  offs, tok, want_debug=True)
 
 
-def _run_and_compare(p, kernel=q.KERNEL_AUTO, exact=False, **upload_kw):
+def _run_and_compare(p, kernel=q.KERNEL_AUTO, exact=False, matvec_tile=0,
+                     **upload_kw):
     d = hz.upload(p, **upload_kw)
     offs_d, tok_d, _ = hz.group(d)
     offs, tok = offs_d.cpu().numpy(), tok_d.cpu().numpy()
     o_offs, o_tok, _ = oracle.group_rows(p.topk, p.E)
     assert np.array_equal(offs, o_offs) and np.array_equal(tok, o_tok)
-    gpu = hz.gate_up(d, offs_d, tok_d, kernel=kernel)
+    gpu = hz.gate_up(d, offs_d, tok_d, kernel=kernel, matvec_tile=matvec_tile)
     orc = _oracle_full(p, offs, tok)
     gs, us = hz.element_scales(p, offs)
     stats = parity.compare(gpu, orc, gs, us, p.H, exact=exact)
     # the plain entry point (no debug outputs) writes the same bits
-    plain = hz.gate_up(d, offs_d, tok_d, kernel=kernel, debug=False)
+    plain = hz.gate_up(d, offs_d, tok_d, kernel=kernel, debug=False,
+                       matvec_tile=matvec_tile)
     assert np.array_equal(plain["out"], gpu["out"])
+    # the matvec's unit height only changes the f32 summation order: every
+    # height meets the same bound (and exact sums give the same bits)
+    if not matvec_tile and kernel != q.KERNEL_GEMM:
+        for tile in (16, 128):
+            tiled = hz.gate_up(d, offs_d, tok_d, kernel=kernel,
+                               matvec_tile=tile)
+            parity.compare(tiled, orc, gs, us, p.H, exact=exact)
+            if exact:
+                assert np.array_equal(tiled["out"], gpu["out"])
     # with a workspace the GEMM reads the grouped rows through TMA: same bits
-    ws = hz.gate_up(d, offs_d, tok_d, kernel=kernel, workspace=True)
+    ws = hz.gate_up(d, offs_d, tok_d, kernel=kernel, workspace=True,
+                    matvec_tile=matvec_tile)
     assert np.array_equal(ws["out"], gpu["out"])
     assert np.array_equal(ws["gate32"].view(np.uint32),
                           gpu["gate32"].view(np.uint32))
@@ -167,6 +179,68 @@ def test_parity_ragged_rows_per_expert(counts):
     p = hz.problem_with_counts(9, counts, 256, 512)
     for kernel in KERNELS:
         _run_and_compare(p, kernel=kernel)
+
+
+@pytest.mark.parametrize("tile", [16, 32, 64, 128])
+def test_matvec_tiles_bit_exact(tile):
+    """Every unit height of the TMA-fed matvec, with I not a multiple of
+    the tile (rows past I arrive as zeros and are never stored) and chunks
+    of 1..8 rows."""
+    counts = [0, 1, 7, 8, 9, 3, 16, 48, 2]
+    p = hz.problem_with_counts(40 + tile, counts, 208, 1024, exact=True)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, exact=True, matvec_tile=tile)
+
+
+@pytest.mark.parametrize("tile", [16, 32, 64, 128])
+def test_matvec_tiles_real_valued(tile):
+    p = hz.problem_with_counts(60 + tile, [1, 5, 8, 9, 0, 2], 1536, 5120)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, matvec_tile=tile)
+
+
+@pytest.mark.parametrize("H", [384, 640])
+def test_matvec_cp_async_path_base_mode(H):
+    """H % 256 == 128 with slabs at base + e * stride: the matvec whose
+    weights move by per-thread cp.async."""
+    p = hz.problem_with_counts(H, [2, 0, 9, 1, 16], 96, H, exact=True)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, exact=True)
+    p = hz.problem_with_counts(H + 1, [2, 0, 9, 1, 16], 96, H)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC)
+
+
+def _scale_bf16(x, shift):
+    """bf16 bits times 2^shift (exponent field moved; zeros kept)."""
+    x = x.astype(np.int32)
+    nz = (x & 0x7FFF) != 0
+    x[nz] += shift << 7
+    return x.astype(np.uint16)
+
+
+@pytest.mark.parametrize("shift", [40, -60, -90])
+def test_matvec_scaled_exact_activations(shift):
+    """Exact-integer activations times 2^shift.  The matvec stages a chunk
+    of activations in f16 under a power-of-two scale when one fits (shift
+    40 and -60), else in bf16 (-90: the scale would leave f32's range);
+    every sum stays exact, so the bits must match the oracle's."""
+    p = hz.problem_with_counts(77, [5, 8, 1, 3], 128, 512, exact=True)
+    p.x = _scale_bf16(p.x, shift)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, exact=True)
+
+
+def test_matvec_wide_exponent_span_falls_back_to_bf16():
+    """Two rows of one chunk 2^40 apart (too wide a span for f16 under one
+    scale) next to an ordinary chunk: bits must still match exactly."""
+    p = hz.problem_with_counts(78, [2, 3], 128, 512, exact=True)
+    rows = np.flatnonzero(p.topk[:, 0] == 0)
+    p.x[rows[0]] = _scale_bf16(p.x[rows[0]][None], 20)[0]
+    p.x[rows[1]] = _scale_bf16(p.x[rows[1]][None], -20)[0]
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, exact=True)
+
+
+def test_matvec_subnormal_activation_falls_back_to_bf16():
+    p = hz.problem_with_counts(79, [3, 2], 256, 1024)
+    p.x[0, 5] = 0x0001                     # smallest positive bf16 subnormal
+    p.x[1, 7] = 0x8003
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC)
 
 
 def test_parity_generic_shapes():

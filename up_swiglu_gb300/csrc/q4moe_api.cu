@@ -290,7 +290,9 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     q4moe_options_t o{};
     if (opts != nullptr)
         o = *opts;
-    if (o.reserved0 != 0 || o.kernel < Q4MOE_KERNEL_AUTO ||
+    if ((o.matvec_tile != 0 && o.matvec_tile != 16 && o.matvec_tile != 32 &&
+         o.matvec_tile != 64 && o.matvec_tile != 128) ||
+        o.kernel < Q4MOE_KERNEL_AUTO ||
         o.kernel > Q4MOE_KERNEL_GEMM || o.num_tokens < 0)
         return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
     if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
@@ -336,6 +338,7 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     a.xg = static_cast<uint16_t *>(o.workspace);
     a.status = d->status;
     a.num_sms = d->num_sms;
+    a.matvec_tile = o.matvec_tile;
 
     const bool gemm_ok = q4moe::gemm_supported(H, I, a);
     int32_t matvec_max = INT32_MAX;

@@ -125,29 +125,6 @@ __device__ __forceinline__ Tile tile_of(int t, const int32_t *off,
     return ti;
 }
 
-// Bounded wait on an mbarrier phase.  Returns false (and, the first time,
-// raises the status bit) once the CTA has aborted or the wait ran out.
-__device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
-                                        volatile int *abort,
-                                        unsigned int *status) {
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if ((it & 63u) == 0) {
-            if (*abort)
-                return false;
-            if (globaltimer_ns() - t0 > kTimeoutNs) {
-                if (atomicExch((int *)abort, 1) == 0)
-                    atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 // One packed word (8 nibbles, K order) -> 8 bf16 (nibble - 8) in K order:
 // each output pair (2j, 2j+1) is byte j of the word split into its two
 // nibbles, placed in the low mantissa bits of 128.0 (0x4300) and then
@@ -174,15 +151,6 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w) {
 // K-major tile.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// Bounded wait that ignores the abort flag, used while draining copies
-// before exit (they land within microseconds; 0.2 s is ample).
-__device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity) &&
-           globaltimer_ns() - t0 < 200000000ull) {
-    }
 }
 
 // Copy the activations of each grouped row that the GEMM will read (rows of
@@ -577,13 +545,8 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
 
 }  // namespace
 
-bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a) {
-    return H % BK == 0 && I % BM == 0 && a.gate_w_off % 16 == 0 &&
-           a.up_w_off % 16 == 0 && a.E <= Q4MOE_MAX_EXPERTS;
-}
-
-namespace {
-
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependence on libcuda); null when the driver lacks it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -598,6 +561,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     });
     return fn;
 }
+
+bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a) {
+    return H % BK == 0 && I % BM == 0 && a.gate_w_off % 16 == 0 &&
+           a.up_w_off % 16 == 0 && a.E <= Q4MOE_MAX_EXPERTS;
+}
+
+namespace {
 
 // Tensor map of the grouped activations bf16 [M][H]: boxes of 64 columns
 // (128 bytes, the swizzle span) x 16 rows, 128-byte swizzle, rows past M

@@ -30,6 +30,7 @@ struct GateUpArgs {
     unsigned int *status;        // device status word (Q4MOE_DEV_* bits)
     int32_t matvec_max_rows;     // experts with more rows go to the GEMM
     int32_t num_sms;
+    int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
 };
 
 // Host-side count of kernel launches (q4moe_launch_count).
@@ -41,6 +42,8 @@ int report_error(int code, const char *message);
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s);
 bool matvec_mma_supported(const GateUpArgs &a);
 cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
+bool matvec_tma_supported(const GateUpArgs &a);
+cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
 bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);
 cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,

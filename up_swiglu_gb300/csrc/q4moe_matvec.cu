@@ -1,9 +1,13 @@
 // q4moe_matvec.cu -- grouped Q4 gate/up + SwiGLU matvec for experts with few
 // rows (decode / speculative verify widths).
 //
-// launch_matvec runs the tensor-core version (q4moe_matvec_mma.cu) whenever
-// the shapes allow it (H % 128 == 0, I % 8 == 0, 16-byte aligned weight
-// sections) and this generic version otherwise.
+// launch_matvec picks the first version the call allows:
+//   q4moe_matvec_tma.cu  slabs at base + e * stride, H % 256 == 0,
+//                        I % 16 == 0, 16-byte aligned weight sections
+//                        (weights moved by TMA);
+//   q4moe_matvec_mma.cu  also a per-expert pointer table, H % 128 == 0
+//                        (weights moved by per-thread cp.async);
+//   this generic version otherwise.
 //
 // Generic version: any H % 8 == 0, I % 4 == 0.  One warp owns one output
 // row i of one expert and up to 8 of the expert's grouped rows at a time,
@@ -123,6 +127,8 @@ __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
 }  // namespace
 
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
+    if (matvec_tma_supported(a))
+        return launch_matvec_tma(a, s);
     if (matvec_mma_supported(a))
         return launch_matvec_mma(a, s);
     const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),

@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include "q4moe.h"
+
 namespace q4moe {
 namespace sm100 {
 
@@ -56,6 +58,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and, the first time,
+// raises Q4MOE_DEV_WAIT_TIMEOUT) once the CTA has aborted or the wait ran
+// out (4 s).
+static __device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort,
+                                               unsigned int *status) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (globaltimer_ns() - t0 > 4000000000ull) {
+                if (atomicExch((int *)abort, 1) == 0)
+                    atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag, used while draining copies
+// before exit (they land within microseconds; 0.2 s is ample).
+__device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity) &&
+           globaltimer_ns() - t0 < 200000000ull) {
+    }
 }
 
 // ---------------------------------------------------------------- cp.async --
@@ -123,6 +158,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1),
         "r"(smem_u32(bar))
         : "memory");
+}
+
+// Tiled 3-D tensor load (c0 inner, c1 row, c2 outer).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap,
+                                            int32_t c0, int32_t c1, int32_t c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+        "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first use.
+__device__ __forceinline__ void tma_desc_prefetch(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap))
+                 : "memory");
 }
 
 // Prefetch one box of a tiled 2-D tensor into L2 (no shared memory write,

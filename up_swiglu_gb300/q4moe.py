@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -78,7 +78,7 @@ class q4moe_options_t(ctypes.Structure):
                 ("gate_f32", ctypes.c_void_p),
                 ("up_f32", ctypes.c_void_p),
                 ("kernel", ctypes.c_int32),
-                ("reserved0", ctypes.c_int32),
+                ("matvec_tile", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_int64)]
 
