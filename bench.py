@@ -478,7 +478,7 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(w.name, "q4moe_matvec_mma.cu"),
+                "traffic": load_traffic(w.name, "q4moe_matvec_tma.cu"),
                 "kernel": "q4moe_gate_up_swiglu matvec",
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
