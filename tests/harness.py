@@ -91,9 +91,11 @@ class DeviceProblem:
     topk: object = None
 
 
-def upload(p: Problem, layout=None, stride_pad=0, ptr_table=False):
+def upload(p: Problem, layout=None, stride_pad=0, ptr_table=False,
+           x_offset=0):
     """Pack the experts into slabs (canonical layout unless given), copy them
-    into one 4096-aligned device pool, and upload x and the routing."""
+    into one 4096-aligned device pool, and upload x and the routing (x_offset
+    bf16 elements past a 256-byte boundary)."""
     import torch
     L = layout or q.q4moe_canonical_layout(p.H, p.I)
     host = q.pack_slab_pool(L, p.gate_w, p.up_w, p.gate_s, p.up_s)
@@ -123,7 +125,15 @@ def upload(p: Problem, layout=None, stride_pad=0, ptr_table=False):
     else:
         slabs = q.make_slabs(p.E, L, base=pool, slab_stride=stride)
     d = DeviceProblem(p, L, slabs, keep)
-    d.x = torch.from_numpy(np.ascontiguousarray(p.x).view(np.int16)).cuda()
+    xh = torch.from_numpy(np.ascontiguousarray(p.x).view(np.int16))
+    if x_offset:
+        xbuf, xv = aligned_device_buffer(xh.numel() * 2 + 2 * x_offset, 256)
+        keep.append(xbuf)
+        d.x = xv.view(torch.int16)[x_offset:x_offset + xh.numel()] \
+            .view(xh.shape)
+        d.x.copy_(xh)
+    else:
+        d.x = xh.cuda()
     d.topk = torch.from_numpy(np.ascontiguousarray(p.topk)).cuda()
     return d
 

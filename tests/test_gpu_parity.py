@@ -243,6 +243,45 @@ def test_matvec_subnormal_activation_falls_back_to_bf16():
     _run_and_compare(p, kernel=q.KERNEL_MATVEC)
 
 
+@pytest.mark.parametrize("exact", [True, False])
+def test_gemm_with_and_without_token_count(exact):
+    """The GEMM's tensor map over x spans num_tokens rows when the caller
+    gives it, else the largest row count a coordinate can name; both must
+    give the oracle's results."""
+    p = hz.problem_with_counts(13, [70, 130, 3], 256, 512, exact=exact)
+    _run_and_compare(p, kernel=q.KERNEL_GEMM, exact=exact)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    with_t = hz.gate_up(d, offs, tok, kernel=q.KERNEL_GEMM, debug=False)
+    import torch
+    M = int(tok.shape[0])
+    out = torch.full((M, p.I), -1, dtype=torch.int16, device="cuda")
+    o = q.q4moe_options_t()
+    o.kernel = q.KERNEL_GEMM                # num_tokens left at 0
+    q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, offs, tok, M, p.H, p.I, out, o)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), with_t["out"])
+
+
+def test_gemm_bad_token_row_reads_zeros():
+    """A token index past num_tokens in a GEMM tile: the status bit is set
+    and that row is computed from zero activations (output +0)."""
+    import torch
+    p = hz.problem_with_counts(14, [100], 256, 512)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    bad = tok.clone()
+    bad[17] = p.T + 3
+    q.q4moe_device_status(clear=True)
+    res = hz.gate_up(d, offs, bad, kernel=q.KERNEL_GEMM)
+    assert q.q4moe_device_status(clear=True) == q.DEV_BAD_TOKEN
+    assert np.all(res["out"][17] == 0)
+    assert np.all(res["gate32"][17] == 0) and np.all(res["up32"][17] == 0)
+    good = hz.gate_up(d, offs, tok, kernel=q.KERNEL_GEMM)
+    rows = np.arange(tok.shape[0]) != 17
+    assert np.array_equal(res["out"][rows], good["out"][rows])
+
+
 def test_parity_generic_shapes():
     """H not a multiple of 32 and tiny I (the pages' minimum rules)."""
     for (I, H) in ((4, 8), (12, 24), (20, 40)):
@@ -299,6 +338,38 @@ def test_bad_offsets_and_tokens_raise_status():
     badtok[3] = p.T + 5
     hz.gate_up(d, offs, badtok)             # num_tokens = T: checked
     assert q.q4moe_device_status(clear=True) == q.DEV_BAD_TOKEN
+
+
+@pytest.mark.parametrize("counts", [[5], [3, 0, 6]])
+def test_bad_offsets_tma_matvec_writes_nothing(counts):
+    """The TMA matvec with inconsistent offsets: a single expert's call has
+    already staged activations and issued weight loads when the offsets are
+    checked; it must drain them, write nothing and raise the status bit."""
+    import torch
+    p = hz.problem_with_counts(11, counts, 256, 512)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    M = int(tok.shape[0])
+    q.q4moe_device_status(clear=True)
+    bad = offs.clone()
+    bad[-1] = M + 1                           # last offset must be M
+    out = torch.full((M, p.I), 5, dtype=torch.int16, device="cuda")
+    o = q.q4moe_options_t()
+    o.kernel = q.KERNEL_MATVEC
+    q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, bad, tok, M, p.H, p.I, out, o)
+    assert q.q4moe_device_status(clear=True) == q.DEV_BAD_ROW_OFFSETS
+    assert torch.all(out == 5)
+    # the library still works afterwards
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC)
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_single_expert_several_chunks(exact):
+    """One expert, 20 rows: three chunks of activations, units computed
+    before the offsets are read."""
+    p = hz.problem_with_counts(12, [20], 1536, 4096, exact=exact)
+    _run_and_compare(p, kernel=q.KERNEL_MATVEC, exact=exact)
+    _run_and_compare(p, exact=exact)
 
 
 def test_misaligned_slab_pointer_raises_status():

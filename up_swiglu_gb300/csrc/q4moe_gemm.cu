@@ -14,7 +14,7 @@
 //           swizzled K-major layout, 64 K per pipeline stage;
 //  B      = the tile's token rows of x in the same layout: with a
 //           workspace, the rows are first copied once into grouped order
-//           and each stage is a few TMA boxes of 16 rows; without one,
+//           and each stage is at most five TMA boxes; without one,
 //           they are gathered row by row with cp.async;
 //  D      = two f32 accumulators in tensor memory (gate: columns 0..N-1,
 //           up: columns 256..256+N-1), lane = intermediate row;
@@ -49,10 +49,16 @@ using namespace sm100;
 constexpr int BM = 128;                      // intermediate rows per tile
 constexpr int BK = 64;                       // K per stage
 constexpr int NMAX = 256;                    // token rows per tile
-constexpr int STAGES = 3;
+// Two rings: the dequantised weights (A: gate and up tiles) refill within
+// about one MMA stage, the token rows (B) come from HBM and need more
+// stages in flight.
+constexpr int A_STAGES = 3;
+constexpr int B_STAGES = 3;
+
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = NMAX * BK * 2;       // 32 KB
-constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr int A_STAGE_BYTES = 2 * A_BYTES;
+constexpr int RING_BYTES = A_STAGES * A_STAGE_BYTES + B_STAGES * B_BYTES;
 constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
@@ -66,12 +72,20 @@ constexpr int kPrefetch = 4;                 // k-blocks of weights in flight
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kUpCol = 256;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
-constexpr int kBoxRows = 16;                 // rows per TMA box of x
-constexpr uint32_t kBoxBytes = kBoxRows * BK * 2;
+// Tensor maps of the grouped activations with boxes of 256, 128, 64, 32
+// and 16 rows: a tile of n rows (a multiple of 16) is at most five loads,
+// one per set bit of n / 16 (each TMA instruction costs the single issuing
+// thread on the order of a hundred cycles).
+constexpr int kBoxLevels = 5;
+struct XgMaps {
+    CUtensorMap m[kBoxLevels];               // box rows 256 >> level
+};
 
 struct Ctl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t a_full[A_STAGES];
+    uint64_t a_empty[A_STAGES];
+    uint64_t b_full[B_STAGES];
+    uint64_t b_empty[B_STAGES];
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
@@ -81,7 +95,7 @@ struct Ctl {
 };
 
 constexpr size_t smem_bytes(int E) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl) +
+    return 1024 + (size_t)RING_BYTES + sizeof(Ctl) +
            2 * sizeof(int32_t) * (size_t)(E + 1) + 16;
 }
 
@@ -155,36 +169,64 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
 
 // Copy the activations of each grouped row that the GEMM will read (rows of
 // experts above the matvec's row limit) into the workspace, bf16 [M][H].
-__global__ void __launch_bounds__(128)
+// The offsets are staged in shared memory (the expert of a row is a binary
+// search there); one warp copies one row, each lane keeping four 16-byte
+// loads in flight.
+constexpr int kGatherThreads = 256;
+__global__ void __launch_bounds__(kGatherThreads)
 gather_rows_kernel(GateUpArgs a) {
+    extern __shared__ int32_t s_goff[];
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x)
+        s_goff[e] = a.row_offsets[e];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
     const int64_t chunks = a.H / 8;
-    for (int64_t p = blockIdx.x; p < a.M; p += gridDim.x) {
+    const int64_t wpb = blockDim.x / 32;
+    const int64_t nwarps = (int64_t)gridDim.x * wpb;
+    for (int64_t p = blockIdx.x * wpb + (threadIdx.x >> 5); p < a.M;
+         p += nwarps) {
         int lo = 0, hi = a.E;         // expert e with off[e] <= p < off[e+1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (a.row_offsets[mid] <= p)
+            if (s_goff[mid] <= p)
                 lo = mid;
             else
                 hi = mid;
         }
-        if (a.row_offsets[lo + 1] - a.row_offsets[lo] <= a.matvec_max_rows)
+        if (s_goff[lo + 1] - s_goff[lo] <= a.matvec_max_rows)
             continue;
-        const int64_t t = row_token(a, p);
+        int64_t t = 0;
+        if (lane == 0)
+            t = row_token(a, p);
+        t = __shfl_sync(0xffffffffu, t, 0);
         uint4 *dst = reinterpret_cast<uint4 *>(a.xg + p * a.H);
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * a.H);
-        for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
-            dst[c] = t >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        for (int64_t c0 = lane; c0 < chunks; c0 += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + 32 * u;
+                v[u] = (t >= 0 && c < chunks) ? __ldg(src + c)
+                                              : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + 32 * u;
+                if (c < chunks)
+                    dst[c] = v[u];
+            }
+        }
     }
 }
 
 template <bool kTma>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
+gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)STAGES * STAGE_BYTES);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)RING_BYTES);
     int32_t *s_off = reinterpret_cast<int32_t *>(ctl + 1);
     int32_t *s_pre = s_off + (a.E + 1);
 
@@ -194,9 +236,13 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
     const int KB = (int)(a.H / BK);
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->full[s], kDeqWarps + (kTma ? 1 : kGatThreads));
-            mbar_init(&ctl->empty[s], 1);
+        for (int s = 0; s < A_STAGES; ++s) {
+            mbar_init(&ctl->a_full[s], kDeqWarps);
+            mbar_init(&ctl->a_empty[s], 1);
+        }
+        for (int s = 0; s < B_STAGES; ++s) {
+            mbar_init(&ctl->b_full[s], kTma ? 1 : kGatThreads);
+            mbar_init(&ctl->b_empty[s], 1);
         }
         mbar_init(&ctl->tmem_full, 1);
         mbar_init(&ctl->tmem_empty, kEpiWarps);
@@ -255,6 +301,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort;
     const uint32_t stage0 = smem_u32(stages);
+    const uint32_t b_ring0 = stage0 + A_STAGES * A_STAGE_BYTES;
 
     if (kTma && warp >= kGatWarp0) {
         // ------------------------------------------- token rows via TMA
@@ -262,28 +309,37 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
             uint32_t g = 0;
             for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
                 const Tile ti = tile_of(t, s_off, s_pre, E, IB);
-                const int boxes = ti.n / kBoxRows;
+
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const uint32_t s = g % STAGES;
-                    if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1,
-                                    abort, a.status)) {
+                    const uint32_t s = g % B_STAGES;
+                    if (!wait_phase(&ctl->b_empty[s],
+                                    ((g / B_STAGES) & 1) ^ 1, abort,
+                                    a.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&ctl->full[s], boxes * kBoxBytes);
-                    const uint32_t bdst =
-                        stage0 + s * STAGE_BYTES + 2 * A_BYTES;
-                    for (int b = 0; b < boxes; ++b)
-                        tma_load_2d(bdst + b * kBoxBytes, &tmap_xg, kb * BK,
-                                    ti.row0 + b * kBoxRows, &ctl->full[s]);
+                    mbar_arrive_expect_tx(&ctl->b_full[s],
+                                          (uint32_t)ti.n * BK * 2);
+                    const uint32_t bdst = b_ring0 + s * B_BYTES;
+                    int off = 0;                 // rows issued so far
+#pragma unroll
+                    for (int lvl = 0; lvl < kBoxLevels; ++lvl) {
+                        const int h = 256 >> lvl;
+                        if (ti.n - off >= h) {
+                            tma_load_2d(bdst + off * (BK * 2),
+                                        &xg_maps.m[lvl], kb * BK,
+                                        ti.row0 + off, &ctl->b_full[s]);
+                            off += h;
+                        }
+                    }
                 }
                 if (!ok)
                     break;
             }
             // let the boxes still in flight land before the CTA exits
-            for (uint32_t gg = g > STAGES ? g - STAGES : 0; gg < g; ++gg)
-                drain_phase(&ctl->full[gg % STAGES], (gg / STAGES) & 1);
+            for (uint32_t gg = g > B_STAGES ? g - B_STAGES : 0; gg < g; ++gg)
+                drain_phase(&ctl->b_full[gg % B_STAGES], (gg / B_STAGES) & 1);
         }
     } else if (warp >= kGatWarp0) {
         // ---------------------------------------------------- token gather
@@ -310,13 +366,13 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
             }
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb, ++g) {
-                const uint32_t s = g % STAGES;
-                if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1, abort,
-                                a.status)) {
+                const uint32_t s = g % B_STAGES;
+                if (!wait_phase(&ctl->b_empty[s], ((g / B_STAGES) & 1) ^ 1,
+                                abort, a.status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bdst = stage0 + s * STAGE_BYTES + 2 * A_BYTES;
+                const uint32_t bdst = b_ring0 + s * B_BYTES;
 #pragma unroll
                 for (int m = 0; m < kGatItems; ++m) {
                     if (tokm[m] == -2)
@@ -332,7 +388,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                         cp_async_16(dst, a.x, 0);
                 }
                 // counted as this thread's arrival once its copies landed
-                cp_async_arrive_noinc(&ctl->full[s]);
+                cp_async_arrive_noinc(&ctl->b_full[s]);
             }
             if (!ok)
                 break;
@@ -373,13 +429,14 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                     const int kb = kb0 + d;
                     if (kb >= KB)
                         break;
-                    const uint32_t s = g % STAGES;
-                    if (!wait_phase(&ctl->empty[s], ((g / STAGES) & 1) ^ 1,
-                                    abort, a.status)) {
+                    const uint32_t s = g % A_STAGES;
+                    if (!wait_phase(&ctl->a_empty[s],
+                                    ((g / A_STAGES) & 1) ^ 1, abort,
+                                    a.status)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *ag = stages + (size_t)s * STAGE_BYTES;
+                    uint8_t *ag = stages + (size_t)s * A_STAGE_BYTES;
                     uint8_t *au = ag + A_BYTES;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -404,7 +461,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&ctl->full[s]);
+                        mbar_arrive(&ctl->a_full[s]);
                     ++g;
                 }
             }
@@ -426,9 +483,11 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                 tc_fence_after();
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const uint32_t s = g % STAGES;
-                    if (!wait_phase(&ctl->full[s], (g / STAGES) & 1, abort,
-                                    a.status)) {
+                    const uint32_t sa = g % A_STAGES, sb = g % B_STAGES;
+                    if (!wait_phase(&ctl->b_full[sb], (g / B_STAGES) & 1,
+                                    abort, a.status) ||
+                        !wait_phase(&ctl->a_full[sa], (g / A_STAGES) & 1,
+                                    abort, a.status)) {
                         ok = false;
                         break;
                     }
@@ -437,9 +496,9 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                     if (!kTma)
                         fence_proxy_async_smem();
                     tc_fence_after();
-                    const uint32_t ag = stage0 + s * STAGE_BYTES;
+                    const uint32_t ag = stage0 + sa * A_STAGE_BYTES;
                     const uint32_t au = ag + A_BYTES;
-                    const uint32_t bb = ag + 2 * A_BYTES;
+                    const uint32_t bb = b_ring0 + sb * B_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {
                         const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
@@ -450,7 +509,8 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tmap_xg) {
                                   sw128_kmajor_desc(au + ks * 32), bd, idesc,
                                   acc);
                     }
-                    umma_commit(&ctl->empty[s]);
+                    umma_commit(&ctl->a_empty[sa]);
+                    umma_commit(&ctl->b_empty[sb]);
                     issued = true;
                 }
                 if (!ok)
@@ -569,28 +629,32 @@ bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a) {
 
 namespace {
 
-// Tensor map of the grouped activations bf16 [M][H]: boxes of 64 columns
-// (128 bytes, the swizzle span) x 16 rows, 128-byte swizzle, rows past M
-// read as zero.
-cudaError_t encode_xg_map(const GateUpArgs &a, CUtensorMap *map) {
+// Tensor maps of the grouped activations bf16 [M][H]: boxes of 64 columns
+// (128 bytes, the swizzle span) x 256 >> level rows, 128-byte swizzle, rows
+// past M read as zero.
+cudaError_t encode_xg_maps(const GateUpArgs &a, XgMaps *maps) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
         return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)kBoxRows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.xg,
-                           dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    for (int lvl = 0; lvl < kBoxLevels; ++lvl) {
+        const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)(256 >> lvl)};
+        const CUresult r = enc(&maps->m[lvl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                               2, a.xg, dims, strides, box, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
 }
 
 template <bool kTma>
-cudaError_t launch_gemm_kernel(const GateUpArgs &a, const CUtensorMap &map,
+cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
                                cudaStream_t s) {
     const size_t smem = smem_bytes(a.E);
     cudaError_t err = cudaFuncSetAttribute(
@@ -598,7 +662,7 @@ cudaError_t launch_gemm_kernel(const GateUpArgs &a, const CUtensorMap &map,
         (int)smem);
     if (err != cudaSuccess)
         return err;
-    gemm_tcgen05_kernel<kTma><<<a.num_sms, kThreads, smem, s>>>(a, map);
+    gemm_tcgen05_kernel<kTma><<<a.num_sms, kThreads, smem, s>>>(a, maps);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -606,19 +670,22 @@ cudaError_t launch_gemm_kernel(const GateUpArgs &a, const CUtensorMap &map,
 }  // namespace
 
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
-    CUtensorMap map;
-    memset(&map, 0, sizeof map);
+    XgMaps maps;
+    memset(&maps, 0, sizeof maps);
     if (a.xg == nullptr)
-        return launch_gemm_kernel<false>(a, map, s);
-    cudaError_t err = encode_xg_map(a, &map);
+        return launch_gemm_kernel<false>(a, maps, s);
+    cudaError_t err = encode_xg_maps(a, &maps);
     if (err != cudaSuccess)
         return err;
-    const int blocks = (int)std::min<int64_t>(a.M, (int64_t)a.num_sms * 16);
-    gather_rows_kernel<<<blocks, 128, 0, s>>>(a);
+    const int blocks = (int)std::min<int64_t>(
+        (a.M + kGatherThreads / 32 - 1) / (kGatherThreads / 32),
+        (int64_t)a.num_sms * 8);
+    gather_rows_kernel<<<blocks, kGatherThreads,
+                         sizeof(int32_t) * (size_t)(a.E + 1), s>>>(a);
     count_launches(1);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
-    return launch_gemm_kernel<true>(a, map, s);
+    return launch_gemm_kernel<true>(a, maps, s);
 }
 
 }  // namespace q4moe

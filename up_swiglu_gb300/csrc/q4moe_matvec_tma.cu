@@ -637,6 +637,9 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
     // programmatic dependent launch: the kernel's set-up overlaps the end
     // of the previous kernel on the stream; it waits for that kernel's
     // results before reading any input
+    // a single expert's rows all above the matvec's limit: nothing to do
+    if (a.E == 1 && a.M > a.matvec_max_rows)
+        return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.num_sms);
     cfg.blockDim = dim3(kThreads);
