@@ -70,8 +70,11 @@ def _run_and_compare(p, kernel=q.KERNEL_AUTO, exact=False, matvec_tile=0,
 
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (0, 8, 4), (5, 3, 7),
                                    (1000, 8, 160), (4096, 8, 160),
-                                   (300, 2, 1024), (2047, 1, 3)])
+                                   (300, 2, 1024), (2047, 1, 3),
+                                   (4096, 4, 1024), (20000, 8, 7)])
 def test_group_rows_matches_oracle(T, k, E):
+    """Small inputs take one thread block; large ones (here 32768, 16384
+    and 160000 pairs) are counted, scanned and scattered by many blocks."""
     import torch
     rng = np.random.default_rng(T + E)
     topk = rng.integers(0, E, size=(T, k)).astype(np.int32)
@@ -97,6 +100,35 @@ def test_group_rows_bad_id_sets_status():
     assert q.q4moe_device_status(clear=True) & q.DEV_BAD_EXPERT_ID
     assert list(offs.cpu().numpy()) == [0, 2, 3, 4, 4]
     assert list(rop.cpu().numpy()) == [0, -1, 2, -1, 3, 1]
+
+
+def test_group_rows_many_blocks_bad_ids():
+    """Ids outside [0, E) on the many-block path: the status bit is set and
+    those pairs get row -1; the others are a stable sort by expert."""
+    import torch
+    T, k, E = 4096, 4, 64
+    topk = np.random.default_rng(5).integers(0, E, size=(T, k)).astype(
+        np.int32)
+    topk[7, 1] = E + 3
+    topk[2000, 0] = -2
+    p = hz.Problem(np.zeros((T, 8), np.uint16), np.zeros((E, 4, 1), np.uint32),
+                   None, None, None, topk)
+    d = hz.DeviceProblem(p, None, None)
+    d.topk = torch.from_numpy(topk).cuda()
+    q.q4moe_device_status(clear=True)
+    offs, tok, rop = hz.group(d)
+    assert q.q4moe_device_status(clear=True) & q.DEV_BAD_EXPERT_ID
+    ids = topk.ravel()
+    valid = [(int(e), qq) for qq, e in enumerate(ids) if 0 <= e < E]
+    order = sorted(valid)                 # by expert, then pair index
+    want_rop = np.full(ids.size, -1, np.int32)
+    for row, (_, qq) in enumerate(order):
+        want_rop[qq] = row
+    want_offs = np.searchsorted([e for e, _ in order], np.arange(E + 1))
+    assert np.array_equal(offs.cpu().numpy(), want_offs)
+    assert np.array_equal(rop.cpu().numpy(), want_rop)
+    assert np.array_equal(tok.cpu().numpy()[:len(order)],
+                          np.array([qq // k for _, qq in order], np.int32))
 
 
 # --------------------------------------------------------------------- tail --

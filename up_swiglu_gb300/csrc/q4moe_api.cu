@@ -230,7 +230,8 @@ int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
         return rc;
     cudaError_t err =
         q4moe::launch_group_rows(topk_ids, T * k, k, E, row_offsets,
-                                 token_of_row, row_of_pair, d->status, stream);
+                                 token_of_row, row_of_pair, d->status,
+                                 d->num_sms, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, "group_rows launch");
     return ok();

@@ -49,7 +49,8 @@ bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);
 cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                               int32_t E, int32_t *row_offsets,
                               int32_t *token_of_row, int32_t *row_of_pair,
-                              unsigned int *status, cudaStream_t s);
+                              unsigned int *status, int num_sms,
+                              cudaStream_t s);
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
                               int64_t n, uint16_t *res, cudaStream_t s);
 
