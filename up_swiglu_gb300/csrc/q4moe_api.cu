@@ -355,6 +355,7 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     a.matvec_max_rows = matvec_max;
 
     cudaError_t err = cudaSuccess;
+    a.matvec_last = matvec_max >= M;         // no GEMM launch after it
     if (matvec_max > 0 && (err = q4moe::launch_matvec(a, stream)) !=
                               cudaSuccess)
         return cuda_fail(err, "matvec launch");

@@ -176,6 +176,7 @@ constexpr int kGatherThreads = 256;
 __global__ void __launch_bounds__(kGatherThreads)
 gather_rows_kernel(GateUpArgs a) {
     extern __shared__ int32_t s_goff[];
+    grid_dependency_wait();
     for (int e = threadIdx.x; e <= a.E; e += blockDim.x)
         s_goff[e] = a.row_offsets[e];
     __syncthreads();
@@ -255,6 +256,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    grid_dependency_wait();
     // stage and check the row offsets
     for (int e = tid; e <= E; e += kThreads) {
         const int32_t v = a.row_offsets[e];
@@ -662,9 +664,8 @@ cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
         (int)smem);
     if (err != cudaSuccess)
         return err;
-    gemm_tcgen05_kernel<kTma><<<a.num_sms, kThreads, smem, s>>>(a, maps);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tcgen05_kernel<kTma>, dim3((unsigned)a.num_sms),
+                      dim3(kThreads), smem, s, a, maps);
 }
 
 }  // namespace
@@ -680,10 +681,10 @@ cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
     const int blocks = (int)std::min<int64_t>(
         (a.M + kGatherThreads / 32 - 1) / (kGatherThreads / 32),
         (int64_t)a.num_sms * 8);
-    gather_rows_kernel<<<blocks, kGatherThreads,
-                         sizeof(int32_t) * (size_t)(a.E + 1), s>>>(a);
-    count_launches(1);
-    if ((err = cudaGetLastError()) != cudaSuccess)
+    if ((err = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks),
+                          dim3(kGatherThreads),
+                          sizeof(int32_t) * (size_t)(a.E + 1), s, a)) !=
+        cudaSuccess)
         return err;
     return launch_gemm_kernel<true>(a, maps, s);
 }

@@ -47,6 +47,7 @@ group_rows_kernel(const int32_t *__restrict__ topk, int32_t pairs,
     const unsigned lt_mask = (1u << lane) - 1u;
     const int32_t b0q = kMulti ? (int32_t)blockIdx.x * seg : 0;
     const int32_t bq1 = kMulti ? min(pairs, b0q + seg) : pairs;
+    grid_dependency_wait();
     for (int j = tid; j < kWarps * E; j += kThreads)
         s_cnt[j] = 0;
     if (kMulti)
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads)
 group_count_kernel(const int32_t *__restrict__ topk, int32_t pairs,
                    int32_t seg, int32_t E, int32_t *__restrict__ row_of_pair) {
     extern __shared__ int32_t s_c[];
+    grid_dependency_wait();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         s_c[e] = 0;
     __syncthreads();
@@ -196,6 +198,7 @@ group_scan_kernel(int32_t nblk, int32_t seg, int32_t E,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bpw = (nblk + kWarps - 1) / kWarps;
     const int b0 = min(nblk, warp * bpw), b1 = min(nblk, b0 + bpw);
+    grid_dependency_wait();
     for (int e = lane; e < E; e += 32) {
         int32_t sum = 0;
         for (int b = b0; b < b1; ++b)
@@ -285,27 +288,26 @@ cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                  (int)scan_smem)) != cudaSuccess)
             return err;
-        group_count_kernel<<<nblk, kThreads, sizeof(int32_t) * (size_t)E,
-                             s>>>(topk, (int32_t)pairs, seg, E, row_of_pair);
-        group_scan_kernel<<<1, kThreads, scan_smem, s>>>(nblk, seg, E,
-                                                         row_offsets,
-                                                         row_of_pair);
-        group_rows_kernel<true><<<nblk, kThreads, smem, s>>>(
-            topk, (int32_t)pairs, seg, k, E, row_offsets, token_of_row,
-            row_of_pair, status);
-        count_launches(3);
-        return cudaGetLastError();
+        if ((err = launch_pdl(group_count_kernel, dim3(nblk), dim3(kThreads),
+                              sizeof(int32_t) * (size_t)E, s, topk,
+                              (int32_t)pairs, seg, E, row_of_pair)) !=
+                cudaSuccess ||
+            (err = launch_pdl(group_scan_kernel, dim3(1), dim3(kThreads),
+                              scan_smem, s, nblk, seg, E, row_offsets,
+                              row_of_pair)) != cudaSuccess)
+            return err;
+        return launch_pdl(group_rows_kernel<true>, dim3(nblk), dim3(kThreads),
+                          smem, s, topk, (int32_t)pairs, seg, k, E,
+                          row_offsets, token_of_row, row_of_pair, status);
     }
     err = cudaFuncSetAttribute(group_rows_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess)
         return err;
-    group_rows_kernel<false><<<1, kThreads, smem, s>>>(
-        topk, (int32_t)pairs, 0, k, E, row_offsets, token_of_row, row_of_pair,
-        status);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(group_rows_kernel<false>, dim3(1), dim3(kThreads), smem,
+                      s, topk, (int32_t)pairs, 0, k, E, row_offsets,
+                      token_of_row, row_of_pair, status);
 }
 
 }  // namespace q4moe

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -31,10 +32,45 @@ struct GateUpArgs {
     int32_t matvec_max_rows;     // experts with more rows go to the GEMM
     int32_t num_sms;
     int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
+    int32_t matvec_last;         // no GEMM launch follows the matvec's
 };
 
 // Host-side count of kernel launches (q4moe_launch_count).
 void count_launches(int n);
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with launch_pdl, so that its launch and set-up overlap the end of the
+// previous kernel on the stream; each one calls grid_dependency_wait before
+// it reads any input or writes any output (it returns once the previous
+// kernel has completed and its memory is visible).  The next kernel may
+// start launching as this one's blocks exit; only the matvec, when it is
+// the call's last kernel, lets it start at once (grid_launch_dependents):
+// measured, an early start slows a following GEMM, gather or grouping.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err =
+        cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    count_launches(1);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
 
 // Record `message` as the calling thread's last error; returns `code`.
 int report_error(int code, const char *message);

@@ -35,6 +35,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 matvec_generic_kernel(GateUpArgs a) {
     __shared__ int32_t s_off[Q4MOE_MAX_EXPERTS + 1];
+    grid_dependency_wait();
     if (!stage_row_offsets(a, s_off))
         return;
     const int e = blockIdx.y;
@@ -112,6 +113,7 @@ matvec_generic_kernel(GateUpArgs a) {
 
 __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
                                   int64_t n, uint16_t *res) {
+    grid_dependency_wait();
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         const uint16_t gT = bf16_rne(bf16_f32(g[j]));
@@ -133,9 +135,8 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
         return launch_matvec_mma(a, s);
     const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),
                     (unsigned)a.E);
-    matvec_generic_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(matvec_generic_kernel, grid, dim3(kWarpsPerBlock * 32),
+                      0, s, a);
 }
 
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
@@ -143,9 +144,8 @@ cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
     if (n == 0)
         return cudaSuccess;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
-    debug_tail_kernel<<<blocks, 256, 0, s>>>(g, u, n, res);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(debug_tail_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                      s, g, u, n, res);
 }
 
 }  // namespace q4moe

@@ -178,6 +178,9 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
     const int GB = ceil_div(IBk, kSlots);          // groups per chunk
     const int steps = H / kStepK;                  // K steps in a row
     const int spw = ceil_div(steps, S);            // steps per warp per task
+    if (a.matvec_last)
+        grid_launch_dependents();
+    grid_dependency_wait();
 
     if (!stage_row_offsets(a, s_off))
         return;
@@ -390,9 +393,8 @@ cudaError_t launch_split(const GateUpArgs &a, size_t smem, int tok_cap,
         (int)smem);
     if (err != cudaSuccess)
         return err;
-    matvec_mma_kernel<S, R><<<a.num_sms, kThreads, smem, s>>>(a, tok_cap);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_pdl(matvec_mma_kernel<S, R>, dim3((unsigned)a.num_sms),
+                      dim3(kThreads), smem, s, a, tok_cap);
 }
 
 size_t matvec_smem(const GateUpArgs &a, int S, int R, int tok_cap) {

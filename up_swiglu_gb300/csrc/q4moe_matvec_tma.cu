@@ -246,16 +246,6 @@ __device__ __forceinline__ bool wait_full(uint64_t *bar, uint32_t parity,
            wait_phase(bar, parity, abort, status);
 }
 
-// Programmatic dependent launch: wait for the grids this one depends on
-// (and their memory) before touching any input; let dependents start
-// launching.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Barrier of the 16 consumer warps only (the producer keeps issuing).
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
@@ -312,7 +302,8 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
         tma_desc_prefetch(&tm_gate);
         tma_desc_prefetch(&tm_up);
     }
-    grid_launch_dependents();
+    if (a.matvec_last)
+        grid_launch_dependents();
     grid_dependency_wait();
 
     int u0 = 0, u1 = 0;
@@ -634,26 +625,11 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
                                (int)smem);
     if (err != cudaSuccess)
         return err;
-    // programmatic dependent launch: the kernel's set-up overlaps the end
-    // of the previous kernel on the stream; it waits for that kernel's
-    // results before reading any input
     // a single expert's rows all above the matvec's limit: nothing to do
     if (a.E == 1 && a.M > a.matvec_max_rows)
         return cudaSuccess;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.num_sms);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, matvec_tma_kernel<NB>, a, mg, mu, tok_cap,
-                             D);
-    count_launches(1);
-    return err != cudaSuccess ? err : cudaGetLastError();
+    return launch_pdl(matvec_tma_kernel<NB>, dim3((unsigned)a.num_sms),
+                      dim3(kThreads), smem, s, a, mg, mu, tok_cap, D);
 }
 
 }  // namespace
