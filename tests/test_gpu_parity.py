@@ -205,6 +205,19 @@ def test_parity_reduced_workloads(kernel, E, T, k, routing, x_std):
     _run_and_compare(p, kernel=kernel)
 
 
+@pytest.mark.parametrize("big", [13, 12])
+def test_auto_mixes_matvec_and_gemm(big):
+    """Automatic choice with I = 1536 (12 GEMM tiles per expert chunk):
+    13 experts above 48 rows make 156 tiles, enough for one per SM, and go
+    to the GEMM while the small ones stay on the matvec; 12 make 144 and the
+    matvec takes every expert.  Either way the oracle's results."""
+    counts = [60] * big + [1, 8, 9, 48, 0, 17]
+    p = hz.problem_with_counts(80 + big, counts, 1536, 512, exact=True)
+    _run_and_compare(p, exact=True)
+    p = hz.problem_with_counts(90 + big, counts, 1536, 512)
+    _run_and_compare(p)
+
+
 @pytest.mark.parametrize("counts", [[0, 1, 7, 8, 9, 47, 48, 49, 63, 64, 65,
                                      129, 200, 257]])
 def test_parity_ragged_rows_per_expert(counts):

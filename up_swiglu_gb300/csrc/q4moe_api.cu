@@ -350,7 +350,15 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
                         "== 0 and 16-byte aligned slab sections");
         matvec_max = 0;
     } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
-        matvec_max = 48;
+        // experts above 48 rows go to the GEMM if they fill the GPU with
+        // tiles (decided on the device); a single expert's count is known
+        const int64_t tiles = (M + 255) / 256 * (I / 128);
+        if (slabs->num_experts > 1) {
+            matvec_max = 48;
+            a.gemm_min_tiles = d->num_sms;
+        } else if (M > 48 && tiles >= d->num_sms) {
+            matvec_max = 0;
+        }
     }
     a.matvec_max_rows = matvec_max;
 

@@ -180,6 +180,7 @@ gather_rows_kernel(GateUpArgs a) {
     for (int e = threadIdx.x; e <= a.E; e += blockDim.x)
         s_goff[e] = a.row_offsets[e];
     __syncthreads();
+    const int32_t mvmax = matvec_limit(a, s_goff);
     const int lane = threadIdx.x & 31;
     const int64_t chunks = a.H / 8;
     const int64_t wpb = blockDim.x / 32;
@@ -194,7 +195,7 @@ gather_rows_kernel(GateUpArgs a) {
             else
                 hi = mid;
         }
-        if (s_goff[lo + 1] - s_goff[lo] <= a.matvec_max_rows)
+        if (s_goff[lo + 1] - s_goff[lo] <= mvmax)
             continue;
         int64_t t = 0;
         if (lane == 0)
@@ -269,6 +270,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
     __syncthreads();
     tc_fence_after();
     const bool offsets_ok = ctl->bad_offsets == 0;
+    const int32_t mvmax = matvec_limit(a, s_off);
     if (!offsets_ok && tid == 0 && blockIdx.x == 0)
         atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
     // tiles per expert (experts above the matvec's row limit), prefix sums
@@ -278,7 +280,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
         int sum = 0;
         for (int e = e0; e < min(E, e0 + per); ++e) {
             const int n_e = s_off[e + 1] - s_off[e];
-            sum += (n_e > a.matvec_max_rows && n_e > 0)
+            sum += (n_e > mvmax && n_e > 0)
                        ? IB * ceil_div(n_e, NMAX) : 0;
         }
         int incl = sum;
@@ -292,7 +294,7 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
         for (int e = e0; e < min(E, e0 + per); ++e) {
             s_pre[e] = run;
             const int n_e = s_off[e + 1] - s_off[e];
-            run += (n_e > a.matvec_max_rows && n_e > 0)
+            run += (n_e > mvmax && n_e > 0)
                        ? IB * ceil_div(n_e, NMAX) : 0;
         }
         if (lane == 31)

@@ -38,10 +38,11 @@ matvec_generic_kernel(GateUpArgs a) {
     grid_dependency_wait();
     if (!stage_row_offsets(a, s_off))
         return;
+    const int32_t mvmax = matvec_limit(a, s_off);
     const int e = blockIdx.y;
     const int32_t r0 = s_off[e], r1 = s_off[e + 1];
     const int32_t rows = r1 - r0;
-    if (rows == 0 || rows > a.matvec_max_rows)
+    if (rows == 0 || rows > mvmax)
         return;
     const uint8_t *slab = expert_slab(a, e);
     if (slab == nullptr)

@@ -184,12 +184,13 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
 
     if (!stage_row_offsets(a, s_off))
         return;
+    const int32_t mvmax = matvec_limit(a, s_off);
     if (warp == 0) {
         const int per = ceil_div(E, 32);
         const int e0 = lane * per;
         int sum = 0;
         for (int e = e0; e < min(E, e0 + per); ++e)
-            sum += groups_of(s_off[e + 1] - s_off[e], a.matvec_max_rows, GB);
+            sum += groups_of(s_off[e + 1] - s_off[e], mvmax, GB);
         int incl = sum;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -200,7 +201,7 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
         int run = incl - sum;
         for (int e = e0; e < min(E, e0 + per); ++e) {
             s_pre[e] = run;
-            run += groups_of(s_off[e + 1] - s_off[e], a.matvec_max_rows, GB);
+            run += groups_of(s_off[e + 1] - s_off[e], mvmax, GB);
         }
         if (lane == 31)
             s_pre[E] = incl;

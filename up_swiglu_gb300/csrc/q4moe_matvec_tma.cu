@@ -308,13 +308,13 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
 
     int u0 = 0, u1 = 0;
     if (stage_row_offsets(a, s_off)) {       // (synchronises the block)
+        const int32_t mvmax = matvec_limit(a, s_off);
         if (warp == 0) {
             const int per = ceil_div(E, 32);
             const int e0 = lane * per;
             int sum = 0;
             for (int e = e0; e < min(E, e0 + per); ++e)
-                sum += units_of(s_off[e + 1] - s_off[e], a.matvec_max_rows,
-                                NT);
+                sum += units_of(s_off[e + 1] - s_off[e], mvmax, NT);
             int incl = sum;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -325,8 +325,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
             int run = incl - sum;
             for (int e = e0; e < min(E, e0 + per); ++e) {
                 s_pre[e] = run;
-                run += units_of(s_off[e + 1] - s_off[e], a.matvec_max_rows,
-                                NT);
+                run += units_of(s_off[e + 1] - s_off[e], mvmax, NT);
             }
             if (lane == 31)
                 s_pre[E] = incl;
