@@ -30,8 +30,11 @@
  *    device; "host" pointers are ordinary host memory.  Every buffer is
  *    borrowed: the caller owns it and keeps it alive until the work queued
  *    on `stream` has completed.
- *  - GPU entry points are asynchronous on `stream`, never synchronise the
- *    host, and allocate no memory.  Argument errors the host can see are
+ *  - GPU entry points are asynchronous on `stream` and allocate no memory.
+ *    They never synchronise the host, except once per device: the first
+ *    call on a device fills a 128 KB table in the library's own device
+ *    memory (the bf16 sigmoid of every bf16 value) and waits for it, so
+ *    that first call must not be made while a stream is being captured.  Argument errors the host can see are
  *    returned before anything is launched.  Inconsistent data that only the
  *    GPU can see (row offsets, token indices, expert ids, slab pointers) sets
  *    a bit in the device status word (Q4MOE_DEV_*) and the affected rows are

@@ -39,6 +39,8 @@ int cuda_fail(cudaError_t err, const char *what) {
 // inconsistent device-side data.  One per device (a __device__ variable
 // exists once in every device context that loads the library).
 __device__ unsigned int g_status_word;
+// bf16 sigmoid of every bf16 gate value, built at the first call on a device
+__device__ uint16_t g_sigmoid_table[65536];
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -46,6 +48,7 @@ struct DeviceInfo {
     bool supported = false;
     int num_sms = 0;
     unsigned int *status = nullptr;
+    const uint16_t *sigmoid = nullptr;
     char why[160] = {0};
 };
 DeviceInfo g_devices[kMaxDevices];
@@ -85,6 +88,22 @@ int device_info(DeviceInfo **out) {
             if (err != cudaSuccess)
                 return cuda_fail(err, "cudaGetSymbolAddress(status word)");
             d.status = static_cast<unsigned int *>(p);
+            // the sigmoid table, built once on a private stream
+            if ((err = cudaGetSymbolAddress(&p, g_sigmoid_table)) !=
+                cudaSuccess)
+                return cuda_fail(err, "cudaGetSymbolAddress(sigmoid table)");
+            cudaStream_t s = nullptr;
+            if ((err = cudaStreamCreateWithFlags(
+                     &s, cudaStreamNonBlocking)) != cudaSuccess)
+                return cuda_fail(err, "cudaStreamCreateWithFlags");
+            err = q4moe::launch_build_sigmoid_table(
+                static_cast<uint16_t *>(p), s);
+            if (err == cudaSuccess)
+                err = cudaStreamSynchronize(s);
+            cudaStreamDestroy(s);
+            if (err != cudaSuccess)
+                return cuda_fail(err, "sigmoid table");
+            d.sigmoid = static_cast<const uint16_t *>(p);
         }
         d.ready = true;
     }
@@ -340,6 +359,7 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     a.status = d->status;
     a.num_sms = d->num_sms;
     a.matvec_tile = o.matvec_tile;
+    a.sigmoid = d->sigmoid;
 
     const bool gemm_ok = q4moe::gemm_supported(H, I, a);
     int32_t matvec_max = INT32_MAX;
@@ -418,7 +438,7 @@ int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
     if (rc)
         return rc;
     cudaError_t err = q4moe::launch_debug_tail(gate_bf16, up_bf16, n, res,
-                                               stream);
+                                               d->sigmoid, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, "debug tail launch");
     return ok();

@@ -555,9 +555,8 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                 if (!slab)
                     continue;
                 // all 16 columns branch-free (independent chains the
-                // scheduler can interleave); the rare exact sigmoids after
+                // scheduler can interleave); sigmoids from the table
                 float gT[16], uT[16], sT[16];
-                uint32_t slow = 0;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const float g32 = __fmul_rn(__uint_as_float(gv[jj]), sg);
@@ -566,15 +565,9 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                     uv[jj] = __float_as_uint(u32);
                     gT[jj] = bf16_round(g32);
                     uT[jj] = bf16_round(u32);
-                    bool ok;
-                    sT[jj] = sigmoid_bf16_fast_f(gT[jj], &ok);
-                    slow |= (ok ? 0u : 1u) << jj;
-                }
-                if (slow) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        if (slow & (1u << jj))
-                            sT[jj] = bf16_f32(sigmoid_bf16_exact(gT[jj]));
+                    sT[jj] = bf16_f32(sigmoid_bf16_table(
+                        a.sigmoid,
+                        (uint16_t)(__float_as_uint(gT[jj]) >> 16)));
                 }
                 const int64_t o0 = (int64_t)(ti.row0 + c0) * a.I + i;
 #pragma unroll

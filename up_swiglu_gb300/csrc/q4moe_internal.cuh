@@ -34,6 +34,8 @@ struct GateUpArgs {
     int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
     int32_t matvec_last;         // no GEMM launch follows the matvec's
     int32_t gemm_min_tiles;      // > 0: the automatic choice (matvec_limit)
+    const uint16_t *sigmoid;     // sigmoid table: [65536] bf16, indexed by
+                                 // the bf16 bits of gateT
 };
 
 // Host-side count of kernel launches (q4moe_launch_count).
@@ -89,7 +91,9 @@ cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                               unsigned int *status, int num_sms,
                               cudaStream_t s);
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
-                              int64_t n, uint16_t *res, cudaStream_t s);
+                              int64_t n, uint16_t *res,
+                              const uint16_t *sigmoid, cudaStream_t s);
+cudaError_t launch_build_sigmoid_table(uint16_t *table, cudaStream_t s);
 
 // ------------------------------------------------------------------------
 // bf16 helpers.  Rounding: nearest, ties to even (page 54, codebook.ts,
@@ -188,21 +192,42 @@ __device__ __forceinline__ uint16_t sigmoid_bf16(float g) {
     return ok ? s : sigmoid_bf16_exact(g);
 }
 
+// sigmoidT depends on the 16 bits of gateT only: the kernels read it from a
+// table of all 65,536 values, built once per device from sigmoid_bf16 (so
+// the table and the direct computation agree bit for bit; both are tested
+// against the oracle on every input).  The table is 128 KB and stays in L2.
+__device__ __forceinline__ uint16_t sigmoid_bf16_table(const uint16_t *table,
+                                                       uint16_t gT) {
+    return __ldg(table + gT);
+}
+
 // gateT, upT -> out (bf16 bits).  sig and silu are also returned.
-__device__ __forceinline__ uint16_t swiglu_tail_bits(uint16_t gT, uint16_t uT,
+__device__ __forceinline__ uint16_t swiglu_tail_bits(const uint16_t *table,
+                                                     uint16_t gT, uint16_t uT,
                                                      uint16_t *sigT,
                                                      uint16_t *siluT) {
     const float g = bf16_f32(gT);
-    const uint16_t s = sigmoid_bf16(g);
+    const uint16_t s = sigmoid_bf16_table(table, gT);
     const uint16_t si = bf16_rne(__fmul_rn(g, bf16_f32(s)));
     *sigT = s;
     *siluT = si;
     return bf16_rne(__fmul_rn(bf16_f32(si), bf16_f32(uT)));
 }
 
-__device__ __forceinline__ uint16_t swiglu_out(float gate32, float up32) {
-    uint16_t s, si;
-    return swiglu_tail_bits(bf16_rne(gate32), bf16_rne(up32), &s, &si);
+// The same for one element whose latency matters more than its count (the
+// matvec's few outputs per thread): the sigmoid computed in registers when
+// the fast form is conclusive (it then equals the table entry, which was
+// built by the same function), the table only otherwise.
+__device__ __forceinline__ uint16_t swiglu_out(const uint16_t *table,
+                                               float gate32, float up32) {
+    const uint16_t gT = bf16_rne(gate32), uT = bf16_rne(up32);
+    const float g = bf16_f32(gT);
+    bool ok;
+    uint16_t s = sigmoid_bf16_fast(g, &ok);
+    if (!ok)
+        s = sigmoid_bf16_table(table, gT);
+    const uint16_t si = bf16_rne(__fmul_rn(g, bf16_f32(s)));
+    return bf16_rne(__fmul_rn(bf16_f32(si), bf16_f32(uT)));
 }
 
 // Slab of expert e; null (and a status bit) for a misaligned table entry.

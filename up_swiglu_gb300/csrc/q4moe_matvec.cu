@@ -101,7 +101,7 @@ matvec_generic_kernel(GateUpArgs a) {
                     const float g32 = __fmul_rn(G, gs[i]);
                     const float u32 = __fmul_rn(U, us[i]);
                     const int64_t o = (int64_t)(p0 + j) * a.I + i;
-                    a.out[o] = swiglu_out(g32, u32);
+                    a.out[o] = swiglu_out(a.sigmoid, g32, u32);
                     if (a.gate_f32)
                         a.gate_f32[o] = g32;
                     if (a.up_f32)
@@ -113,13 +113,14 @@ matvec_generic_kernel(GateUpArgs a) {
 }
 
 __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
-                                  int64_t n, uint16_t *res) {
+                                  int64_t n, uint16_t *res,
+                                  const uint16_t *table) {
     grid_dependency_wait();
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         const uint16_t gT = bf16_rne(bf16_f32(g[j]));
         uint16_t s, si;
-        const uint16_t o = swiglu_tail_bits(gT, u[j], &s, &si);
+        const uint16_t o = swiglu_tail_bits(table, gT, u[j], &s, &si);
         res[4 * j + 0] = s;
         res[4 * j + 1] = si;
         res[4 * j + 2] = o;
@@ -141,12 +142,28 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
-                              uint16_t *res, cudaStream_t s) {
+                              uint16_t *res, const uint16_t *sigmoid,
+                              cudaStream_t s) {
     if (n == 0)
         return cudaSuccess;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
     return launch_pdl(debug_tail_kernel, dim3((unsigned)blocks), dim3(256), 0,
-                      s, g, u, n, res);
+                      s, g, u, n, res, sigmoid);
+}
+
+namespace {
+// sigmoid_bf16 of every bf16 value (the kernels' table)
+__global__ void build_sigmoid_table_kernel(uint16_t *table) {
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < 65536;
+         j += gridDim.x * blockDim.x)
+        table[j] = sigmoid_bf16(bf16_f32((uint16_t)j));
+}
+}  // namespace
+
+cudaError_t launch_build_sigmoid_table(uint16_t *table, cudaStream_t s) {
+    build_sigmoid_table_kernel<<<256, 256, 0, s>>>(table);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace q4moe

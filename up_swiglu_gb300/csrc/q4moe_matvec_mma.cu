@@ -367,7 +367,7 @@ matvec_mma_kernel(GateUpArgs a, int tok_cap) {
                                     __fmul_rn(acc[i][2 + jj], su);
                                 const int64_t o =
                                     (int64_t)(k.p0 + n) * a.I + row;
-                                a.out[o] = swiglu_out(g32, u32);
+                                a.out[o] = swiglu_out(a.sigmoid, g32, u32);
                                 if (a.gate_f32)
                                     a.gate_f32[o] = g32;
                                 if (a.up_f32)

@@ -549,7 +549,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                             const float u32 = __fmul_rn(
                                 __fmul_rn(acc[i][2 + jj], unscale), su[i]);
                             const int64_t o = (int64_t)(t.p0 + n) * a.I + row;
-                            a.out[o] = swiglu_out(g32, u32);
+                            a.out[o] = swiglu_out(a.sigmoid, g32, u32);
                             if (a.gate_f32)
                                 a.gate_f32[o] = g32;
                             if (a.up_f32)
