@@ -343,6 +343,26 @@ def cpu_value(w, units, sec_per_row):
     return units["weight_bytes"] / t_step / 1e9, t_step
 
 
+# --------------------------------------------------------------- replicas --
+
+def max_over_ranks(ms: float, dist=None, device=None) -> float:
+    """The slowest rank's time (every rank gets it); ms itself alone."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rates(units: dict, steps: int, world: int, total_ms: float):
+    """Whole-job weight GB/s and TFLOP/s: every replica processes the same
+    units per step, over the slowest replica's time."""
+    sec = total_ms * 1e-3
+    return (units["weight_bytes"] * steps * world / sec / 1e9,
+            units["flops"] * steps * world / sec / 1e12)
+
+
 # ------------------------------------------------------------------- main --
 
 def run_reference(args, w, rank, world):
@@ -454,14 +474,9 @@ def main():
         launches = gw.launches_per_step * args.steps
     total_ms = t_start.elapsed_time(t_stop)
     gate_up_ms = [ev[k][1].elapsed_time(ev_end[k]) for k in range(args.steps)]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    world_weight = units["weight_bytes"] * args.steps * world
-    value = world_weight / (total_ms * 1e-3) / 1e9
-    tflops = units["flops"] * args.steps * world / (total_ms * 1e-3) / 1e12
+    value, tflops = job_rates(units, args.steps, world, total_ms)
     clocks = clk.summary()
 
     # roofline of the dominant kernel: the fused gate/up launch(es)

@@ -417,6 +417,26 @@ def test_single_expert_several_chunks(exact):
     _run_and_compare(p, exact=exact)
 
 
+@pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
+def test_single_chunk_bad_token_reads_zeros(kernel):
+    """One expert, 6 rows (a single chunk, whose rows of x move as bulk
+    copies): a token index past num_tokens sets the status bit and its row
+    is computed from zeros; the other rows are the oracle's."""
+    p = hz.problem_with_counts(15, [6], 256, 1024, exact=True)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    bad = tok.clone()
+    bad[2] = p.T + 1
+    q.q4moe_device_status(clear=True)
+    res = hz.gate_up(d, offs, bad, kernel=kernel)
+    assert q.q4moe_device_status(clear=True) == q.DEV_BAD_TOKEN
+    assert np.all(res["out"][2] == 0) and np.all(res["gate32"][2] == 0)
+    good = hz.gate_up(d, offs, tok, kernel=kernel)
+    rows = np.arange(6) != 2
+    assert np.array_equal(res["out"][rows], good["out"][rows])
+    _run_and_compare(p, kernel=kernel, exact=True)
+
+
 def test_misaligned_slab_pointer_raises_status():
     import torch
     p = hz.random_problem(8, 2, 16, 64, 3, 1)
