@@ -7,7 +7,7 @@ and it imports nothing from the CUDA library's package.
 The arithmetic lives in ``q4moe_oracle.c`` (plain C, f64 accumulation); this
 module compiles it with gcc on first use and marshals numpy arrays.  Every
 function cites the passage it follows in the C source.  ``group_rows``,
-``tail`` and ``gate_up_swiglu`` are pinned by the ``-m "not gpu"`` tests in
+``tail``, ``gate_up_swiglu``, ``down_proj`` and ``expert_mlp`` are pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -69,6 +69,13 @@ def _load():
         lib.q4o_gate_up_swiglu_sampled.argtypes = [
             _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I64, _INT,
             _I64, _P, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_down_proj.restype = _INT
+        lib.q4o_down_proj.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_down_proj_sampled.restype = _INT
+        lib.q4o_down_proj_sampled.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
+            _INT]
         lib.q4o_group_rows.restype = _INT
         lib.q4o_group_rows.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
         lib.q4o_max_threads.restype = _INT
@@ -200,3 +207,68 @@ def gate_up_swiglu_sampled(x_bits, gate_w, up_w, gate_s, up_s, row_offsets,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return res
+
+
+def down_proj(mid_bits, down_w, down_s, row_offsets, nthreads: int = 0,
+              want_debug: bool = False):
+    """All M x H outputs of the grouped down projection (page 52,
+    streamed-experts.ts, DOWN_SOURCE).
+
+    mid_bits bf16 bits [M, I] (grouped order); down_w uint32 [E, H, I/8];
+    down_s f32 [E, H]; row_offsets int32 [E+1].  Returns out bits [M, H], or
+    with want_debug a dict with out, out32 (f32 before the bf16 rounding) and
+    dabs (f64 sums of |w*mid|)."""
+    mid = _c(mid_bits, np.uint16)
+    dw, ds = _c(down_w, np.uint32), _c(down_s, np.float32)
+    offs = _c(row_offsets, np.int32)
+    M, I = mid.shape
+    E, H, _ = dw.shape
+    out = np.zeros((M, H), dtype=np.uint16)
+    dbg = None
+    if want_debug:
+        dbg = dict(out32=np.zeros((M, H), np.float32),
+                   dabs=np.zeros((M, H), np.float64))
+    g = (lambda k: _ptr(dbg[k])) if dbg else (lambda k: None)
+    rc = _load().q4o_down_proj(_ptr(mid), M, I, H, E, _ptr(dw), _ptr(ds),
+                               _ptr(offs), _ptr(out), g("out32"), g("dabs"),
+                               int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    if dbg is not None:
+        dbg["out"] = out
+        return dbg
+    return out
+
+
+def down_proj_sampled(mid_bits, down_w, down_s, row_offsets, rows, cols,
+                      nthreads: int = 0):
+    """The down projection at (rows[j], cols[j]) only; mid_bits must hold
+    every row that rows names (other rows may be anything).  Returns a dict
+    with out (bf16 bits), out32 (f32) and dabs (f64), each of length n."""
+    mid = _c(mid_bits, np.uint16)
+    dw, ds = _c(down_w, np.uint32), _c(down_s, np.float32)
+    offs = _c(row_offsets, np.int32)
+    r, c = _c(rows, np.int64), _c(cols, np.int64)
+    M, I = mid.shape
+    E, H, _ = dw.shape
+    n = r.shape[0]
+    res = dict(out=np.zeros(n, np.uint16), out32=np.zeros(n, np.float32),
+               dabs=np.zeros(n, np.float64))
+    rc = _load().q4o_down_proj_sampled(
+        _ptr(mid), M, I, H, E, _ptr(dw), _ptr(ds), _ptr(offs), n, _ptr(r),
+        _ptr(c), _ptr(res["out"]), _ptr(res["out32"]), _ptr(res["dabs"]),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return res
+
+
+def expert_mlp(x_bits, gate_w, up_w, gate_s, up_s, down_w, down_s,
+               row_offsets, token_of_row, nthreads: int = 0):
+    """The whole routed expert MLP as the page runs it (page 52,
+    streamed-experts.ts: the gate/up kernel writes mid, the down kernel
+    reads it): returns (mid bits [M, I], out bits [M, H])."""
+    mid = gate_up_swiglu(x_bits, gate_w, up_w, gate_s, up_s, row_offsets,
+                         token_of_row, nthreads=nthreads)
+    return mid, down_proj(mid, down_w, down_s, row_offsets,
+                          nthreads=nthreads)

@@ -15,6 +15,10 @@
  *    bf16);
  *  - page 54, src/kernels/trellis/codebook.ts, trellis_bf16: the f32 -> bf16
  *    rounding (round to nearest, ties to even, on the bit pattern);
+ *  - page 52, DOWN_SOURCE: the down projection that follows gate/up in the
+ *    same expert (the row of packed words belongs to output row h and runs
+ *    over the intermediate index k; f32 accumulation; times the f32 row
+ *    scale of h; rounded to bf16);
  *  - page 51, src/kernels/glm52/layout.ts: the per-expert section layout
  *    (the oracle takes the sections as separate arrays, so it never parses
  *    a slab).
@@ -251,6 +255,98 @@ int q4o_gate_up_swiglu_sampled(const uint16_t *x, int64_t T, int64_t H,
                     token_of_row[p], i, silu_mode, &out[j],
                     gate32 ? &gate32[j] : 0, up32 ? &up32[j] : 0, 0, 0,
                     gabs ? &gabs[j] : 0, uabs ? &uabs[j] : 0);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* ---- the down projection ------------------------------------------------
+ * Page 52, streamed-experts.ts, DOWN_SOURCE, run after gate/up on the same
+ * expert slot: grouped row p (of expert e) of the intermediate activations
+ * mid, output row h:
+ *   D = sum_k (nib(down_w[e][h][k/8], k%8) - 8) * mid[p][k]
+ *   out[p][h] = bf16(f32(D * down_s[e][h]))
+ * mid:         bf16 bits [M, I] in grouped-row order (the gate/up output)
+ * down_w:      uint32 [E, H, I/8] (row h of expert e: I/8 packed words)
+ * down_s:      f32 [E, H]
+ * row_offsets: int32 [E+1]
+ * out:         bf16 bits [M, H] in grouped-row order
+ * Optional (NULL to skip): out32 f32 [M, H] (the value before the bf16
+ * rounding), dabs f64 [M, H] (sum_k |w*mid|).  The sum is taken in f64
+ * (exact products), rounded once to f32 with the scale, as for gate/up. */
+static int q4o_down_check(int64_t M, int64_t I, int64_t H, int32_t E,
+                          const int32_t *row_offsets)
+{
+    if (M < 0 || I <= 0 || H <= 0 || E <= 0 || (I % 8) != 0)
+        return -1;
+    if (row_offsets[0] != 0 || row_offsets[E] != M)
+        return -2;
+    for (int32_t e = 0; e < E; ++e)
+        if (row_offsets[e + 1] < row_offsets[e])
+            return -2;
+    return 0;
+}
+
+static void q4o_down_element(const uint16_t *mid, int64_t I, int64_t H,
+                             const uint32_t *down_w, const float *down_s,
+                             int32_t e, int64_t p, int64_t h, uint16_t *out,
+                             float *out32, double *dabs)
+{
+    const uint32_t *wrow = down_w + ((int64_t)e * H + h) * (I / 8);
+    double a;
+    const double D = q4o_dot(wrow, mid + p * I, I, &a);
+    const float v = (float)(D * (double)down_s[(int64_t)e * H + h]);
+    *out = q4o_bf16_rne(v);
+    if (out32) *out32 = v;
+    if (dabs) *dabs = a;
+}
+
+int q4o_down_proj(const uint16_t *mid, int64_t M, int64_t I, int64_t H,
+                  int32_t E, const uint32_t *down_w, const float *down_s,
+                  const int32_t *row_offsets, uint16_t *out, float *out32,
+                  double *dabs, int nthreads)
+{
+    const int rc = q4o_down_check(M, I, H, E, row_offsets);
+    if (rc != 0)
+        return rc;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+#endif
+    for (int64_t ph = 0; ph < M * H; ++ph) {
+        const int64_t p = ph / H, h = ph % H;
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        q4o_down_element(mid, I, H, down_w, down_s, e, p, h, &out[ph],
+                         out32 ? &out32[ph] : 0, dabs ? &dabs[ph] : 0);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* The same for n chosen elements (rows[j], cols[j]); outputs indexed by j. */
+int q4o_down_proj_sampled(const uint16_t *mid, int64_t M, int64_t I,
+                          int64_t H, int32_t E, const uint32_t *down_w,
+                          const float *down_s, const int32_t *row_offsets,
+                          int64_t n, const int64_t *rows, const int64_t *cols,
+                          uint16_t *out, float *out32, double *dabs,
+                          int nthreads)
+{
+    const int rc = q4o_down_check(M, I, H, E, row_offsets);
+    if (rc != 0)
+        return rc;
+    for (int64_t j = 0; j < n; ++j)
+        if (rows[j] < 0 || rows[j] >= M || cols[j] < 0 || cols[j] >= H)
+            return -4;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        const int32_t e = q4o_expert_of_row(row_offsets, E, rows[j]);
+        q4o_down_element(mid, I, H, down_w, down_s, e, rows[j], cols[j],
+                         &out[j], out32 ? &out32[j] : 0, dabs ? &dabs[j] : 0);
     }
     (void)nthreads;
     return 0;

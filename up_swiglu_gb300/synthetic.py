@@ -21,7 +21,10 @@ Recipe (the workloads' shapes and value distributions):
   other with probability proportional to ``rank**-a`` over the experts not
   yet drawn (expert id = rank - 1);
 - the exact-integer case: activations integer-valued in [-8, 8], scales
-  ``2**-k`` with k uniform in 4..9, so every dot product is exact in f32.
+  ``2**-k`` with k uniform in 4..9, so every dot product is exact in f32;
+- the down projection's weights and scales follow the same recipe (own
+  streams); its exact case draws the intermediate activations as integers
+  in [-8, 8] and the scales as ``2**-k``, k uniform in 4..9.
 """
 from __future__ import annotations
 
@@ -37,6 +40,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # stream ids (distinct per array kind)
 S_X, S_GATE_W, S_UP_W, S_GATE_S, S_UP_S, S_ROUTE, S_EXACT_X, S_EXACT_S = \
     range(1, 9)
+S_DOWN_W, S_DOWN_S, S_EXACT_MID, S_EXACT_DS = range(9, 13)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -117,6 +121,30 @@ def weights(seed: int, E: int, I: int, H: int):
     up_s = (0.002 + 0.018 * uniform(seed, S_UP_S, E * I)).astype(
         np.float32).reshape(E, I)
     return gate_w, up_w, gate_s, up_s
+
+
+def down_weights(seed: int, E: int, H: int, I: int):
+    """down_w uint32 [E, H, I/8] and down_s f32 [E, H] (the same recipe as
+    gate/up, own streams)."""
+    assert I % 8 == 0
+    n = E * H * (I // 8)
+    down_w = words_u32(seed, S_DOWN_W, n).reshape(E, H, I // 8)
+    down_s = (0.002 + 0.018 * uniform(seed, S_DOWN_S, E * H)).astype(
+        np.float32).reshape(E, H)
+    return down_w, down_s
+
+
+def exact_down_case(seed: int, M: int, I: int, E: int, H: int):
+    """Intermediate activations integer-valued in [-8, 8] (bf16 bits
+    [M, I]), power-of-two scales 2**-k, k in 4..9 (f32 [E, H]) and the packed
+    words of ``down_weights``: every dot product is an integer below 2**24 in
+    magnitude, exact in f32 in any summation order."""
+    mi = (u64(seed, S_EXACT_MID, M * I) % np.uint64(17)).astype(np.int64) - 8
+    mid = f32_to_bf16_bits(mi.astype(np.float32)).reshape(M, I)
+    ks = (u64(seed, S_EXACT_DS, E * H) % np.uint64(6)).astype(np.int64) + 4
+    ds = np.ldexp(np.float32(1.0), -ks).astype(np.float32).reshape(E, H)
+    down_w, _ = down_weights(seed, E, H, I)
+    return mid, down_w, ds
 
 
 def route_uniform(seed: int, T: int, k: int, E: int) -> np.ndarray:
