@@ -22,6 +22,15 @@
  * [-8, 8] and power-of-two scales every sum is exact and the output is
  * bit-exact.
  *
+ * The down projection of the same page (DOWN_SOURCE), which the page's
+ * executor runs on the gate/up output mid of the same expert slot, completes
+ * the expert MLP: for output row h < H,
+ *
+ *   out[p][h] = bf16(f32(sum_k (nib(down_w[e][h][k/8], k%8) - 8) * mid[p][k])
+ *                    * down_s[e][h])
+ *
+ * (q4moe_down_proj; q4moe_expert_mlp runs both).
+ *
  * Conventions for every entry point:
  *  - Return 0 (Q4MOE_OK) or a negative Q4MOE_ERR_* code; no C++ exception
  *    crosses the ABI.  q4moe_last_error() gives the calling thread's message
@@ -51,7 +60,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 3
+#define Q4MOE_ABI_VERSION 4
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -83,22 +92,29 @@ extern "C" {
 
 /*
  * Byte layout of one expert slab (page 51, layout.ts,
- * Glm52CanonicalMetalLayout, restricted to the sections this operation
- * reads).  Offsets are bytes from the start of the slab.
+ * Glm52CanonicalMetalLayout).  Offsets are bytes from the start of the slab.
  *   gate_w_offset, up_w_offset: uint32 [I][H/8] row-major packed nibbles,
  *       4-byte aligned; element k of row i is nibble k%8 (bits 4*(k%8)) of
  *       word i*(H/8) + k/8.
  *   gate_s_offset, up_s_offset: f32 [I] row scales, 4-byte aligned.
+ *   down_w_offset: uint32 [H][I/8] row-major packed nibbles (element k of
+ *       output row h is nibble k%8 of word h*(I/8) + k/8), 4-byte aligned;
+ *   down_s_offset: f32 [H] row scales, 4-byte aligned.  Both negative: the
+ *       slab has no down sections (the gate/up calls never read them; the
+ *       down calls then fail with Q4MOE_ERR_INVALID_ARG).
  * Each section must lie inside [0, slab_bytes) (page 51, validateRange).
  */
 typedef struct q4moe_layout {
     int64_t hidden_size;       /* H: > 0, multiple of 8 (page 52, validateCall) */
-    int64_t intermediate_size; /* I: > 0, multiple of 4                         */
+    int64_t intermediate_size; /* I: > 0, multiple of 4 (of 8 for the down
+                                  sections)                                     */
     int64_t slab_bytes;        /* bytes of one slab                             */
     int64_t gate_w_offset;
     int64_t up_w_offset;
     int64_t gate_s_offset;
     int64_t up_s_offset;
+    int64_t down_w_offset;
+    int64_t down_s_offset;
 } q4moe_layout_t;
 
 /*
@@ -187,8 +203,10 @@ const char *q4moe_last_error(void);
 
 /*
  * Fill *layout with the canonical slab layout for (H, I): gate words at 0,
- * up words at I*H/2, gate scales at I*H, up scales at I*H + 4*I, slab size
- * rounded up to Q4MOE_SLAB_ALIGNMENT.  Host only.
+ * up words at I*H/2, gate scales at I*H, up scales at I*H + 4*I; when
+ * I % 8 == 0 also down words at D = (I*H + 8*I) rounded up to 256 and down
+ * scales at D + H*I/2 (else no down sections); slab size rounded up to
+ * Q4MOE_SLAB_ALIGNMENT.  Host only.
  */
 int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout);
 
@@ -205,6 +223,14 @@ int q4moe_validate_layout(const q4moe_layout_t *layout);
 int q4moe_pack_slab(const q4moe_layout_t *layout, const uint32_t *gate_w,
                     const uint32_t *up_w, const float *gate_s,
                     const float *up_s, void *slab_host);
+
+/*
+ * Copy one expert's down sections into a host slab buffer already filled by
+ * q4moe_pack_slab (nothing else is touched).  down_w: host uint32 [H][I/8];
+ * down_s: host f32 [H].  Host only.
+ */
+int q4moe_pack_slab_down(const q4moe_layout_t *layout, const uint32_t *down_w,
+                         const float *down_s, void *slab_host);
 
 /*
  * Token -> expert grouping: a stable counting sort of the T*k routed
@@ -252,6 +278,48 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *expert_slabs,
                             const int32_t *token_to_expert_map, int64_t M,
                             int64_t H, int64_t I, void *out,
                             const q4moe_options_t *opts, cudaStream_t stream);
+
+/*
+ * The down projection over grouped rows (the second formula at the top;
+ * page 52, streamed-experts.ts, DOWN_SOURCE).
+ *   mid                     device bf16 [M][I], grouped-row order (the out of
+ *                           the gate/up call), 16-byte aligned.
+ *   expert_slabs            host pointer, read during the call only; its
+ *                           layout must hold the down sections.
+ *   row_offsets_per_expert  device int32 [E+1] as for the gate/up call.
+ *   M                       grouped rows (>= 0; 0 is a no-op).
+ *   H, I                    must equal the layout's; I % 8 == 0.
+ *   out                     device bf16 [M][H], grouped-row order.
+ *   opts                    may be NULL.  kernel and matvec_tile as for the
+ *                           gate/up call (the matvec's unit then covers
+ *                           twice matvec_tile output rows); gate_f32, if
+ *                           set, receives f32 [M][H]: the sum times the
+ *                           scale before rounding.  num_tokens, up_f32 and
+ *                           workspace must be 0 / NULL (the rows of mid are
+ *                           already grouped).
+ * Kernel choice per expert as for gate/up; the GEMM's tiles are 256 output
+ * rows.  Summation order: as for gate/up (exact inputs give exact bits).
+ */
+int q4moe_down_proj(const void *mid, const q4moe_slabs_t *expert_slabs,
+                    const int32_t *row_offsets_per_expert, int64_t M,
+                    int64_t H, int64_t I, void *out,
+                    const q4moe_options_t *opts, cudaStream_t stream);
+
+/*
+ * The whole routed expert MLP: q4moe_gate_up_swiglu_ex from x into mid,
+ * then q4moe_down_proj from mid into out, queued on `stream` (the page's
+ * executor, page 52, runs its gate/up kernel and then its down kernel on
+ * the same slot).  Arguments as for those two calls; mid is caller-owned
+ * device scratch bf16 [M][I], 16-byte aligned, not overlapping x or out,
+ * and holds the gate/up output afterwards.  opts apply to the gate/up stage
+ * as documented there (gate_f32/up_f32, num_tokens, workspace); kernel and
+ * matvec_tile to both stages.
+ */
+int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *expert_slabs,
+                     const int32_t *row_offsets_per_expert,
+                     const int32_t *token_to_expert_map, int64_t M, int64_t H,
+                     int64_t I, void *mid, void *out,
+                     const q4moe_options_t *opts, cudaStream_t stream);
 
 /*
  * Wait for `stream`, then read the current device's status word into

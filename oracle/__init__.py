@@ -57,6 +57,8 @@ def _load():
         lib.q4o_bf16_rne.argtypes = [ctypes.c_float]
         lib.q4o_bf16_to_f32.restype = ctypes.c_float
         lib.q4o_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.q4o_bf16_rne_array.restype = None
+        lib.q4o_bf16_rne_array.argtypes = [_I64, _P, _P]
         lib.q4o_tail.restype = None
         lib.q4o_tail.argtypes = [ctypes.c_float, ctypes.c_float, _INT, _P]
         lib.q4o_tail_array.restype = None
@@ -102,10 +104,10 @@ def bf16_rne(v: float) -> int:
 
 
 def bf16_rne_array(a) -> np.ndarray:
-    lib = _load()
-    flat = np.asarray(a, dtype=np.float32).ravel()
-    return np.array([lib.q4o_bf16_rne(float(v)) for v in flat],
-                    dtype=np.uint16).reshape(np.shape(a))
+    flat = _c(np.asarray(a, dtype=np.float32).ravel(), np.float32)
+    out = np.zeros(flat.shape[0], np.uint16)
+    _load().q4o_bf16_rne_array(flat.shape[0], _ptr(flat), _ptr(out))
+    return out.reshape(np.shape(a))
 
 
 def tail(gate32: float, up32: float, silu_mode: int = 0):

@@ -71,6 +71,13 @@ float q4o_bf16_to_f32(uint16_t b)
     return f;
 }
 
+/* q4o_bf16_rne over n values. */
+void q4o_bf16_rne_array(int64_t n, const float *v, uint16_t *out)
+{
+    for (int64_t j = 0; j < n; ++j)
+        out[j] = q4o_bf16_rne(v[j]);
+}
+
 /* ---- SwiGLU tail (page 52, streamed-experts.ts, GATE_UP_SOURCE tail) ---- */
 
 /* res[0..4] = gateT, upT, sigmoidT, siluT, out  (bf16 bit patterns).

@@ -19,6 +19,8 @@ class Problem:
     gate_s: np.ndarray    # f32 [E, I]
     up_s: np.ndarray
     topk: np.ndarray      # int32 [T, k]
+    down_w: np.ndarray = None   # uint32 [E, H, I/8] (optional)
+    down_s: np.ndarray = None   # f32 [E, H]
 
     @property
     def E(self):
@@ -98,7 +100,8 @@ def upload(p: Problem, layout=None, stride_pad=0, ptr_table=False,
     bf16 elements past a 256-byte boundary)."""
     import torch
     L = layout or q.q4moe_canonical_layout(p.H, p.I)
-    host = q.pack_slab_pool(L, p.gate_w, p.up_w, p.gate_s, p.up_s)
+    host = q.pack_slab_pool(L, p.gate_w, p.up_w, p.gate_s, p.up_s,
+                            p.down_w, p.down_s)
     stride = L.slab_bytes + stride_pad
     keep = []
     buf, pool = aligned_device_buffer(p.E * stride)
@@ -198,3 +201,109 @@ def element_scales(p: Problem, offs: np.ndarray):
     e_of_row = np.repeat(np.arange(p.E), np.diff(offs))
     assert e_of_row.shape[0] == M
     return p.gate_s[e_of_row], p.up_s[e_of_row]
+
+
+def with_down(p: Problem, seed, exact=False) -> Problem:
+    """p with down sections drawn from the seeded generator (power-of-two
+    scales when exact)."""
+    dw, ds = syn.down_weights(seed, p.E, p.H, p.I)
+    if exact:
+        _, dw, ds = syn.exact_down_case(seed, 1, p.I, p.E, p.H)
+    p.down_w, p.down_s = dw, ds
+    return p
+
+
+def down_only_problem(seed, counts, K, N, exact=False, mid_std=0.1):
+    """A down projection on its own: expert e gets counts[e] grouped rows of
+    mid (bf16 [M, K]); N output rows.  Returns (Problem, mid bits,
+    row_offsets).  The gate/up sections are filler (never read)."""
+    E, M = len(counts), int(sum(counts))
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    if exact:
+        mid, dw, ds = syn.exact_down_case(seed, max(M, 1), K, E, N)
+        mid = mid[:M]
+    else:
+        mid = syn.normal_x(seed, max(M, 1), K, std=mid_std,
+                           stream=syn.S_EXACT_MID)[:M]
+        dw, ds = syn.down_weights(seed, E, N, K)
+    gw = np.zeros((E, K, N // 8), np.uint32)
+    gs = np.zeros((E, K), np.float32)
+    p = Problem(np.zeros((1, N), np.uint16), gw, gw, gs, gs,
+                np.zeros((1, 1), np.int32), dw, ds)
+    return p, mid, offs
+
+
+def down(d: DeviceProblem, offs, mid, kernel=q.KERNEL_AUTO, debug=True,
+         matvec_tile=0, stream=None, mid_offset=0):
+    """Run q4moe_down_proj on mid (numpy bits [M, I] or a device tensor);
+    returns numpy out bits [M, H] (+ out32)."""
+    import torch
+    H, I = d.p.H, d.p.I
+    if isinstance(mid, np.ndarray):
+        M = mid.shape[0]
+        mh = torch.from_numpy(np.ascontiguousarray(mid).view(np.int16))
+        mbuf, md = aligned_device_buffer(max(mh.numel(), 1) * 2 +
+                                         2 * mid_offset, 256)
+        d.keep.append(mbuf)
+        md = md.view(torch.int16)[mid_offset:mid_offset + mh.numel()]
+        md.copy_(mh.reshape(-1))
+    else:
+        md = mid
+        M = mid.shape[0] if mid.dim() == 2 else mid.numel() // I
+    offs_d = offs if not isinstance(offs, np.ndarray) else \
+        torch.from_numpy(offs).cuda()
+    out = torch.full((max(M, 1), H), -1, dtype=torch.int16, device="cuda")
+    o = q.q4moe_options_t()
+    o.kernel = kernel
+    o.matvec_tile = matvec_tile
+    o32 = None
+    if debug:
+        o32 = torch.full((max(M, 1), H), float("nan"), device="cuda")
+        o.gate_f32 = o32.data_ptr()
+    q.q4moe_down_proj(md, d.slabs, offs_d, M, H, I, out, o, stream)
+    torch.cuda.synchronize()
+    res = {"out": out[:M].cpu().numpy().view(np.uint16)}
+    if debug:
+        res["out32"] = o32[:M].cpu().numpy()
+    return res
+
+
+def expert_mlp(d: DeviceProblem, offs, tok, kernel=q.KERNEL_AUTO,
+               debug=True, workspace=False, matvec_tile=0, stream=None):
+    """Run q4moe_expert_mlp; returns numpy mid bits [M, I], out bits [M, H]
+    (+ gate32/up32 of the gate/up stage)."""
+    import torch
+    M = int(tok.shape[0])
+    H, I = d.p.H, d.p.I
+    mid = torch.full((max(M, 1), I), -1, dtype=torch.int16, device="cuda")
+    out = torch.full((max(M, 1), H), -1, dtype=torch.int16, device="cuda")
+    o = q.q4moe_options_t()
+    o.num_tokens = d.p.T
+    o.kernel = kernel
+    o.matvec_tile = matvec_tile
+    g32 = u32 = None
+    if debug:
+        g32 = torch.full((max(M, 1), I), float("nan"), device="cuda")
+        u32 = torch.full((max(M, 1), I), float("nan"), device="cuda")
+        o.gate_f32, o.up_f32 = g32.data_ptr(), u32.data_ptr()
+    if workspace:
+        nbytes = q.q4moe_workspace_bytes(M, H)
+        wbuf, ws = aligned_device_buffer(max(nbytes, 256), 256)
+        ws.fill_(0xFF)
+        d.keep.append(wbuf)
+        o.workspace = ws.data_ptr()
+        o.workspace_bytes = nbytes
+    q.q4moe_expert_mlp(d.x, d.slabs, offs, tok, M, H, I, mid, out, o, stream)
+    torch.cuda.synchronize()
+    res = {"mid": mid[:M].cpu().numpy().view(np.uint16),
+           "out": out[:M].cpu().numpy().view(np.uint16)}
+    if debug:
+        res["gate32"] = g32[:M].cpu().numpy()
+        res["up32"] = u32[:M].cpu().numpy()
+    return res
+
+
+def down_scales(p: Problem, offs: np.ndarray):
+    """down scale of every output element [M, H] (grouped order)."""
+    e_of_row = np.repeat(np.arange(p.E), np.diff(offs))
+    return p.down_s[e_of_row]

@@ -36,9 +36,20 @@ def test_canonical_layout():
     assert (L.gate_w_offset, L.up_w_offset) == (0, 1536 * 2560)
     assert L.gate_s_offset == 1536 * 5120
     assert L.up_s_offset == 1536 * 5120 + 4 * 1536
-    assert L.slab_bytes == 7876608 == 1923 * 4096
-    assert q.q4moe_canonical_layout(512, 256).slab_bytes == 135168
-    assert q.q4moe_canonical_layout(4096, 1536).slab_bytes == 6303744
+    # down words after the up scales, rounded up to 256; down scales after
+    # the down words; the slab rounded up to 4096
+    assert L.down_w_offset == 7876608
+    assert L.down_s_offset == 7876608 + 5120 * 768
+    assert L.slab_bytes == 11829248 == 2888 * 4096
+    L2 = q.q4moe_canonical_layout(512, 256)
+    assert (L2.down_w_offset, L2.down_s_offset, L2.slab_bytes) == \
+        (133120, 198656, 200704)
+    assert q.q4moe_canonical_layout(4096, 1536).slab_bytes == 9465856
+    L3 = q.q4moe_canonical_layout(64, 12)       # I % 8 != 0: no down
+    assert (L3.down_w_offset, L3.down_s_offset) == (-1, -1)
+    assert L3.slab_bytes == 4096
+    L4 = q.q4moe_canonical_layout(64, 40)       # 8*I not a multiple of 256
+    assert L4.down_w_offset == (2 * 40 * 32 + 8 * 40 + 255) // 256 * 256
     for H, I in ((0, 4), (12, 4), (8, 6), (8, 0), (-8, 4)):
         with pytest.raises(q.Q4moeError) as ei:
             q.q4moe_canonical_layout(H, I)
@@ -65,6 +76,32 @@ def test_validate_layout_ranges_and_alignment():
     assert ei.value.code == q.ERR_ALIGNMENT
 
 
+def test_validate_layout_down_sections():
+    L = q.q4moe_canonical_layout(64, 8)
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.down_s_offset = -1                      # one of the two absent
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_INVALID_ARG
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.down_s_offset = L.slab_bytes - 4 * 64 + 4   # past the slab
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_RANGE
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.down_w_offset += 2
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_ALIGNMENT
+    no_down = q.q4moe_layout_t.from_buffer_copy(L)
+    no_down.down_w_offset = no_down.down_s_offset = -1
+    q.q4moe_validate_layout(no_down)
+    with pytest.raises(q.Q4moeError):
+        q.q4moe_pack_slab_down(no_down, np.zeros(64, np.uint32),
+                               np.zeros(64, np.float32),
+                               np.zeros(L.slab_bytes, np.uint8))
+
+
 def test_pack_slab_places_sections():
     H, I = 64, 8
     L = q.q4moe_canonical_layout(H, I)
@@ -84,6 +121,17 @@ def test_pack_slab_places_sections():
     assert np.array_equal(
         slab[2 * wb + 4 * I:2 * wb + 8 * I].view(np.float32), us)
     assert np.all(slab[2 * wb + 8 * I:] == 0)
+    dw = rng.integers(0, 2**32, size=(H, I // 8), dtype=np.uint64).astype(
+        np.uint32)
+    ds = rng.random(H).astype(np.float32)
+    q.q4moe_pack_slab_down(L, dw, ds, slab)
+    d0, s0 = L.down_w_offset, L.down_s_offset
+    assert np.array_equal(slab[d0:d0 + H * I // 2].view(np.uint32)
+                          .reshape(H, -1), dw)
+    assert np.array_equal(slab[s0:s0 + 4 * H].view(np.float32), ds)
+    assert np.array_equal(slab[:wb].view(np.uint32).reshape(I, -1), gw)
+    assert np.all(slab[2 * wb + 8 * I:d0] == 0)
+    assert np.all(slab[s0 + 4 * H:] == 0)
 
 
 FAKE = 1 << 40     # an aligned address that is never dereferenced on host
@@ -137,6 +185,47 @@ def test_host_argument_errors():
                                 FAKE, None) == q.ERR_INVALID_ARG
     assert lib.q4moe_debug_tail(None, None, 4, None, None) == \
         q.ERR_INVALID_ARG
+
+
+def test_down_and_mlp_host_argument_errors():
+    lib = q.load()
+    L = q.q4moe_canonical_layout(64, 8)
+    s = q.make_slabs(2, L, base=FAKE)
+
+    def down(mid=FAKE, slabs=s, offs=FAKE, M=4, H=64, I=8, out=FAKE,
+             opts=None):
+        return lib.q4moe_down_proj(mid, ctypes.byref(slabs), offs, M, H, I,
+                                   out, None if opts is None
+                                   else ctypes.byref(opts), None)
+
+    def mlp(x=FAKE, mid=FAKE + (1 << 20), out=FAKE + (2 << 20), slabs=s,
+            M=4):
+        return lib.q4moe_expert_mlp(x, ctypes.byref(slabs), FAKE, FAKE, M, 64,
+                                    8, mid, out, None, None)
+
+    assert down(mid=FAKE + 8) == q.ERR_ALIGNMENT      # mid not 16-aligned
+    assert down(out=FAKE + 1) == q.ERR_ALIGNMENT
+    assert down(offs=None) == q.ERR_INVALID_ARG
+    assert down(mid=None) == q.ERR_INVALID_ARG
+    assert down(I=16) == q.ERR_INVALID_ARG            # differs from layout
+    no_down = q.q4moe_layout_t.from_buffer_copy(L)
+    no_down.down_w_offset = no_down.down_s_offset = -1
+    nd = q.make_slabs(2, no_down, base=FAKE)
+    assert down(slabs=nd) == q.ERR_INVALID_ARG
+    assert "down sections" in q.q4moe_last_error()
+    for field, val in (("num_tokens", 4), ("up_f32", FAKE),
+                       ("workspace", FAKE)):
+        o = q.q4moe_options_t()
+        setattr(o, field, val)
+        assert down(opts=o) == q.ERR_INVALID_ARG, field
+    assert mlp(slabs=nd) == q.ERR_INVALID_ARG
+    assert mlp(mid=FAKE + 8) == q.ERR_ALIGNMENT
+    assert mlp(mid=FAKE + 64, out=FAKE) == q.ERR_INVALID_ARG   # overlap
+    assert "overlaps" in q.q4moe_last_error()
+    import torch
+    if not torch.cuda.is_available():
+        assert down() in (q.ERR_CUDA, q.ERR_DEVICE)
+        assert mlp() in (q.ERR_CUDA, q.ERR_DEVICE)
 
 
 def test_valid_call_without_gpu_reports_device_error():

@@ -1,6 +1,7 @@
 // q4moe_api.cu -- the C ABI: argument validation, the device status word and
 // kernel dispatch.  Validation rules follow the pages' host checks (page 52,
 // streamed-experts.ts, validateCall; page 51, layout.ts, validateRange).
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstdarg>
@@ -117,6 +118,12 @@ bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a),
+                    y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
 int check_range(int64_t off, int64_t len, int64_t slab_bytes,
                 const char *what) {
     if (off < 0)
@@ -158,6 +165,104 @@ int validate_layout(const q4moe_layout_t *L) {
          L->up_s_offset) % 4 != 0)
         return fail(Q4MOE_ERR_ALIGNMENT,
                     "slab sections must start on 4-byte boundaries");
+    // the down sections, when present (both offsets >= 0)
+    if ((L->down_w_offset < 0) != (L->down_s_offset < 0))
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "down weights and down scales must both be present or "
+                    "both absent (negative offsets)");
+    if (L->down_w_offset >= 0) {
+        if (I % 8 != 0)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "Q4 down sections need I divisible by 8");
+        if ((rc = check_range(L->down_w_offset, H * (I / 2), L->slab_bytes,
+                              "down weights")) ||
+            (rc = check_range(L->down_s_offset, H * 4, L->slab_bytes,
+                              "down scales")))
+            return rc;
+        if ((L->down_w_offset | L->down_s_offset) % 4 != 0)
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab sections must start on 4-byte boundaries");
+    }
+    return Q4MOE_OK;
+}
+
+// Checks of the slab placement and the call's dimensions shared by every
+// call that reads expert slabs.
+int check_slabs(const q4moe_slabs_t *slabs, int64_t H, int64_t I,
+                int64_t M) {
+    if (slabs == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "expert_slabs is null");
+    int rc = validate_layout(&slabs->layout);
+    if (rc)
+        return rc;
+    const q4moe_layout_t &L = slabs->layout;
+    if (H != L.hidden_size || I != L.intermediate_size)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "H, I (%lld, %lld) differ from the slab layout's "
+                    "(%lld, %lld)", (long long)H, (long long)I,
+                    (long long)L.hidden_size,
+                    (long long)L.intermediate_size);
+    if (slabs->num_experts <= 0 || slabs->num_experts > Q4MOE_MAX_EXPERTS)
+        return fail(Q4MOE_ERR_INVALID_ARG, "num_experts must be in 1..%d",
+                    Q4MOE_MAX_EXPERTS);
+    if (slabs->reserved0 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "reserved field must be 0");
+    if (M < 0 || M > INT32_MAX)
+        return fail(Q4MOE_ERR_INVALID_ARG, "M must be in 0..2^31-1");
+    if (M > 0 && M * std::max(H, I) > (INT64_C(1) << 40))
+        return fail(Q4MOE_ERR_INVALID_ARG, "output too large");
+    if (slabs->slab_ptrs == nullptr) {
+        if (slabs->base == nullptr)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "slab base is null and no pointer table given");
+        if (!aligned(slabs->base, Q4MOE_SLAB_ALIGNMENT))
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab base must be %d-byte aligned",
+                        Q4MOE_SLAB_ALIGNMENT);
+        if (slabs->slab_stride % Q4MOE_SLAB_ALIGNMENT != 0 ||
+            (slabs->num_experts > 1 && slabs->slab_stride < L.slab_bytes) ||
+            slabs->slab_stride < 0)
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab stride must be a multiple of %d and at least "
+                        "the slab size", Q4MOE_SLAB_ALIGNMENT);
+    } else if (!aligned(slabs->slab_ptrs, 8)) {
+        return fail(Q4MOE_ERR_ALIGNMENT, "slab pointer table misaligned");
+    }
+    return Q4MOE_OK;
+}
+
+int check_kernel_options(const q4moe_options_t &o) {
+    if ((o.matvec_tile != 0 && o.matvec_tile != 16 && o.matvec_tile != 32 &&
+         o.matvec_tile != 64 && o.matvec_tile != 128) ||
+        o.kernel < Q4MOE_KERNEL_AUTO ||
+        o.kernel > Q4MOE_KERNEL_GEMM || o.num_tokens < 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
+    if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
+        return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
+                                         "aligned");
+    return Q4MOE_OK;
+}
+
+// Checks of a down projection's own arguments (before anything launches).
+int check_down(const q4moe_slabs_t *slabs, const void *mid, const void *out,
+               const int32_t *row_offsets, int64_t M,
+               const q4moe_options_t &o, bool own_options) {
+    if (slabs->layout.down_w_offset < 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "the slab layout has no down sections");
+    if (row_offsets == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "row_offsets_per_expert is null");
+    if (M > 0 && (mid == nullptr || out == nullptr))
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(mid, 16))
+        return fail(Q4MOE_ERR_ALIGNMENT, "mid must be 16-byte aligned");
+    if (!aligned(out, 2))
+        return fail(Q4MOE_ERR_ALIGNMENT, "out must be 2-byte aligned");
+    if (own_options && (o.num_tokens != 0 || o.up_f32 != nullptr ||
+                        o.workspace != nullptr || o.workspace_bytes != 0))
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "the down projection takes no num_tokens, up_f32 or "
+                    "workspace");
     return Q4MOE_OK;
 }
 
@@ -171,6 +276,65 @@ int report_error(int code, const char *message) {
     return fail(code, "%s", message);
 }
 }  // namespace q4moe
+
+namespace {
+
+q4moe::GateUpArgs base_args(const q4moe_slabs_t *slabs, int64_t M,
+                            const DeviceInfo *d, const q4moe_options_t &o) {
+    q4moe::GateUpArgs a{};
+    a.base = static_cast<const uint8_t *>(slabs->base);
+    a.stride = slabs->slab_stride;
+    a.slab_ptrs = reinterpret_cast<const uint8_t *const *>(slabs->slab_ptrs);
+    a.M = M;
+    a.E = slabs->num_experts;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
+    a.matvec_tile = o.matvec_tile;
+    a.sigmoid = d->sigmoid;
+    return a;
+}
+
+// Kernel choice and launches of one projection (gate/up or down).
+int dispatch(q4moe::GateUpArgs &a, const q4moe_options_t &o,
+             const DeviceInfo *d, cudaStream_t stream) {
+    const bool gemm_ok = q4moe::gemm_supported(a.H, a.I, a);
+    int32_t matvec_max = INT32_MAX;
+    if (o.kernel == Q4MOE_KERNEL_GEMM) {
+        if (!gemm_ok)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        a.down ? "the tensor-core GEMM needs I %% 64 == 0, "
+                                 "H %% 128 == 0 and 16-byte aligned slab "
+                                 "sections"
+                               : "the tensor-core GEMM needs H %% 64 == 0, "
+                                 "I %% 128 == 0 and 16-byte aligned slab "
+                                 "sections");
+        matvec_max = 0;
+    } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
+        // experts above 48 rows go to the GEMM if they fill the GPU with
+        // tiles (decided on the device); a single expert's count is known
+        const int64_t tiles = (a.M + 255) / 256 * q4moe::gemm_row_tiles(a);
+        if (a.E > 1) {
+            matvec_max = 48;
+            a.gemm_min_tiles = d->num_sms;
+        } else if (a.M > 48 && tiles >= d->num_sms) {
+            matvec_max = 0;
+        }
+    }
+    a.matvec_max_rows = matvec_max;
+
+    cudaError_t err = cudaSuccess;
+    a.matvec_last = matvec_max >= a.M;       // no GEMM launch after it
+    if (matvec_max > 0 && (err = q4moe::launch_matvec(a, stream)) !=
+                              cudaSuccess)
+        return cuda_fail(err, "matvec launch");
+    // every expert has at most M rows: no GEMM work when M <= matvec_max
+    if (matvec_max < a.M && (err = q4moe::launch_gemm(a, stream)) !=
+                                cudaSuccess)
+        return cuda_fail(err, "gemm launch");
+    return ok();
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -202,7 +366,13 @@ int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout) {
     L.up_w_offset = wbytes;
     L.gate_s_offset = 2 * wbytes;
     L.up_s_offset = 2 * wbytes + 4 * I;
-    const int64_t used = 2 * wbytes + 8 * I;
+    int64_t used = 2 * wbytes + 8 * I;
+    L.down_w_offset = L.down_s_offset = -1;
+    if (I % 8 == 0) {
+        L.down_w_offset = (used + 255) / 256 * 256;
+        L.down_s_offset = L.down_w_offset + H * (I / 2);
+        used = L.down_s_offset + 4 * H;
+    }
     L.slab_bytes = (used + Q4MOE_SLAB_ALIGNMENT - 1) /
                    Q4MOE_SLAB_ALIGNMENT * Q4MOE_SLAB_ALIGNMENT;
     *layout = L;
@@ -229,6 +399,22 @@ int q4moe_pack_slab(const q4moe_layout_t *L, const uint32_t *gate_w,
     memcpy(s + L->up_w_offset, up_w, (size_t)(I * (H / 2)));
     memcpy(s + L->gate_s_offset, gate_s, (size_t)(I * 4));
     memcpy(s + L->up_s_offset, up_s, (size_t)(I * 4));
+    return ok();
+}
+
+int q4moe_pack_slab_down(const q4moe_layout_t *L, const uint32_t *down_w,
+                         const float *down_s, void *slab_host) {
+    int rc = validate_layout(L);
+    if (rc)
+        return rc;
+    if (L->down_w_offset < 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "the layout has no down sections");
+    if (!down_w || !down_s || !slab_host)
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    const int64_t H = L->hidden_size, I = L->intermediate_size;
+    uint8_t *s = static_cast<uint8_t *>(slab_host);
+    memcpy(s + L->down_w_offset, down_w, (size_t)(H * (I / 2)));
+    memcpy(s + L->down_s_offset, down_s, (size_t)(H * 4));
     return ok();
 }
 
@@ -261,27 +447,9 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
                             const int32_t *token_of_row, int64_t M, int64_t H,
                             int64_t I, void *out, const q4moe_options_t *opts,
                             cudaStream_t stream) {
-    if (slabs == nullptr)
-        return fail(Q4MOE_ERR_INVALID_ARG, "expert_slabs is null");
-    int rc = validate_layout(&slabs->layout);
+    int rc = check_slabs(slabs, H, I, M);
     if (rc)
         return rc;
-    const q4moe_layout_t &L = slabs->layout;
-    if (H != L.hidden_size || I != L.intermediate_size)
-        return fail(Q4MOE_ERR_INVALID_ARG,
-                    "H, I (%lld, %lld) differ from the slab layout's "
-                    "(%lld, %lld)", (long long)H, (long long)I,
-                    (long long)L.hidden_size,
-                    (long long)L.intermediate_size);
-    if (slabs->num_experts <= 0 || slabs->num_experts > Q4MOE_MAX_EXPERTS)
-        return fail(Q4MOE_ERR_INVALID_ARG, "num_experts must be in 1..%d",
-                    Q4MOE_MAX_EXPERTS);
-    if (slabs->reserved0 != 0)
-        return fail(Q4MOE_ERR_INVALID_ARG, "reserved field must be 0");
-    if (M < 0 || M > INT32_MAX)
-        return fail(Q4MOE_ERR_INVALID_ARG, "M must be in 0..2^31-1");
-    if (M > 0 && M * I > (INT64_C(1) << 40))
-        return fail(Q4MOE_ERR_INVALID_ARG, "output too large");
     if (row_offsets == nullptr)
         return fail(Q4MOE_ERR_INVALID_ARG, "row_offsets_per_expert is null");
     if (M > 0 && (x == nullptr || token_of_row == nullptr || out == nullptr))
@@ -290,34 +458,11 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
         return fail(Q4MOE_ERR_ALIGNMENT, "x must be 16-byte aligned");
     if (!aligned(out, 2))
         return fail(Q4MOE_ERR_ALIGNMENT, "out must be 2-byte aligned");
-    if (slabs->slab_ptrs == nullptr) {
-        if (slabs->base == nullptr)
-            return fail(Q4MOE_ERR_INVALID_ARG,
-                        "slab base is null and no pointer table given");
-        if (!aligned(slabs->base, Q4MOE_SLAB_ALIGNMENT))
-            return fail(Q4MOE_ERR_ALIGNMENT,
-                        "slab base must be %d-byte aligned",
-                        Q4MOE_SLAB_ALIGNMENT);
-        if (slabs->slab_stride % Q4MOE_SLAB_ALIGNMENT != 0 ||
-            (slabs->num_experts > 1 && slabs->slab_stride < L.slab_bytes) ||
-            slabs->slab_stride < 0)
-            return fail(Q4MOE_ERR_ALIGNMENT,
-                        "slab stride must be a multiple of %d and at least "
-                        "the slab size", Q4MOE_SLAB_ALIGNMENT);
-    } else if (!aligned(slabs->slab_ptrs, 8)) {
-        return fail(Q4MOE_ERR_ALIGNMENT, "slab pointer table misaligned");
-    }
     q4moe_options_t o{};
     if (opts != nullptr)
         o = *opts;
-    if ((o.matvec_tile != 0 && o.matvec_tile != 16 && o.matvec_tile != 32 &&
-         o.matvec_tile != 64 && o.matvec_tile != 128) ||
-        o.kernel < Q4MOE_KERNEL_AUTO ||
-        o.kernel > Q4MOE_KERNEL_GEMM || o.num_tokens < 0)
-        return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
-    if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
-        return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
-                                         "aligned");
+    if ((rc = check_kernel_options(o)))
+        return rc;
     if (o.workspace != nullptr) {
         if (!aligned(o.workspace, 256))
             return fail(Q4MOE_ERR_ALIGNMENT,
@@ -336,62 +481,83 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     if (M == 0)
         return ok();
 
-    q4moe::GateUpArgs a{};
+    q4moe::GateUpArgs a = base_args(slabs, M, d, o);
+    const q4moe_layout_t &L = slabs->layout;
     a.x = static_cast<const uint16_t *>(x);
-    a.base = static_cast<const uint8_t *>(slabs->base);
-    a.stride = slabs->slab_stride;
-    a.slab_ptrs = reinterpret_cast<const uint8_t *const *>(slabs->slab_ptrs);
     a.gate_w_off = L.gate_w_offset;
     a.up_w_off = L.up_w_offset;
     a.gate_s_off = L.gate_s_offset;
     a.up_s_off = L.up_s_offset;
     a.row_offsets = row_offsets;
     a.token_of_row = token_of_row;
-    a.M = M;
     a.H = H;
     a.I = I;
     a.T = o.num_tokens;
-    a.E = slabs->num_experts;
     a.out = static_cast<uint16_t *>(out);
     a.gate_f32 = o.gate_f32;
     a.up_f32 = o.up_f32;
     a.xg = static_cast<uint16_t *>(o.workspace);
-    a.status = d->status;
-    a.num_sms = d->num_sms;
-    a.matvec_tile = o.matvec_tile;
-    a.sigmoid = d->sigmoid;
+    return dispatch(a, o, d, stream);
+}
 
-    const bool gemm_ok = q4moe::gemm_supported(H, I, a);
-    int32_t matvec_max = INT32_MAX;
-    if (o.kernel == Q4MOE_KERNEL_GEMM) {
-        if (!gemm_ok)
-            return fail(Q4MOE_ERR_INVALID_ARG,
-                        "the tensor-core GEMM needs H %% 64 == 0, I %% 128 "
-                        "== 0 and 16-byte aligned slab sections");
-        matvec_max = 0;
-    } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
-        // experts above 48 rows go to the GEMM if they fill the GPU with
-        // tiles (decided on the device); a single expert's count is known
-        const int64_t tiles = (M + 255) / 256 * (I / 128);
-        if (slabs->num_experts > 1) {
-            matvec_max = 48;
-            a.gemm_min_tiles = d->num_sms;
-        } else if (M > 48 && tiles >= d->num_sms) {
-            matvec_max = 0;
-        }
-    }
-    a.matvec_max_rows = matvec_max;
+int q4moe_down_proj(const void *mid, const q4moe_slabs_t *slabs,
+                    const int32_t *row_offsets, int64_t M, int64_t H,
+                    int64_t I, void *out, const q4moe_options_t *opts,
+                    cudaStream_t stream) {
+    int rc = check_slabs(slabs, H, I, M);
+    if (rc)
+        return rc;
+    q4moe_options_t o{};
+    if (opts != nullptr)
+        o = *opts;
+    if ((rc = check_kernel_options(o)) ||
+        (rc = check_down(slabs, mid, out, row_offsets, M, o, true)))
+        return rc;
+    DeviceInfo *d = nullptr;
+    rc = device_info(&d);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return ok();
+    q4moe::GateUpArgs a = base_args(slabs, M, d, o);
+    const q4moe_layout_t &L = slabs->layout;
+    a.down = 1;
+    a.x = static_cast<const uint16_t *>(mid);
+    a.gate_w_off = a.up_w_off = L.down_w_offset;
+    a.gate_s_off = a.up_s_off = L.down_s_offset;
+    a.row_offsets = row_offsets;
+    a.token_of_row = nullptr;
+    a.H = I;                                 // the projection's K
+    a.I = H;                                 // its output rows
+    a.out = static_cast<uint16_t *>(out);
+    a.gate_f32 = o.gate_f32;
+    return dispatch(a, o, d, stream);
+}
 
-    cudaError_t err = cudaSuccess;
-    a.matvec_last = matvec_max >= M;         // no GEMM launch after it
-    if (matvec_max > 0 && (err = q4moe::launch_matvec(a, stream)) !=
-                              cudaSuccess)
-        return cuda_fail(err, "matvec launch");
-    // every expert has at most M rows: no GEMM work when M <= matvec_max
-    if (matvec_max < M && (err = q4moe::launch_gemm(a, stream)) !=
-                              cudaSuccess)
-        return cuda_fail(err, "gemm launch");
-    return ok();
+int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *slabs,
+                     const int32_t *row_offsets, const int32_t *token_of_row,
+                     int64_t M, int64_t H, int64_t I, void *mid, void *out,
+                     const q4moe_options_t *opts, cudaStream_t stream) {
+    // every check of both stages before the first launch
+    int rc = check_slabs(slabs, H, I, M);
+    if (rc)
+        return rc;
+    q4moe_options_t o{};
+    if (opts != nullptr)
+        o = *opts;
+    if ((rc = check_down(slabs, mid, out, row_offsets, M, o, false)))
+        return rc;
+    if (overlap(mid, M * I * 2, out, M * H * 2) ||
+        overlap(mid, M * I * 2, x, M > 0 ? 1 : 0))
+        return fail(Q4MOE_ERR_INVALID_ARG, "mid overlaps x or out");
+    if ((rc = q4moe_gate_up_swiglu_ex(x, slabs, row_offsets, token_of_row, M,
+                                      H, I, mid, &o, stream)))
+        return rc;
+    q4moe_options_t od{};
+    od.kernel = o.kernel;
+    od.matvec_tile = o.matvec_tile;
+    return q4moe_down_proj(mid, slabs, row_offsets, M, H, I, out, &od,
+                           stream);
 }
 
 int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *slabs,

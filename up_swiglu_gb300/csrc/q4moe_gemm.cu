@@ -29,6 +29,13 @@
 //   13-15 token rows: one thread issuing TMA boxes (workspace), or all
 //         three warps gathering with cp.async, each thread's copies
 //         counting as its arrival on the stage barrier when they land
+// The down projection (page 52, DOWN_SOURCE) runs on the same kernel
+// (kDown): a tile is 256 output rows of the one matrix, rows 0-127 in the
+// "gate" accumulator and 128-255 in the "up" one (a half past the last row
+// is dequantised as zeros and never stored); the token operand is mid
+// itself, already in grouped order, read through TMA without a copy; the
+// epilogue applies the row scale and rounds to bf16.
+//
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // Q4MOE_DEV_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -221,9 +228,10 @@ gather_rows_kernel(GateUpArgs a) {
     }
 }
 
-template <bool kTma>
+template <bool kTma, bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
+    static_assert(kTma || !kDown, "the down projection reads mid by TMA");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -234,8 +242,11 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E;
-    const int IB = (int)(a.I / BM);
+    const int IB = gemm_row_tiles(a);        // tiles over the output rows
     const int KB = (int)(a.H / BK);
+    // first row of a tile's second half (down: 128 rows further)
+    const int64_t hi_row = kDown ? BM : 0;
+    const int64_t tile_rows = kDown ? 2 * BM : BM;
 
     if (tid == 0) {
         for (int s = 0; s < A_STAGES; ++s) {
@@ -405,26 +416,26 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
         for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
             const Tile ti = tile_of(t, s_off, s_pre, E, IB);
             const uint8_t *slab = expert_slab(a, ti.e);
-            const int64_t row = (int64_t)ti.iblk * BM + r;
+            const int64_t row = (int64_t)ti.iblk * tile_rows + r;
+            // the second half's row exists (always, for gate/up)
+            const bool uok = slab && (!kDown || row + hi_row < a.I);
             const uint4 *gp = slab ? reinterpret_cast<const uint4 *>(
                                          slab + a.gate_w_off + row * (a.H / 2))
                                    : nullptr;
-            const uint4 *up = slab ? reinterpret_cast<const uint4 *>(
-                                         slab + a.up_w_off + row * (a.H / 2))
-                                   : nullptr;
+            const uint4 *up = uok ? reinterpret_cast<const uint4 *>(
+                                        slab + a.up_w_off +
+                                        (row + hi_row) * (a.H / 2))
+                                  : nullptr;
             uint4 ring[kPrefetch][4];
+            const uint4 kZero = make_uint4(0x88888888u, 0x88888888u,
+                                           0x88888888u, 0x88888888u);
 #pragma unroll
             for (int d = 0; d < kPrefetch; ++d) {
-                if (d < KB && slab) {
-                    ring[d][0] = __ldg(gp + 2 * d);
-                    ring[d][1] = __ldg(gp + 2 * d + 1);
-                    ring[d][2] = __ldg(up + 2 * d);
-                    ring[d][3] = __ldg(up + 2 * d + 1);
-                } else {
-                    ring[d][0] = ring[d][1] = ring[d][2] = ring[d][3] =
-                        make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
-                                   0x88888888u);
-                }
+                const bool in = d < KB;
+                ring[d][0] = (in && slab) ? __ldg(gp + 2 * d) : kZero;
+                ring[d][1] = (in && slab) ? __ldg(gp + 2 * d + 1) : kZero;
+                ring[d][2] = (in && uok) ? __ldg(up + 2 * d) : kZero;
+                ring[d][3] = (in && uok) ? __ldg(up + 2 * d + 1) : kZero;
             }
             bool ok = true;
             for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
@@ -459,8 +470,10 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                     if (kn < KB && slab) {
                         ring[d][0] = __ldg(gp + 2 * kn);
                         ring[d][1] = __ldg(gp + 2 * kn + 1);
-                        ring[d][2] = __ldg(up + 2 * kn);
-                        ring[d][3] = __ldg(up + 2 * kn + 1);
+                        if (uok) {
+                            ring[d][2] = __ldg(up + 2 * kn);
+                            ring[d][3] = __ldg(up + 2 * kn + 1);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -540,11 +553,14 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                 break;
             tc_fence_after();
             const uint8_t *slab = expert_slab(a, ti.e);
-            const int64_t i = (int64_t)ti.iblk * BM + quad * 32 + lane;
+            const int64_t i = (int64_t)ti.iblk * tile_rows + quad * 32 + lane;
+            const bool hi_ok = !kDown || i + hi_row < a.I;
             float sg = 0.0f, su = 0.0f;
             if (slab) {
                 sg = reinterpret_cast<const float *>(slab + a.gate_s_off)[i];
-                su = reinterpret_cast<const float *>(slab + a.up_s_off)[i];
+                if (hi_ok)
+                    su = reinterpret_cast<const float *>(
+                        slab + a.up_s_off)[i + hi_row];
             }
             const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
             for (int c0 = half * 16; c0 < ti.n; c0 += 32) {
@@ -554,6 +570,27 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                 tmem_ld_wait();
                 if (!slab)
                     continue;
+                if (kDown) {
+                    // out = bf16(sum * scale) for both halves
+                    const int64_t o0 = (int64_t)(ti.row0 + c0) * a.I + i;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float lo = __fmul_rn(__uint_as_float(gv[jj]), sg);
+                        const float hi = __fmul_rn(__uint_as_float(uv[jj]), su);
+                        if (c0 + jj < ti.nvalid) {
+                            const int64_t oi = o0 + (int64_t)jj * a.I;
+                            a.out[oi] = bf16_bits(lo);
+                            if (a.gate_f32)
+                                a.gate_f32[oi] = lo;
+                            if (hi_ok) {
+                                a.out[oi + hi_row] = bf16_bits(hi);
+                                if (a.gate_f32)
+                                    a.gate_f32[oi + hi_row] = hi;
+                            }
+                        }
+                    }
+                    continue;
+                }
                 // all 16 columns branch-free (independent chains the
                 // scheduler can interleave); sigmoids from the table
                 float gT[16], uT[16], sT[16];
@@ -629,7 +666,8 @@ namespace {
 // Tensor maps of the grouped activations bf16 [M][H]: boxes of 64 columns
 // (128 bytes, the swizzle span) x 256 >> level rows, 128-byte swizzle, rows
 // past M read as zero.
-cudaError_t encode_xg_maps(const GateUpArgs &a, XgMaps *maps) {
+cudaError_t encode_xg_maps(const GateUpArgs &a, const uint16_t *rows,
+                           XgMaps *maps) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
         return cudaErrorNotSupported;
@@ -639,7 +677,8 @@ cudaError_t encode_xg_maps(const GateUpArgs &a, XgMaps *maps) {
     for (int lvl = 0; lvl < kBoxLevels; ++lvl) {
         const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)(256 >> lvl)};
         const CUresult r = enc(&maps->m[lvl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                               2, a.xg, dims, strides, box, estr,
+                               2, const_cast<uint16_t *>(rows), dims,
+                               strides, box, estr,
                                CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -650,17 +689,18 @@ cudaError_t encode_xg_maps(const GateUpArgs &a, XgMaps *maps) {
     return cudaSuccess;
 }
 
-template <bool kTma>
+template <bool kTma, bool kDown>
 cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
                                cudaStream_t s) {
     const size_t smem = smem_bytes(a.E);
     cudaError_t err = cudaFuncSetAttribute(
-        gemm_tcgen05_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)smem);
+        gemm_tcgen05_kernel<kTma, kDown>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
-    return launch_pdl(gemm_tcgen05_kernel<kTma>, dim3((unsigned)a.num_sms),
-                      dim3(kThreads), smem, s, a, maps);
+    return launch_pdl(gemm_tcgen05_kernel<kTma, kDown>,
+                      dim3((unsigned)a.num_sms), dim3(kThreads), smem, s, a,
+                      maps);
 }
 
 }  // namespace
@@ -668,9 +708,15 @@ cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
     XgMaps maps;
     memset(&maps, 0, sizeof maps);
+    if (a.down) {                    // mid is grouped already: no copy
+        cudaError_t err = encode_xg_maps(a, a.x, &maps);
+        if (err != cudaSuccess)
+            return err;
+        return launch_gemm_kernel<true, true>(a, maps, s);
+    }
     if (a.xg == nullptr)
-        return launch_gemm_kernel<false>(a, maps, s);
-    cudaError_t err = encode_xg_maps(a, &maps);
+        return launch_gemm_kernel<false, false>(a, maps, s);
+    cudaError_t err = encode_xg_maps(a, a.xg, &maps);
     if (err != cudaSuccess)
         return err;
     const int blocks = (int)std::min<int64_t>(
@@ -681,7 +727,7 @@ cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
                           sizeof(int32_t) * (size_t)(a.E + 1), s, a)) !=
         cudaSuccess)
         return err;
-    return launch_gemm_kernel<true>(a, maps, s);
+    return launch_gemm_kernel<true, false>(a, maps, s);
 }
 
 }  // namespace q4moe

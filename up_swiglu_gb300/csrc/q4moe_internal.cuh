@@ -13,6 +13,12 @@
 namespace q4moe {
 
 // Everything a gate/up kernel needs, resolved and validated on the host.
+// The down projection (down = 1) runs on the same kernels with the roles
+// renamed: x is mid (bf16 [M][H], H = the projection's K, the MLP's
+// intermediate size), row p reads x row p (token_of_row unused), I is its
+// output rows (the MLP's hidden size), the gate and up sections both name
+// the down words and scales, and the two halves of a tile are two blocks
+// of output rows of the one matrix: out = bf16(sum * scale), no tail.
 struct GateUpArgs {
     const uint16_t *x;           // bf16 [T][H]
     const uint8_t *base;         // slab of expert e at base + e * stride ...
@@ -36,6 +42,7 @@ struct GateUpArgs {
     int32_t gemm_min_tiles;      // > 0: the automatic choice (matvec_limit)
     const uint16_t *sigmoid;     // sigmoid table: [65536] bf16, indexed by
                                  // the bf16 bits of gateT
+    int32_t down;                // 1: the down projection (above)
 };
 
 // Host-side count of kernel launches (q4moe_launch_count).
@@ -84,6 +91,12 @@ cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
 bool matvec_tma_supported(const GateUpArgs &a);
 cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
+// GEMM tiles over the output rows of one expert's 256 grouped rows: 128
+// intermediate rows (gate and up) per tile, or 256 output rows (two halves
+// of 128) for the down projection.
+__host__ __device__ __forceinline__ int gemm_row_tiles(const GateUpArgs &a) {
+    return a.down ? (int)((a.I + 255) / 256) : (int)(a.I / 128);
+}
 bool gemm_supported(int64_t H, int64_t I, const GateUpArgs &a);
 cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                               int32_t E, int32_t *row_offsets,
@@ -273,8 +286,8 @@ __device__ __forceinline__ bool stage_row_offsets(const GateUpArgs &a,
 
 // Experts with more rows than this go to the GEMM.  Under the automatic
 // choice (a.gemm_min_tiles > 0) the experts above a.matvec_max_rows go to
-// the GEMM only when they make at least a.gemm_min_tiles GEMM tiles (128
-// intermediate rows x up to 256 grouped rows): fewer would leave most SMs
+// the GEMM only when they make at least a.gemm_min_tiles GEMM tiles
+// (gemm_row_tiles x up to 256 grouped rows): fewer would leave most SMs
 // idle while the GEMM runs, and the matvec takes every expert instead.
 // Every kernel of the call evaluates the same rule on the staged offsets;
 // all threads of the block must call it.
@@ -290,7 +303,7 @@ __device__ __forceinline__ int32_t matvec_limit(const GateUpArgs &a,
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         const int n = s_off[e + 1] - s_off[e];
         if (n > a.matvec_max_rows)
-            t += (n + 255) / 256 * (int)(a.I / 128);
+            t += (n + 255) / 256 * gemm_row_tiles(a);
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)

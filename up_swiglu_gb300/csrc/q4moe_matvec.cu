@@ -15,6 +15,11 @@
 // the pages' trellis GATEUP_SHARED_M_SOURCE, page 57, gate-up.ts); lanes
 // stride over the row's words as the page's GATE_UP_SOURCE does (page 52),
 // accumulate gate and up in f32, and meet in a shuffle reduction.
+//
+// The down projection (page 52, DOWN_SOURCE) uses the TMA version when it
+// can (its K, the MLP's intermediate size, % 256 == 0, output rows % 16 ==
+// 0, slabs at base + e * stride), else the generic down kernel below (any
+// K % 8 == 0): one warp per output row, one matrix, no tail.
 #include "q4moe_internal.cuh"
 
 namespace q4moe {
@@ -112,6 +117,74 @@ matvec_generic_kernel(GateUpArgs a) {
     }
 }
 
+// Down projection, generic: warp per output row h (a.I of them) of one
+// expert, lanes over the row's K/8 words, up to 8 grouped rows of mid at a
+// time; out = bf16(sum * scale).
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+down_generic_kernel(GateUpArgs a) {
+    __shared__ int32_t s_off[Q4MOE_MAX_EXPERTS + 1];
+    grid_dependency_wait();
+    if (!stage_row_offsets(a, s_off))
+        return;
+    const int32_t mvmax = matvec_limit(a, s_off);
+    const int e = blockIdx.y;
+    const int32_t r0 = s_off[e], r1 = s_off[e + 1];
+    const int32_t rows = r1 - r0;
+    if (rows == 0 || rows > mvmax)
+        return;
+    const uint8_t *slab = expert_slab(a, e);
+    if (slab == nullptr)
+        return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t words = a.H / 8;
+    const float *ds = reinterpret_cast<const float *>(slab + a.gate_s_off);
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int64_t h = (int64_t)blockIdx.x * kRowsPerBlock +
+                          warp * kRowsPerWarp + rr;
+        if (h >= a.I)
+            break;
+        const uint32_t *dw = reinterpret_cast<const uint32_t *>(
+                                 slab + a.gate_w_off) + h * words;
+        for (int32_t p0 = r0; p0 < r1; p0 += kChunk) {
+            const int nt = min(kChunk, r1 - p0);
+            float acc[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j)
+                acc[j] = 0.0f;
+            for (int64_t w = lane; w < words; w += 32) {
+                const uint32_t q = dw[w];
+#pragma unroll
+                for (int j = 0; j < kChunk; ++j) {
+                    if (j >= nt)
+                        continue;
+                    const uint4 mv = *reinterpret_cast<const uint4 *>(
+                        a.x + (int64_t)(p0 + j) * a.H + w * 8);
+                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                    for (int place = 0; place < 8; ++place) {
+                        const float mf = bf16_f32(
+                            (mw[place >> 1] >> (16 * (place & 1))) & 0xFFFFu);
+                        const float wq =
+                            (float)((int)((q >> (4 * place)) & 0xFu) - 8);
+                        acc[j] = __fmaf_rn(wq, mf, acc[j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const float D = warp_sum(acc[j]);
+                if (lane == j && j < nt) {
+                    const float v = __fmul_rn(D, ds[h]);
+                    const int64_t o = (int64_t)(p0 + j) * a.I + h;
+                    a.out[o] = bf16_rne(v);
+                    if (a.gate_f32)
+                        a.gate_f32[o] = v;
+                }
+            }
+        }
+    }
+}
+
 __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
                                   int64_t n, uint16_t *res,
                                   const uint16_t *table) {
@@ -133,10 +206,13 @@ __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
     if (matvec_tma_supported(a))
         return launch_matvec_tma(a, s);
-    if (matvec_mma_supported(a))
-        return launch_matvec_mma(a, s);
     const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),
                     (unsigned)a.E);
+    if (a.down)
+        return launch_pdl(down_generic_kernel, grid,
+                          dim3(kWarpsPerBlock * 32), 0, s, a);
+    if (matvec_mma_supported(a))
+        return launch_matvec_mma(a, s);
     return launch_pdl(matvec_generic_kernel, grid, dim3(kWarpsPerBlock * 32),
                       0, s, a);
 }

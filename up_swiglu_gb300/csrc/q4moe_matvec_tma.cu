@@ -34,6 +34,12 @@
 // bits do not depend on the other rows of its chunk); K part 0 applies the
 // scales and the tail.
 //
+// The down projection (page 52, DOWN_SOURCE) runs on the same kernel
+// (kDown): one matrix, a tile of 32*NB output rows whose two halves take the
+// places of gate and up (the second box starts 16*NB rows further down the
+// same tensor map), x = the grouped intermediate rows themselves, and the
+// tail is the row scale and one bf16 rounding per output.
+//
 // Every mbarrier wait is bounded; on time-out the CTA raises
 // Q4MOE_DEV_WAIT_TIMEOUT, waits for its copies in flight and exits.
 #include <cuda.h>
@@ -258,7 +264,7 @@ __host__ __device__ __forceinline__ size_t red_bytes(int NB) {
     return (size_t)(kWarps - NB) * 32 * 2 * 16;
 }
 
-template <int NB>
+template <int NB, bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
 matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                   const __grid_constant__ CUtensorMap tm_up, int tok_cap,
@@ -267,6 +273,9 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
     constexpr int kBoxes = P / 2;            // boxes per matrix per stage
     constexpr int kRows = NB * 16;           // rows per box
     constexpr uint32_t kBoxBytes = kRows * 128;
+    // output rows per tile, and the first row of the second ("up") half
+    constexpr int kTileRows = kDown ? 2 * kRows : kRows;
+    constexpr int kHiRow = kDown ? kRows : 0;
     static_assert(2 * kBoxes * kBoxBytes == kStageBytes, "stage size");
 
     extern __shared__ uint8_t smem_raw[];
@@ -287,8 +296,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const int IBk = (int)(a.I / 16);
-    const int NT = ceil_div(IBk, NB);        // tiles per chunk
+    const int NT = ceil_div((int)a.I, kTileRows);  // tiles per chunk
     const int nst = ceil_div(H, P * kStepK); // stages per unit
 
     if (warp == kWarps && lane == 0) {
@@ -354,6 +362,10 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     e = t.e;
                     tile = t.tile;
                 }
+                const int row0 = tile * kTileRows;
+                // the down projection's second half may lie past the last
+                // row: not loaded (its stale slot is never stored)
+                const bool hi = !kDown || row0 + kHiRow < (int)a.I;
                 for (int st = 0; st < nst; ++st, ++j) {
                     const int slot = j % D;
                     if (j >= D && !wait_full(&empty[slot], (j / D - 1) & 1,
@@ -363,14 +375,17 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     }
                     const int k0 = st * P * kStepK;
                     const int nbox = min(kBoxes, ceil_div(H - k0, kBoxK));
-                    mbar_arrive_expect_tx(&full[slot], 2u * nbox * kBoxBytes);
+                    mbar_arrive_expect_tx(&full[slot],
+                                          (hi ? 2u : 1u) * nbox * kBoxBytes);
                     const uint32_t dst = smem_u32(ring) + slot * kStageBytes;
                     for (int bx = 0; bx < nbox; ++bx) {
                         const int c0 = (k0 + bx * kBoxK) / 8;
-                        tma_load_3d(dst + bx * kBoxBytes, &tm_gate, c0,
-                                    tile * kRows, e, &full[slot]);
-                        tma_load_3d(dst + (kBoxes + bx) * kBoxBytes, &tm_up,
-                                    c0, tile * kRows, e, &full[slot]);
+                        tma_load_3d(dst + bx * kBoxBytes, &tm_gate, c0, row0,
+                                    e, &full[slot]);
+                        if (hi)
+                            tma_load_3d(dst + (kBoxes + bx) * kBoxBytes,
+                                        &tm_up, c0, row0 + kHiRow, e,
+                                        &full[slot]);
                     }
                 }
             }
@@ -394,17 +409,20 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
         bool ok = true;
         for (int u = u0; u < u1 && ok; ++u) {
             const Unit t = unit_of(u, s_off, s_pre, E, NT);
-            const int blk = t.tile * NB + b;
-            const bool live = blk < IBk;
+            const int rbase = t.tile * kTileRows + b * 16;  // block's 1st row
+            const bool live = rbase < (int)a.I;
+            const bool live_hi = kDown ? rbase + kHiRow < (int)a.I : live;
             const uint8_t *slab = a.base + (int64_t)t.e * a.stride;
             const float *gs_row = reinterpret_cast<const float *>(
-                                      slab + a.gate_s_off) + blk * 16 + g;
+                                      slab + a.gate_s_off) + rbase + g;
             const float *us_row = reinterpret_cast<const float *>(
-                                      slab + a.up_s_off) + blk * 16 + g;
+                                      slab + a.up_s_off) + rbase + kHiRow + g;
             float sg[2] = {0.f, 0.f}, su[2] = {0.f, 0.f};
             if (kp == 0 && live) {               // in flight during the K loop
                 sg[0] = gs_row[0];
                 sg[1] = gs_row[8];
+            }
+            if (kp == 0 && live_hi) {
                 su[0] = us_row[0];
                 su[1] = us_row[8];
             }
@@ -416,7 +434,8 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                 int emax = 0, emin = 255, sub = 0;
                 for (int idx = tid; idx < t.nt * qn; idx += kCThreads) {
                     const int n = idx / qn, q = idx - n * qn;
-                    const int64_t tok = row_token(a, t.p0 + n);
+                    const int64_t tok =
+                        kDown ? (int64_t)(t.p0 + n) : row_token(a, t.p0 + n);
                     uint4 v = make_uint4(0, 0, 0, 0);
                     if (tok >= 0)
                         v = __ldg(reinterpret_cast<const uint4 *>(a.x + tok * a.H) +
@@ -538,7 +557,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
             if (kp == 0 && live) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int64_t row = (int64_t)blk * 16 + 8 * i + g;
+                    const int64_t row = (int64_t)rbase + 8 * i + g;
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const int n = 2 * tq + jj;
@@ -549,11 +568,22 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                             const float u32 = __fmul_rn(
                                 __fmul_rn(acc[i][2 + jj], unscale), su[i]);
                             const int64_t o = (int64_t)(t.p0 + n) * a.I + row;
-                            a.out[o] = swiglu_out(a.sigmoid, g32, u32);
-                            if (a.gate_f32)
-                                a.gate_f32[o] = g32;
-                            if (a.up_f32)
-                                a.up_f32[o] = u32;
+                            if (kDown) {
+                                a.out[o] = bf16_rne(g32);
+                                if (a.gate_f32)
+                                    a.gate_f32[o] = g32;
+                                if (live_hi) {
+                                    a.out[o + kHiRow] = bf16_rne(u32);
+                                    if (a.gate_f32)
+                                        a.gate_f32[o + kHiRow] = u32;
+                                }
+                            } else {
+                                a.out[o] = swiglu_out(a.sigmoid, g32, u32);
+                                if (a.gate_f32)
+                                    a.gate_f32[o] = g32;
+                                if (a.up_f32)
+                                    a.up_f32[o] = u32;
+                            }
                         }
                     }
                 }
@@ -605,7 +635,7 @@ cudaError_t encode_weight_map(const GateUpArgs &a, int64_t section_off,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NB>
+template <int NB, bool kDown>
 cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
     int D = kMaxStages;
     while (D > 2 && tma_smem(a, NB, D, tok_cap) > kSmemLimit)
@@ -619,7 +649,7 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
         err = encode_weight_map(a, a.up_w_off, NB * 16, &mu);
     if (err != cudaSuccess)
         return err;
-    err = cudaFuncSetAttribute(matvec_tma_kernel<NB>,
+    err = cudaFuncSetAttribute(matvec_tma_kernel<NB, kDown>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess)
@@ -627,8 +657,14 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
     // a single expert's rows all above the matvec's limit: nothing to do
     if (a.E == 1 && a.M > a.matvec_max_rows)
         return cudaSuccess;
-    return launch_pdl(matvec_tma_kernel<NB>, dim3((unsigned)a.num_sms),
+    return launch_pdl(matvec_tma_kernel<NB, kDown>, dim3((unsigned)a.num_sms),
                       dim3(kThreads), smem, s, a, mg, mu, tok_cap, D);
+}
+
+template <int NB>
+cudaError_t launch_mode(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
+    return a.down ? launch_nb<NB, true>(a, tok_cap, s)
+                  : launch_nb<NB, false>(a, tok_cap, s);
 }
 
 }  // namespace
@@ -650,22 +686,25 @@ bool matvec_tma_supported(const GateUpArgs &a) {
 cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s) {
     const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
     switch (a.matvec_tile) {
-    case 16: return launch_nb<1>(a, tok_cap, s);
-    case 32: return launch_nb<2>(a, tok_cap, s);
-    case 64: return launch_nb<4>(a, tok_cap, s);
-    case 128: return launch_nb<8>(a, tok_cap, s);
+    case 16: return launch_mode<1>(a, tok_cap, s);
+    case 32: return launch_mode<2>(a, tok_cap, s);
+    case 64: return launch_mode<4>(a, tok_cap, s);
+    case 128: return launch_mode<8>(a, tok_cap, s);
     default: break;
     }
     const int64_t chunks = std::min<int64_t>(a.E, a.M);
-    const int64_t IBk = a.I / 16;
+    const int64_t rows16 = a.down ? 32 : 16;   // output rows per 16-row box
     const int64_t want = 4ll * a.num_sms;
-    if (chunks * ((IBk + 7) / 8) >= want)
-        return launch_nb<8>(a, tok_cap, s);
-    if (chunks * ((IBk + 3) / 4) >= want)
-        return launch_nb<4>(a, tok_cap, s);
-    if (chunks * ((IBk + 1) / 2) >= want)
-        return launch_nb<2>(a, tok_cap, s);
-    return launch_nb<1>(a, tok_cap, s);
+    auto units = [&](int64_t nb) {
+        return chunks * ((a.I + rows16 * nb - 1) / (rows16 * nb));
+    };
+    if (units(8) >= want)
+        return launch_mode<8>(a, tok_cap, s);
+    if (units(4) >= want)
+        return launch_mode<4>(a, tok_cap, s);
+    if (units(2) >= want)
+        return launch_mode<2>(a, tok_cap, s);
+    return launch_mode<1>(a, tok_cap, s);
 }
 
 }  // namespace q4moe

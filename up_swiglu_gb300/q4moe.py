@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -41,7 +41,8 @@ EXPORTS = (
     "q4moe_validate_layout", "q4moe_pack_slab", "q4moe_group_rows",
     "q4moe_gate_up_swiglu", "q4moe_gate_up_swiglu_ex", "q4moe_device_status",
     "q4moe_debug_tail", "q4moe_launch_count", "q4moe_workspace_bytes",
-    "q4moe_gate_up_swiglu_noalloc",
+    "q4moe_gate_up_swiglu_noalloc", "q4moe_pack_slab_down",
+    "q4moe_down_proj", "q4moe_expert_mlp",
 )
 
 # Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
@@ -61,7 +62,9 @@ class q4moe_layout_t(ctypes.Structure):
                 ("gate_w_offset", ctypes.c_int64),
                 ("up_w_offset", ctypes.c_int64),
                 ("gate_s_offset", ctypes.c_int64),
-                ("up_s_offset", ctypes.c_int64)]
+                ("up_s_offset", ctypes.c_int64),
+                ("down_w_offset", ctypes.c_int64),
+                ("down_s_offset", ctypes.c_int64)]
 
 
 class q4moe_slabs_t(ctypes.Structure):
@@ -131,6 +134,12 @@ def load(build_if_missing: bool = True):
             "q4moe_gate_up_swiglu_noalloc": (ctypes.c_int,
                                              [_P, _P, _P, _P, _I64, _I64,
                                               _I64, _P, _P]),
+            "q4moe_pack_slab_down": (ctypes.c_int, [_P, _P, _P, _P]),
+            "q4moe_down_proj": (ctypes.c_int,
+                                [_P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+            "q4moe_expert_mlp": (ctypes.c_int,
+                                 [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P,
+                                  _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -196,6 +205,11 @@ def q4moe_pack_slab(layout, gate_w, up_w, gate_s, up_s, slab_host) -> None:
                                   _ptr(slab_host)))
 
 
+def q4moe_pack_slab_down(layout, down_w, down_s, slab_host) -> None:
+    _check(load().q4moe_pack_slab_down(ctypes.byref(layout), _ptr(down_w),
+                                       _ptr(down_s), _ptr(slab_host)))
+
+
 def q4moe_group_rows(topk_ids, T, k, E, row_offsets, token_of_row,
                      row_of_pair, stream=None) -> None:
     _check(load().q4moe_group_rows(_ptr(topk_ids), T, k, E, _ptr(row_offsets),
@@ -230,6 +244,23 @@ def q4moe_gate_up_swiglu_noalloc(x, expert_slabs, row_offsets_per_expert,
     _check(load().q4moe_gate_up_swiglu_noalloc(
         _ptr(x), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
         _ptr(token_to_expert_map), M, H, I, _ptr(out), _stream(stream)))
+
+
+def q4moe_down_proj(mid, expert_slabs, row_offsets_per_expert, M, H, I, out,
+                    opts=None, stream=None) -> None:
+    _check(load().q4moe_down_proj(
+        _ptr(mid), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
+        M, H, I, _ptr(out), None if opts is None else ctypes.byref(opts),
+        _stream(stream)))
+
+
+def q4moe_expert_mlp(x, expert_slabs, row_offsets_per_expert,
+                     token_to_expert_map, M, H, I, mid, out, opts=None,
+                     stream=None) -> None:
+    _check(load().q4moe_expert_mlp(
+        _ptr(x), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
+        _ptr(token_to_expert_map), M, H, I, _ptr(mid), _ptr(out),
+        None if opts is None else ctypes.byref(opts), _stream(stream)))
 
 
 def q4moe_device_status(stream=None, clear: bool = True) -> int:
@@ -273,10 +304,12 @@ def make_slabs(num_experts: int, layout: q4moe_layout_t, base=None,
     return s
 
 
-def pack_slab_pool(layout: q4moe_layout_t, gate_w, up_w, gate_s, up_s):
+def pack_slab_pool(layout: q4moe_layout_t, gate_w, up_w, gate_s, up_s,
+                   down_w=None, down_s=None):
     """Host uint8 array [E, slab_bytes] holding every expert's slab (numpy
-    inputs [E, I, H/8] / [E, I]); copy it to one 4096-aligned device
-    allocation to use it."""
+    inputs [E, I, H/8] / [E, I], and optionally the down sections
+    [E, H, I/8] / [E, H]); copy it to one 4096-aligned device allocation to
+    use it."""
     import numpy as np
     E = gate_w.shape[0]
     pool = np.empty((E, layout.slab_bytes), dtype=np.uint8)
@@ -285,4 +318,7 @@ def pack_slab_pool(layout: q4moe_layout_t, gate_w, up_w, gate_s, up_s):
                         np.ascontiguousarray(up_w[e]),
                         np.ascontiguousarray(gate_s[e]),
                         np.ascontiguousarray(up_s[e]), pool[e])
+        if down_w is not None:
+            q4moe_pack_slab_down(layout, np.ascontiguousarray(down_w[e]),
+                                 np.ascontiguousarray(down_s[e]), pool[e])
     return pool
