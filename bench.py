@@ -2,7 +2,10 @@
 """Benchmark of the fused Q4 MoE expert gate/up + SwiGLU on one GB300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-  * grouped workloads: token->expert grouping + the fused gate/up call;
+  * grouped workloads: token->expert grouping + the fused gate/up call
+    (--op down: grouping + the down projection of synthetic intermediate
+    activations; --op mlp: grouping + the whole expert MLP, gate/up then
+    down);
   * the single-expert decode workload (H=4096, I=1536, one token): the call
     repeated 1000 times (the workload's own definition), each repeat on a
     different expert slab from a pool larger than 4x L2, captured once in a
@@ -10,7 +13,8 @@ One step = one pass of the whole path over one batch of synthetic input:
 Inputs stay resident in HBM; every step streams its weights from HBM (the
 weight pool of every workload is larger than L2).  Prints one JSON line.
 
-  python bench.py [--workload NAME] [--steps K] [--warmup W] [--gpus N]
+  python bench.py [--workload NAME] [--op gate_up|down|mlp] [--steps K]
+                  [--warmup W] [--gpus N]
   python bench.py --impl reference ...   (the CPU oracle, timed alone)
 """
 from __future__ import annotations
@@ -34,6 +38,15 @@ from up_swiglu_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = ("weight GB/s and TFLOP/s of Q4 MoE gate/up/SwiGLU; "
           "% of HBM / tensor roofline")
+OP_METRIC = {
+    "gate_up": METRIC,
+    "down": ("weight GB/s and TFLOP/s of the Q4 MoE down projection; "
+             "% of HBM / tensor roofline"),
+    "mlp": ("weight GB/s and TFLOP/s of the Q4 MoE expert MLP (gate/up/"
+            "SwiGLU, then down); % of HBM / tensor roofline"),
+}
+OP_ENTRY = {"gate_up": "q4moe_gate_up_swiglu", "down": "q4moe_down_proj",
+            "mlp": "q4moe_expert_mlp"}
 DEFAULT_WORKLOAD = "expert1_h4096_i1536_m1_x1000"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
@@ -48,6 +61,10 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--op", default="gate_up",
+                    choices=["gate_up", "down", "mlp"],
+                    help="the gate/up call (default), the down projection, "
+                         "or the whole expert MLP")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -63,26 +80,34 @@ def parse_args():
 
 # ------------------------------------------------------------ workload math --
 
-def workload_units(w: syn.Workload, topk: np.ndarray, E_pool: int):
+def workload_units(w: syn.Workload, topk: np.ndarray, E_pool: int,
+                   op: str = "gate_up"):
     """Algorithmic work of one step: weight bytes (each touched expert's
-    packed words + f32 scales, once per call), all bytes (+ x read + out
-    written) and flops (4*H*I per routed row)."""
-    per_expert = w.I * (w.H + 8)
+    packed words + f32 scales, once per call), all bytes (+ activations read
+    + outputs written) and flops.  gate/up: I*(H+8) weight bytes per expert,
+    x read (2*H per token), out written (2*I per routed row), 4*H*I flops per
+    routed row.  down: H*(I/2+4) weight bytes, mid read (2*I per row), out
+    written (2*H per row), 2*H*I flops.  mlp: both, mid written and read
+    back."""
+    gu = w.I * (w.H + 8)
+    dn = w.H * (w.I // 2 + 4)
+    per_expert = {"gate_up": gu, "down": dn, "mlp": gu + dn}[op]
+    rows = w.routed_rows
+    act = {"gate_up": 2 * w.H * w.T + 2 * w.I * rows,
+           "down": 2 * w.I * rows + 2 * w.H * rows,
+           "mlp": 2 * w.H * w.T + 4 * w.I * rows + 2 * w.H * rows}[op]
+    fl = {"gate_up": 4, "down": 2, "mlp": 6}[op] * w.H * w.I * rows
     if w.repeats > 1:
         calls = w.repeats
-        weight = calls * per_expert
-        x_bytes = calls * 2 * w.H * w.T
-        out_bytes = calls * 2 * w.I * w.routed_rows
-        flops = calls * 4 * w.H * w.I * w.routed_rows
         touched = calls
+        weight = calls * per_expert
+        act *= calls
+        fl *= calls
     else:
         touched = int(np.unique(topk).size)
         weight = touched * per_expert
-        x_bytes = 2 * w.H * w.T
-        out_bytes = 2 * w.I * w.routed_rows
-        flops = 4 * w.H * w.I * w.routed_rows
-    return dict(weight_bytes=weight, bytes=weight + x_bytes + out_bytes,
-                flops=flops, touched_experts=touched)
+    return dict(weight_bytes=weight, bytes=weight + act, flops=fl,
+                touched_experts=touched)
 
 
 def load_peaks():
@@ -189,10 +214,11 @@ class GpuWorkload:
     """Device-resident inputs for one workload and the step launcher."""
 
     def __init__(self, w: syn.Workload, kernel: str, device: int,
-                 use_workspace: bool = True, matvec_tile: int = 0):
+                 use_workspace: bool = True, matvec_tile: int = 0,
+                 op: str = "gate_up"):
         import torch
         from up_swiglu_gb300 import q4moe as q
-        self.torch, self.q, self.w = torch, q, w
+        self.torch, self.q, self.w, self.op = torch, q, w, op
         self.kernel = {"auto": q.KERNEL_AUTO, "matvec": q.KERNEL_MATVEC,
                        "gemm": q.KERNEL_GEMM}[kernel]
         self.dev = torch.device("cuda", device)
@@ -207,10 +233,13 @@ class GpuWorkload:
             pool_experts = w.E
         self.pool_experts = pool_experts
         g = syn.generate(w, experts=pool_experts)
+        if op != "gate_up":
+            g.update(syn.generate_down(w, experts=pool_experts))
         self.host = g
         self.topk_host = g["topk"]
         host_pool = q.pack_slab_pool(L, g["gate_w"], g["up_w"], g["gate_s"],
-                                     g["up_s"])
+                                     g["up_s"], g.get("down_w"),
+                                     g.get("down_s"))
         nbytes = host_pool.size
         self._buf = torch.empty(nbytes + 4096, dtype=torch.uint8,
                                 device=self.dev)
@@ -225,8 +254,14 @@ class GpuWorkload:
         self.offs = torch.empty(w.E + 1, dtype=torch.int32, device=self.dev)
         self.tok = torch.empty(self.M, dtype=torch.int32, device=self.dev)
         self.rop = torch.empty(self.M, dtype=torch.int32, device=self.dev)
-        self.out = torch.empty((self.calls * self.M, w.I), dtype=torch.int16,
-                               device=self.dev)
+        self.out_cols = w.I if op == "gate_up" else w.H
+        self.out = torch.empty((self.calls * self.M, self.out_cols),
+                               dtype=torch.int16, device=self.dev)
+        if op == "down":            # the down projection's input, resident
+            self.mid = torch.from_numpy(g["mid"].view(np.int16)).to(self.dev)
+        elif op == "mlp":           # the MLP's intermediate scratch
+            self.mid = torch.empty((self.calls * self.M, w.I),
+                                   dtype=torch.int16, device=self.dev)
         if w.repeats > 1:
             # single expert, single row: the grouping is the identity
             self.offs.copy_(torch.tensor([0, self.M], dtype=torch.int32))
@@ -239,7 +274,10 @@ class GpuWorkload:
         self.opts = q.q4moe_options_t()
         self.opts.kernel = self.kernel
         self.opts.matvec_tile = matvec_tile
-        if use_workspace:
+        self.opts_down = q.q4moe_options_t()
+        self.opts_down.kernel = self.kernel
+        self.opts_down.matvec_tile = matvec_tile
+        if use_workspace and op != "down":
             # scratch for the grouped activations the tensor-core GEMM reads
             nbytes = q.q4moe_workspace_bytes(self.M, w.H)
             self._ws = torch.empty(nbytes + 256, dtype=torch.uint8,
@@ -251,11 +289,22 @@ class GpuWorkload:
         self.launches_per_step = None
 
     def _gate_up(self, r):
-        q = self.q
-        out = self.out.data_ptr() + r * self.M * self.w.I * 2
-        q.q4moe_gate_up_swiglu_ex(self.x, self.slabs[r], self.offs, self.tok,
-                                  self.M, self.w.H, self.w.I, out, self.opts,
-                                  self.stream)
+        """Call r of the step (one per repeat) through the library's entry
+        point for the measured operation."""
+        q, w = self.q, self.w
+        out = self.out.data_ptr() + r * self.M * self.out_cols * 2
+        if self.op == "gate_up":
+            q.q4moe_gate_up_swiglu_ex(self.x, self.slabs[r], self.offs,
+                                      self.tok, self.M, w.H, w.I, out,
+                                      self.opts, self.stream)
+        elif self.op == "down":
+            q.q4moe_down_proj(self.mid, self.slabs[r], self.offs, self.M,
+                              w.H, w.I, out, self.opts_down, self.stream)
+        else:
+            mid = self.mid.data_ptr() + r * self.M * w.I * 2
+            q.q4moe_expert_mlp(self.x, self.slabs[r], self.offs, self.tok,
+                               self.M, w.H, w.I, mid, out, self.opts,
+                               self.stream)
 
     def enqueue_step(self, ev=None):
         """Queue one step; ev = (start, mid) events bracket the grouping so
@@ -301,10 +350,12 @@ class GpuWorkload:
 
 # ------------------------------------------------------------ CPU oracle ----
 
-def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0):
-    """Time the oracle on grouped rows (all I outputs each) until about
+def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0,
+                  op: str = "gate_up"):
+    """Time the oracle on grouped rows (all outputs of each) until about
     budget_s seconds of work; returns (seconds per routed row, rows done,
-    threads)."""
+    threads).  op down: the down projection of the rows of g["mid"]; op
+    mlp: the rows' gate/up outputs, then their down outputs."""
     import oracle
     oracle.build()
     topk = g["topk"]
@@ -325,10 +376,22 @@ def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0):
         rows = order[i % M: i % M + batch] if M > 1 else order
         cols = np.tile(np.arange(w.I), rows.size)
         rr = np.repeat(rows, w.I)
+        rh = np.repeat(rows, w.H)
+        ch = np.tile(np.arange(w.H), rows.size)
         t0 = time.perf_counter()
-        oracle.gate_up_swiglu_sampled(
-            g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
-            g["up_s"][:Ew], offs, tok, rr, cols, nthreads=nthreads)
+        if op in ("gate_up", "mlp"):
+            r = oracle.gate_up_swiglu_sampled(
+                g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
+                g["up_s"][:Ew], offs, tok, rr, cols, nthreads=nthreads)
+        if op in ("down", "mlp"):
+            if op == "mlp":
+                mid = np.zeros((M, w.I), np.uint16)
+                mid[rr, cols] = r["out"]
+            else:
+                mid = g["mid"][:M]
+            oracle.down_proj_sampled(mid, g["down_w"][:Ew],
+                                     g["down_s"][:Ew], offs, rh, ch,
+                                     nthreads=nthreads)
         t_total += time.perf_counter() - t0
         rows_done += rows.size
         i += batch
@@ -370,31 +433,35 @@ def run_reference(args, w, rank, world):
     each step a bounded sample of the workload (rank 0 only)."""
     if rank != 0:
         return 0
+    op = args.op
     g = syn.generate(w, experts=w.E if w.repeats == 1 else 1)
-    units = workload_units(w, g["topk"], w.E)
+    if op != "gate_up":
+        g.update(syn.generate_down(w, experts=w.E if w.repeats == 1 else 1))
+    units = workload_units(w, g["topk"], w.E, op)
     per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps +
                                                     args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(w, g, per_step_budget / 4)
+        oracle_sample(w, g, per_step_budget / 4, op=op)
     times, rows = [], 0
     for _ in range(args.steps):
-        spr, n, threads = oracle_sample(w, g, per_step_budget)
+        spr, n, threads = oracle_sample(w, g, per_step_budget, op=op)
         times.append(spr)
         rows += n
     spr = statistics.mean(times)
     value, t_step = cpu_value(w, units, spr)
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4),
+        "impl": "reference", "metric": OP_METRIC[op],
+        "value": round(value, 4),
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded generator)",
-        "config": {"workload": w.name, "E": w.E, "H": w.H, "I": w.I,
-                   "tokens": w.T, "top_k": w.topk,
+        "config": {"workload": w.name, "op": op, "E": w.E, "H": w.H,
+                   "I": w.I, "tokens": w.T, "top_k": w.topk,
                    "routed_rows": w.routed_rows, "repeats": w.repeats},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
                          "cores": threads, "kind": "oracle",
-                         "sample": f"{rows} routed rows x all {w.I} outputs "
+                         "sample": f"{rows} routed rows x all their outputs "
                                    f"over {args.steps} steps, scaled to the "
                                    f"step's {w.routed_rows * w.repeats} rows"},
         "e2e": {"value": round(value, 4), "unit": "GB/s",
@@ -425,21 +492,23 @@ def main():
         dist.init_process_group("nccl")
     q.load()
 
+    op = args.op
     gw = GpuWorkload(w, args.kernel, local,
                      use_workspace=not args.no_workspace,
-                     matvec_tile=args.matvec_tile)
-    units = workload_units(w, gw.topk_host, gw.pool_experts)
+                     matvec_tile=args.matvec_tile, op=op)
+    units = workload_units(w, gw.topk_host, gw.pool_experts, op)
     dev = gw.dev
     stream = gw.stream
 
     # CPU baseline (host threads only, before the timed GPU work)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        spr, n, threads = oracle_sample(w, gw.host, args.cpu_seconds)
+        spr, n, threads = oracle_sample(w, gw.host, args.cpu_seconds,
+                                        op=op)
         v, _ = cpu_value(w, units, spr)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
                "kind": "oracle",
-               "sample": f"{n} routed rows x all {w.I} outputs "
+               "sample": f"{n} routed rows x all their outputs "
                          f"(~{args.cpu_seconds:.0f} s), scaled to the step's "
                          f"{w.routed_rows * w.repeats} rows"}
 
@@ -479,13 +548,14 @@ def main():
     value, tflops = job_rates(units, args.steps, world, total_ms)
     clocks = clk.summary()
 
-    # roofline of the dominant kernel: the fused gate/up launch(es)
+    # roofline of the dominant kernel: the fused call(s) of the operation
     peaks, peak_src = load_peaks()
     gu_ms = statistics.mean(gate_up_ms)
     per_launch_ms = gu_ms / gw.calls
     rows_per_expert = (w.routed_rows if w.repeats > 1 else
                        w.routed_rows / units["touched_experts"])
     decode = rows_per_expert < 64
+    traffic_key = w.name if op == "gate_up" else f"{w.name}:{op}"
     if decode:
         bytes_per_launch = units["bytes"] / gw.calls
         achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
@@ -493,8 +563,8 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(w.name, "q4moe_matvec_tma.cu"),
-                "kernel": "q4moe_gate_up_swiglu matvec",
+                "traffic": load_traffic(traffic_key, "q4moe_matvec_tma.cu"),
+                "kernel": f"{OP_ENTRY[op]} matvec",
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
         flops_per_launch = units["flops"] / gw.calls
@@ -503,13 +573,16 @@ def main():
         roof = {"bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(w.name, "q4moe_gemm.cu"),
-                "kernel": "q4moe_gate_up_swiglu gemm",
+                "traffic": load_traffic(traffic_key, "q4moe_gemm.cu"),
+                "kernel": f"{OP_ENTRY[op]} gemm",
                 "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (activations + routing) from pinned memory, D2H of the outputs
-    x_h = torch.from_numpy(gw.host["x"].view(np.int16)).pin_memory()
+    # (the down projection's input is mid instead of x)
+    x_dev = gw.mid if op == "down" else gw.x
+    x_src = gw.host["mid"] if op == "down" else gw.host["x"]
+    x_h = torch.from_numpy(x_src.view(np.int16)).pin_memory()
     t_h = torch.from_numpy(gw.topk_host).pin_memory()
     o_h = torch.empty(gw.out.shape, dtype=torch.int16).pin_memory()
     h2d = x_h.numel() * 2 + (t_h.numel() * 4 if w.repeats == 1 else 0)
@@ -520,7 +593,7 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        gw.x.copy_(x_h, non_blocking=True)
+        x_dev.copy_(x_h, non_blocking=True)
         if w.repeats == 1:
             gw.topk.copy_(t_h, non_blocking=True)
         gw.enqueue_step()
@@ -533,12 +606,13 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "metric": OP_METRIC[op], "value": round(value, 3), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": w.name, "E": w.E, "H": w.H, "I": w.I,
+            "config": {"workload": w.name, "op": op, "E": w.E, "H": w.H,
+                       "I": w.I,
                        "tokens": w.T, "top_k": w.topk,
                        "routed_rows": w.routed_rows, "repeats": w.repeats,
                        "touched_experts": units["touched_experts"],

@@ -24,7 +24,9 @@ Recipe (the workloads' shapes and value distributions):
   ``2**-k`` with k uniform in 4..9, so every dot product is exact in f32;
 - the down projection's weights and scales follow the same recipe (own
   streams); its exact case draws the intermediate activations as integers
-  in [-8, 8] and the scales as ``2**-k``, k uniform in 4..9.
+  in [-8, 8] and the scales as ``2**-k``, k uniform in 4..9; measured on
+  its own, its input (the intermediate activations) is a Box-Muller normal
+  with standard deviation 0.1, rounded to bf16.
 """
 from __future__ import annotations
 
@@ -40,7 +42,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # stream ids (distinct per array kind)
 S_X, S_GATE_W, S_UP_W, S_GATE_S, S_UP_S, S_ROUTE, S_EXACT_X, S_EXACT_S = \
     range(1, 9)
-S_DOWN_W, S_DOWN_S, S_EXACT_MID, S_EXACT_DS = range(9, 13)
+S_DOWN_W, S_DOWN_S, S_EXACT_MID, S_EXACT_DS, S_MID = range(9, 14)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -256,3 +258,13 @@ def generate(w: Workload, experts: int | None = None):
     gate_w, up_w, gate_s, up_s = weights(w.seed, E, w.I, w.H)
     return dict(x=x, gate_w=gate_w, up_w=up_w, gate_s=gate_s, up_s=up_s,
                 topk=routing(w))
+
+
+def generate_down(w: Workload, experts: int | None = None):
+    """The down projection's weights for ``experts`` experts (default w.E)
+    and, for measuring it on its own, grouped intermediate activations
+    (bf16 bits [routed rows, I], normal with standard deviation 0.1)."""
+    E = w.E if experts is None else experts
+    down_w, down_s = down_weights(w.seed, E, w.H, w.I)
+    mid = normal_x(w.seed, w.routed_rows, w.I, std=0.1, stream=S_MID)
+    return dict(down_w=down_w, down_s=down_s, mid=mid)
