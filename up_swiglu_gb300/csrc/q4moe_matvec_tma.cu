@@ -17,8 +17,9 @@
 // A pipeline stage is 32 KB: for both gate and up, P/2 TMA boxes of 128
 // bytes (256 K) x 16*NB rows, 128-byte swizzled, so a stage covers 128*P of
 // K and every warp one 128-wide K step of it.  A ring of D stages keeps the
-// stream in flight; after releasing stage j, warp j mod 16 waits until all
-// threads have released it and loads stage j + D into the freed slot.
+// stream in flight: one producer thread refills each slot once all consumer
+// threads have released it (measured: issuing a stage's boxes from several
+// lanes at once gains nothing).
 // Weights are dequantised in registers to f16: masking a word (or the word
 // shifted by 8) with 0x000F000F or 0x00F000F0 under the exponent of 1024.0
 // gives 1024 + n or 1024 + 16 n for the pairs {n_j, n_j+4}; one f16x2 fma
@@ -363,8 +364,6 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     tile = t.tile;
                 }
                 const int row0 = tile * kTileRows;
-                // the down projection's second half may lie past the last
-                // row: not loaded (its stale slot is never stored)
                 const bool hi = !kDown || row0 + kHiRow < (int)a.I;
                 for (int st = 0; st < nst; ++st, ++j) {
                     const int slot = j % D;
