@@ -364,6 +364,8 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     tile = t.tile;
                 }
                 const int row0 = tile * kTileRows;
+                // the down projection's second half may lie past the last
+                // row: not loaded (its stale slot is never stored)
                 const bool hi = !kDown || row0 + kHiRow < (int)a.I;
                 for (int st = 0; st < nst; ++st, ++j) {
                     const int slot = j % D;
