@@ -264,8 +264,13 @@ int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
  *   H, I                    must equal the layout's.
  *   out                     device bf16 [M][I], grouped-row order, fully
  *                           written on success.
- * Kernel choice per expert: up to 8 rows (and, measured, up to 48) on the
- * HBM-streaming matvec, more on the tcgen05 tensor-core GEMM.
+ * Kernel choice (Q4MOE_KERNEL_AUTO): experts with at most 48 rows run on
+ * the HBM-streaming matvec; the experts above go to the tcgen05 tensor-core
+ * GEMM when between them they make at least one GEMM tile (128 intermediate
+ * rows x up to 256 grouped rows) per SM, else the matvec takes every
+ * expert.  Decided on the host for one expert and on the device for
+ * several; a call with fewer than 49 * ceil(SMs / (I / 128)) rows never
+ * launches the GEMM.
  */
 int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *expert_slabs,
                          const int32_t *row_offsets_per_expert,

@@ -218,6 +218,27 @@ def test_auto_mixes_matvec_and_gemm(big):
     _run_and_compare(p)
 
 
+@pytest.mark.parametrize("counts,launches", [([60] * 10, 1),
+                                             ([60] * 11 + [40], 2)])
+def test_auto_skips_a_gemm_that_cannot_get_work(counts, launches):
+    """Under the automatic choice the GEMM needs ceil(152 / 12) = 13
+    experts above 48 rows: with fewer than 13 * 49 = 637 rows in the call
+    only the matvec is launched (600 rows here), with more the GEMM is
+    launched and finds too few tiles (700 rows: 11 experts of 60).  Same
+    results either way."""
+    import torch
+    p = hz.problem_with_counts(77, counts, 1536, 512, exact=True)
+    d = hz.upload(p)
+    offs_d, tok_d, _ = hz.group(d)
+    torch.cuda.synchronize()
+    n0 = q.q4moe_launch_count()
+    gpu = hz.gate_up(d, offs_d, tok_d, debug=False)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert q.q4moe_launch_count() - n0 == launches
+    orc = _oracle_full(p, offs_d.cpu().numpy(), tok_d.cpu().numpy())
+    assert np.array_equal(gpu["out"], orc["out"])
+
+
 @pytest.mark.parametrize("counts", [[0, 1, 7, 8, 9, 47, 48, 49, 63, 64, 65,
                                      129, 200, 257]])
 def test_parity_ragged_rows_per_expert(counts):

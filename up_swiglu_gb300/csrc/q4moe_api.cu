@@ -312,11 +312,17 @@ int dispatch(q4moe::GateUpArgs &a, const q4moe_options_t &o,
     } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
         // experts above 48 rows go to the GEMM if they fill the GPU with
         // tiles (decided on the device); a single expert's count is known
-        const int64_t tiles = (a.M + 255) / 256 * q4moe::gemm_row_tiles(a);
-        if (a.E > 1) {
+        const int64_t row_tiles = q4moe::gemm_row_tiles(a);
+        const int64_t tiles = (a.M + 255) / 256 * row_tiles;
+        // the GEMM's experts must make num_sms tiles between them: at least
+        // ceil(num_sms / row_tiles) experts of more than 48 rows, so fewer
+        // rows than that in the whole call never reach it (no GEMM launch)
+        const int64_t min_rows =
+            49 * ((d->num_sms + row_tiles - 1) / row_tiles);
+        if (a.E > 1 && a.M >= min_rows) {
             matvec_max = 48;
             a.gemm_min_tiles = d->num_sms;
-        } else if (a.M > 48 && tiles >= d->num_sms) {
+        } else if (a.E == 1 && a.M > 48 && tiles >= d->num_sms) {
             matvec_max = 0;
         }
     }
