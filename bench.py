@@ -69,7 +69,7 @@ def parse_args():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default="auto",
-                    choices=["auto", "matvec", "gemm"])
+                    choices=["auto", "matvec", "gemm", "invariant"])
     ap.add_argument("--no-workspace", action="store_true",
                     help="call without the scratch workspace")
     ap.add_argument("--matvec-tile", type=int, default=0,
@@ -220,7 +220,8 @@ class GpuWorkload:
         from up_swiglu_gb300 import q4moe as q
         self.torch, self.q, self.w, self.op = torch, q, w, op
         self.kernel = {"auto": q.KERNEL_AUTO, "matvec": q.KERNEL_MATVEC,
-                       "gemm": q.KERNEL_GEMM}[kernel]
+                       "gemm": q.KERNEL_GEMM,
+                       "invariant": q.KERNEL_BATCH_INVARIANT}[kernel]
         self.dev = torch.device("cuda", device)
         self.stream = torch.cuda.current_stream(self.dev)
         L = q.q4moe_canonical_layout(w.H, w.I)

@@ -89,6 +89,13 @@ extern "C" {
 #define Q4MOE_KERNEL_AUTO 0   /* by rows per expert                          */
 #define Q4MOE_KERNEL_MATVEC 1 /* every expert on the streamed matvec         */
 #define Q4MOE_KERNEL_GEMM 2   /* every nonempty expert on the tensor-core GEMM */
+/* Every expert on the matvec with a fixed unit height (matvec_tile, 128 if
+ * 0), never the GEMM or the cp.async matvec: each output's bits then depend
+ * on its own row's inputs only, not on how many rows (or which) share the
+ * call, so a row decoded alone and the same row in a verify batch agree bit
+ * for bit (page 52's matvec has this property: one SIMD group per row and
+ * sample).  Large groups stream each expert's weights once per 8 rows. */
+#define Q4MOE_KERNEL_BATCH_INVARIANT 3
 
 /*
  * Byte layout of one expert slab (page 51, layout.ts,

@@ -235,7 +235,7 @@ int check_kernel_options(const q4moe_options_t &o) {
     if ((o.matvec_tile != 0 && o.matvec_tile != 16 && o.matvec_tile != 32 &&
          o.matvec_tile != 64 && o.matvec_tile != 128) ||
         o.kernel < Q4MOE_KERNEL_AUTO ||
-        o.kernel > Q4MOE_KERNEL_GEMM || o.num_tokens < 0)
+        o.kernel > Q4MOE_KERNEL_BATCH_INVARIANT || o.num_tokens < 0)
         return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
     if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
         return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
@@ -299,7 +299,12 @@ int dispatch(q4moe::GateUpArgs &a, const q4moe_options_t &o,
              const DeviceInfo *d, cudaStream_t stream) {
     const bool gemm_ok = q4moe::gemm_supported(a.H, a.I, a);
     int32_t matvec_max = INT32_MAX;
-    if (o.kernel == Q4MOE_KERNEL_GEMM) {
+    if (o.kernel == Q4MOE_KERNEL_BATCH_INVARIANT) {
+        // the matvec alone, one unit height for every call
+        a.invariant = 1;
+        if (a.matvec_tile == 0)
+            a.matvec_tile = 128;
+    } else if (o.kernel == Q4MOE_KERNEL_GEMM) {
         if (!gemm_ok)
             return fail(Q4MOE_ERR_INVALID_ARG,
                         a.down ? "the tensor-core GEMM needs I %% 64 == 0, "

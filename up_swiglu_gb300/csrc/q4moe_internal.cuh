@@ -43,6 +43,7 @@ struct GateUpArgs {
     const uint16_t *sigmoid;     // sigmoid table: [65536] bf16, indexed by
                                  // the bf16 bits of gateT
     int32_t down;                // 1: the down projection (above)
+    int32_t invariant;           // 1: batch-invariant matvec versions only
 };
 
 // Host-side count of kernel launches (q4moe_launch_count).

@@ -1,7 +1,9 @@
 // q4moe_matvec.cu -- grouped Q4 gate/up + SwiGLU matvec for experts with few
 // rows (decode / speculative verify widths).
 //
-// launch_matvec picks the first version the call allows:
+// launch_matvec picks the first version the call allows (the TMA version
+// with a fixed unit height and the generic version are batch-invariant: a
+// row's result does not depend on the other rows of the call):
 //   q4moe_matvec_tma.cu  slabs at base + e * stride, H % 256 == 0,
 //                        I % 16 == 0, 16-byte aligned weight sections
 //                        (weights moved by TMA);
@@ -211,7 +213,9 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
     if (a.down)
         return launch_pdl(down_generic_kernel, grid,
                           dim3(kWarpsPerBlock * 32), 0, s, a);
-    if (matvec_mma_supported(a))
+    // (the cp.async version's reduction depends on the call's size: not
+    // used when the call must be batch-invariant)
+    if (!a.invariant && matvec_mma_supported(a))
         return launch_matvec_mma(a, s);
     return launch_pdl(matvec_generic_kernel, grid, dim3(kWarpsPerBlock * 32),
                       0, s, a);

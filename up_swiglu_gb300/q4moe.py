@@ -34,6 +34,7 @@ DEV_WAIT_TIMEOUT = 0x10
 KERNEL_AUTO = 0
 KERNEL_MATVEC = 1
 KERNEL_GEMM = 2
+KERNEL_BATCH_INVARIANT = 3
 
 # Every symbol include/q4moe.h declares (checked by the CPU tests).
 EXPORTS = (
