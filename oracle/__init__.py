@@ -78,6 +78,14 @@ def _load():
         lib.q4o_down_proj_sampled.argtypes = [
             _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
             _INT]
+        lib.q4o_q8_gate_up_swiglu.restype = _INT
+        lib.q4o_q8_gate_up_swiglu.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I64, _INT,
+            _I64, _P, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_q8_down_proj.restype = _INT
+        lib.q4o_q8_down_proj.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
+            _INT]
         lib.q4o_group_rows.restype = _INT
         lib.q4o_group_rows.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
         lib.q4o_max_threads.restype = _INT
@@ -274,3 +282,65 @@ def expert_mlp(x_bits, gate_w, up_w, gate_s, up_s, down_w, down_s,
                          token_of_row, nthreads=nthreads)
     return mid, down_proj(mid, down_w, down_s, row_offsets,
                           nthreads=nthreads)
+
+
+def q8_gate_up_swiglu(x_bits, gate_w, up_w, gate_s, up_s, row_offsets,
+                      token_of_row, rows=None, cols=None, silu_mode: int = 0,
+                      nthreads: int = 0):
+    """Q8 gate/up (page 52, Q8_GATE_UP_SOURCE): gate_w/up_w int8 [E, I, H].
+    All M x I outputs (arrays [M, I]) or, with rows/cols, those elements
+    only (arrays [n]).  Returns a dict with out, gate32, up32, gabs, uabs."""
+    x = _c(x_bits, np.uint16)
+    gw, uw = _c(gate_w, np.int8), _c(up_w, np.int8)
+    gs, us = _c(gate_s, np.float32), _c(up_s, np.float32)
+    offs, tok = _c(row_offsets, np.int32), _c(token_of_row, np.int32)
+    T, H = x.shape
+    E, I, _ = gw.shape
+    M = tok.shape[0]
+    if rows is None:
+        shape, n, r, c = (M, I), M * I, None, None
+    else:
+        r, c = _c(rows, np.int64), _c(cols, np.int64)
+        shape, n = (r.shape[0],), r.shape[0]
+    res = dict(out=np.zeros(shape, np.uint16),
+               gate32=np.zeros(shape, np.float32),
+               up32=np.zeros(shape, np.float32),
+               gabs=np.zeros(shape, np.float64),
+               uabs=np.zeros(shape, np.float64))
+    rc = _load().q4o_q8_gate_up_swiglu(
+        _ptr(x), T, H, I, E, _ptr(gw), _ptr(uw), _ptr(gs), _ptr(us),
+        _ptr(offs), _ptr(tok), M, int(silu_mode), n,
+        None if r is None else _ptr(r), None if c is None else _ptr(c),
+        _ptr(res["out"]), _ptr(res["gate32"]), _ptr(res["up32"]),
+        _ptr(res["gabs"]), _ptr(res["uabs"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return res
+
+
+def q8_down_proj(mid_bits, down_w, down_s, row_offsets, rows=None,
+                 cols=None, nthreads: int = 0):
+    """Q8 down projection (page 52, Q8_DOWN_SOURCE): down_w int8 [E, H, I].
+    All M x H outputs or the (rows, cols) elements; a dict with out, out32,
+    dabs."""
+    mid = _c(mid_bits, np.uint16)
+    dw, ds = _c(down_w, np.int8), _c(down_s, np.float32)
+    offs = _c(row_offsets, np.int32)
+    M, I = mid.shape
+    E, H, _ = dw.shape
+    if rows is None:
+        shape, n, r, c = (M, H), M * H, None, None
+    else:
+        r, c = _c(rows, np.int64), _c(cols, np.int64)
+        shape, n = (r.shape[0],), r.shape[0]
+    res = dict(out=np.zeros(shape, np.uint16),
+               out32=np.zeros(shape, np.float32),
+               dabs=np.zeros(shape, np.float64))
+    rc = _load().q4o_q8_down_proj(
+        _ptr(mid), M, I, H, E, _ptr(dw), _ptr(ds), _ptr(offs), n,
+        None if r is None else _ptr(r), None if c is None else _ptr(c),
+        _ptr(res["out"]), _ptr(res["out32"]), _ptr(res["dabs"]),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return res

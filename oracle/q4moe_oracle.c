@@ -19,6 +19,9 @@
  *    same expert (the row of packed words belongs to output row h and runs
  *    over the intermediate index k; f32 accumulation; times the f32 row
  *    scale of h; rounded to bf16);
+ *  - page 52, Q8_GATE_UP_SOURCE and Q8_DOWN_SOURCE: the same two
+ *    operations on signed int8 weights (one byte per weight, row-major, the
+ *    byte's two's-complement value, no zero point);
  *  - page 51, src/kernels/glm52/layout.ts: the per-expert section layout
  *    (the oracle takes the sections as separate arrays, so it never parses
  *    a slab).
@@ -129,6 +132,21 @@ static double q4o_dot(const uint32_t *wrow, const uint16_t *xrow, int64_t H,
         const int place = (int)(k & 7);
         const int q = (int)((word >> (4 * place)) & 0xFu) - 8;
         const double prod = (double)q * (double)q4o_bf16_to_f32(xrow[k]);
+        s += prod;
+        a += fabs(prod);
+    }
+    *absdot = a;
+    return s;
+}
+
+/* The same over a row of H signed bytes (page 52, Q8_GATE_UP_SOURCE:
+ * weight k is the int8 value of byte k of the row). */
+static double q4o_dot_q8(const int8_t *wrow, const uint16_t *xrow, int64_t H,
+                         double *absdot)
+{
+    double s = 0.0, a = 0.0;
+    for (int64_t k = 0; k < H; ++k) {
+        const double prod = (double)wrow[k] * (double)q4o_bf16_to_f32(xrow[k]);
         s += prod;
         a += fabs(prod);
     }
@@ -367,6 +385,118 @@ int q4o_down_proj_sampled(const uint16_t *mid, int64_t M, int64_t I,
  * putting outputs back in token order).  Rows of one expert keep the
  * token order (a stable counting sort).  Returns -1 on an expert id outside
  * [0, E). */
+/* ---- Q8 (page 52, Q8_GATE_UP_SOURCE, Q8_DOWN_SOURCE) ---------------------
+ * gate_w/up_w: int8 [E, I, H]; down_w: int8 [E, H, I]; everything else as
+ * for Q4 (the tail and the roundings are the same). */
+static void q4o_q8_element(const uint16_t *x, int64_t H, int64_t I,
+                           const int8_t *gate_w, const int8_t *up_w,
+                           const float *gate_s, const float *up_s, int32_t e,
+                           int64_t t, int64_t i, int silu_mode, uint16_t *out,
+                           float *gate32, float *up32, double *gabs,
+                           double *uabs)
+{
+    const int8_t *grow = gate_w + ((int64_t)e * I + i) * H;
+    const int8_t *urow = up_w + ((int64_t)e * I + i) * H;
+    double ga, ua;
+    const double G = q4o_dot_q8(grow, x + t * H, H, &ga);
+    const double U = q4o_dot_q8(urow, x + t * H, H, &ua);
+    const float g32 = (float)(G * (double)gate_s[(int64_t)e * I + i]);
+    const float u32 = (float)(U * (double)up_s[(int64_t)e * I + i]);
+    uint16_t res[5];
+    q4o_tail(g32, u32, silu_mode, res);
+    *out = res[4];
+    if (gate32) *gate32 = g32;
+    if (up32) *up32 = u32;
+    if (gabs) *gabs = ga;
+    if (uabs) *uabs = ua;
+}
+
+/* All M x I outputs, or (rows != NULL) the n elements (rows[j], cols[j]).
+ * Same arguments and results as q4o_gate_up_swiglu(_sampled). */
+int q4o_q8_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                          int32_t E, const int8_t *gate_w, const int8_t *up_w,
+                          const float *gate_s, const float *up_s,
+                          const int32_t *row_offsets,
+                          const int32_t *token_of_row, int64_t M,
+                          int silu_mode, int64_t n, const int64_t *rows,
+                          const int64_t *cols, uint16_t *out, float *gate32,
+                          float *up32, double *gabs, double *uabs,
+                          int nthreads)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || M < 0)
+        return -1;
+    if (row_offsets[0] != 0 || row_offsets[E] != M)
+        return -2;
+    for (int32_t e = 0; e < E; ++e)
+        if (row_offsets[e + 1] < row_offsets[e])
+            return -2;
+    for (int64_t p = 0; p < M; ++p)
+        if (token_of_row[p] < 0 || token_of_row[p] >= T)
+            return -3;
+    if (rows == 0)
+        n = M * I;
+    else
+        for (int64_t j = 0; j < n; ++j)
+            if (rows[j] < 0 || rows[j] >= M || cols[j] < 0 || cols[j] >= I)
+                return -4;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = rows ? rows[j] : j / I, i = rows ? cols[j] : j % I;
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        q4o_q8_element(x, H, I, gate_w, up_w, gate_s, up_s, e,
+                       token_of_row[p], i, silu_mode, &out[j],
+                       gate32 ? &gate32[j] : 0, up32 ? &up32[j] : 0,
+                       gabs ? &gabs[j] : 0, uabs ? &uabs[j] : 0);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* Q8 down projection: all M x H outputs, or the n elements (rows[j],
+ * cols[j]) when rows != NULL. */
+int q4o_q8_down_proj(const uint16_t *mid, int64_t M, int64_t I, int64_t H,
+                     int32_t E, const int8_t *down_w, const float *down_s,
+                     const int32_t *row_offsets, int64_t n,
+                     const int64_t *rows, const int64_t *cols, uint16_t *out,
+                     float *out32, double *dabs, int nthreads)
+{
+    if (M < 0 || I <= 0 || H <= 0 || E <= 0)
+        return -1;
+    if (row_offsets[0] != 0 || row_offsets[E] != M)
+        return -2;
+    for (int32_t e = 0; e < E; ++e)
+        if (row_offsets[e + 1] < row_offsets[e])
+            return -2;
+    if (rows == 0)
+        n = M * H;
+    else
+        for (int64_t j = 0; j < n; ++j)
+            if (rows[j] < 0 || rows[j] >= M || cols[j] < 0 || cols[j] >= H)
+                return -4;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = rows ? rows[j] : j / H, h = rows ? cols[j] : j % H;
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        double a;
+        const double D = q4o_dot_q8(down_w + ((int64_t)e * H + h) * I,
+                                    mid + p * I, I, &a);
+        const float v = (float)(D * (double)down_s[(int64_t)e * H + h]);
+        out[j] = q4o_bf16_rne(v);
+        if (out32) out32[j] = v;
+        if (dabs) dabs[j] = a;
+    }
+    (void)nthreads;
+    return 0;
+}
+
 int q4o_group_rows(const int32_t *topk, int64_t T, int32_t k, int32_t E,
                    int32_t *row_offsets, int32_t *token_of_row,
                    int32_t *row_of_pair)
