@@ -45,6 +45,13 @@ OP_METRIC = {
     "mlp": ("weight GB/s and TFLOP/s of the Q4 MoE expert MLP (gate/up/"
             "SwiGLU, then down); % of HBM / tensor roofline"),
 }
+
+
+def op_metric(op: str, fmt: str) -> str:
+    m = OP_METRIC[op]
+    return m.replace("Q4", "Q8") if fmt == "q8" else m
+
+
 OP_ENTRY = {"gate_up": "q4moe_gate_up_swiglu", "down": "q4moe_down_proj",
             "mlp": "q4moe_expert_mlp"}
 DEFAULT_WORKLOAD = "expert1_h4096_i1536_m1_x1000"
@@ -61,6 +68,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--format", default="q4", choices=["q4", "q8"],
+                    help="weight format: packed nibbles (q4) or signed "
+                         "bytes (q8)")
     ap.add_argument("--op", default="gate_up",
                     choices=["gate_up", "down", "mlp"],
                     help="the gate/up call (default), the down projection, "
@@ -81,16 +91,17 @@ def parse_args():
 # ------------------------------------------------------------ workload math --
 
 def workload_units(w: syn.Workload, topk: np.ndarray, E_pool: int,
-                   op: str = "gate_up"):
+                   op: str = "gate_up", fmt: str = "q4"):
     """Algorithmic work of one step: weight bytes (each touched expert's
     packed words + f32 scales, once per call), all bytes (+ activations read
     + outputs written) and flops.  gate/up: I*(H+8) weight bytes per expert,
     x read (2*H per token), out written (2*I per routed row), 4*H*I flops per
     routed row.  down: H*(I/2+4) weight bytes, mid read (2*I per row), out
     written (2*H per row), 2*H*I flops.  mlp: both, mid written and read
-    back."""
-    gu = w.I * (w.H + 8)
-    dn = w.H * (w.I // 2 + 4)
+    back.  Q8: one byte per weight instead of half a byte."""
+    per_byte = 1 if fmt == "q8" else 2           # weights per byte
+    gu = w.I * (2 * w.H // per_byte + 8)
+    dn = w.H * (w.I // per_byte + 4)
     per_expert = {"gate_up": gu, "down": dn, "mlp": gu + dn}[op]
     rows = w.routed_rows
     act = {"gate_up": 2 * w.H * w.T + 2 * w.I * rows,
@@ -215,7 +226,7 @@ class GpuWorkload:
 
     def __init__(self, w: syn.Workload, kernel: str, device: int,
                  use_workspace: bool = True, matvec_tile: int = 0,
-                 op: str = "gate_up"):
+                 op: str = "gate_up", fmt: str = "q4"):
         import torch
         from up_swiglu_gb300 import q4moe as q
         self.torch, self.q, self.w, self.op = torch, q, w, op
@@ -224,7 +235,8 @@ class GpuWorkload:
                        "invariant": q.KERNEL_BATCH_INVARIANT}[kernel]
         self.dev = torch.device("cuda", device)
         self.stream = torch.cuda.current_stream(self.dev)
-        L = q.q4moe_canonical_layout(w.H, w.I)
+        L = q.q4moe_canonical_layout_format(
+            w.H, w.I, q.FORMAT_Q8 if fmt == "q8" else q.FORMAT_Q4)
         self.layout = L
         if w.repeats > 1:
             # distinct expert slabs, more than 4x L2 in total
@@ -233,9 +245,9 @@ class GpuWorkload:
         else:
             pool_experts = w.E
         self.pool_experts = pool_experts
-        g = syn.generate(w, experts=pool_experts)
+        g = syn.generate(w, experts=pool_experts, fmt=fmt)
         if op != "gate_up":
-            g.update(syn.generate_down(w, experts=pool_experts))
+            g.update(syn.generate_down(w, experts=pool_experts, fmt=fmt))
         self.host = g
         self.topk_host = g["topk"]
         host_pool = q.pack_slab_pool(L, g["gate_w"], g["up_w"], g["gate_s"],
@@ -352,7 +364,7 @@ class GpuWorkload:
 # ------------------------------------------------------------ CPU oracle ----
 
 def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0,
-                  op: str = "gate_up"):
+                  op: str = "gate_up", fmt: str = "q4"):
     """Time the oracle on grouped rows (all outputs of each) until about
     budget_s seconds of work; returns (seconds per routed row, rows done,
     threads).  op down: the down projection of the rows of g["mid"]; op
@@ -381,18 +393,20 @@ def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0,
         ch = np.tile(np.arange(w.H), rows.size)
         t0 = time.perf_counter()
         if op in ("gate_up", "mlp"):
-            r = oracle.gate_up_swiglu_sampled(
-                g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
-                g["up_s"][:Ew], offs, tok, rr, cols, nthreads=nthreads)
+            gu = oracle.q8_gate_up_swiglu if fmt == "q8" else \
+                oracle.gate_up_swiglu_sampled
+            r = gu(g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
+                   g["up_s"][:Ew], offs, tok, rr, cols, nthreads=nthreads)
         if op in ("down", "mlp"):
             if op == "mlp":
                 mid = np.zeros((M, w.I), np.uint16)
                 mid[rr, cols] = r["out"]
             else:
                 mid = g["mid"][:M]
-            oracle.down_proj_sampled(mid, g["down_w"][:Ew],
-                                     g["down_s"][:Ew], offs, rh, ch,
-                                     nthreads=nthreads)
+            dn = oracle.q8_down_proj if fmt == "q8" else \
+                oracle.down_proj_sampled
+            dn(mid, g["down_w"][:Ew], g["down_s"][:Ew], offs, rh, ch,
+               nthreads=nthreads)
         t_total += time.perf_counter() - t0
         rows_done += rows.size
         i += batch
@@ -435,30 +449,33 @@ def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
     op = args.op
-    g = syn.generate(w, experts=w.E if w.repeats == 1 else 1)
+    fmt = args.format
+    g = syn.generate(w, experts=w.E if w.repeats == 1 else 1, fmt=fmt)
     if op != "gate_up":
-        g.update(syn.generate_down(w, experts=w.E if w.repeats == 1 else 1))
-    units = workload_units(w, g["topk"], w.E, op)
+        g.update(syn.generate_down(w, experts=w.E if w.repeats == 1 else 1,
+                                   fmt=fmt))
+    units = workload_units(w, g["topk"], w.E, op, fmt)
     per_step_budget = max(0.5, min(6.0, 150.0 / max(1, args.steps +
                                                     args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(w, g, per_step_budget / 4, op=op)
+        oracle_sample(w, g, per_step_budget / 4, op=op, fmt=fmt)
     times, rows = [], 0
     for _ in range(args.steps):
-        spr, n, threads = oracle_sample(w, g, per_step_budget, op=op)
+        spr, n, threads = oracle_sample(w, g, per_step_budget, op=op,
+                                        fmt=fmt)
         times.append(spr)
         rows += n
     spr = statistics.mean(times)
     value, t_step = cpu_value(w, units, spr)
     line = {
-        "impl": "reference", "metric": OP_METRIC[op],
+        "impl": "reference", "metric": op_metric(op, fmt),
         "value": round(value, 4),
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded generator)",
-        "config": {"workload": w.name, "op": op, "E": w.E, "H": w.H,
-                   "I": w.I, "tokens": w.T, "top_k": w.topk,
+        "config": {"workload": w.name, "op": op, "format": fmt, "E": w.E,
+                   "H": w.H, "I": w.I, "tokens": w.T, "top_k": w.topk,
                    "routed_rows": w.routed_rows, "repeats": w.repeats},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
                          "cores": threads, "kind": "oracle",
@@ -493,11 +510,11 @@ def main():
         dist.init_process_group("nccl")
     q.load()
 
-    op = args.op
+    op, fmt = args.op, args.format
     gw = GpuWorkload(w, args.kernel, local,
                      use_workspace=not args.no_workspace,
-                     matvec_tile=args.matvec_tile, op=op)
-    units = workload_units(w, gw.topk_host, gw.pool_experts, op)
+                     matvec_tile=args.matvec_tile, op=op, fmt=fmt)
+    units = workload_units(w, gw.topk_host, gw.pool_experts, op, fmt)
     dev = gw.dev
     stream = gw.stream
 
@@ -505,7 +522,7 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         spr, n, threads = oracle_sample(w, gw.host, args.cpu_seconds,
-                                        op=op)
+                                        op=op, fmt=fmt)
         v, _ = cpu_value(w, units, spr)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
                "kind": "oracle",
@@ -557,6 +574,8 @@ def main():
                        w.routed_rows / units["touched_experts"])
     decode = rows_per_expert < 64
     traffic_key = w.name if op == "gate_up" else f"{w.name}:{op}"
+    if fmt == "q8":
+        traffic_key += ":q8"
     if decode:
         bytes_per_launch = units["bytes"] / gw.calls
         achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
@@ -607,13 +626,13 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": OP_METRIC[op], "value": round(value, 3), "unit": "GB/s",
+            "metric": op_metric(op, fmt), "value": round(value, 3), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": w.name, "op": op, "E": w.E, "H": w.H,
-                       "I": w.I,
+            "config": {"workload": w.name, "op": op, "format": fmt,
+                       "E": w.E, "H": w.H, "I": w.I,
                        "tokens": w.T, "top_k": w.topk,
                        "routed_rows": w.routed_rows, "repeats": w.repeats,
                        "touched_experts": units["touched_experts"],

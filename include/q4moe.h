@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 4
+#define Q4MOE_ABI_VERSION 5
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -84,6 +84,10 @@ extern "C" {
 #define Q4MOE_DEV_BAD_SLAB_PTR 0x4u    /* per-expert slab pointer misaligned */
 #define Q4MOE_DEV_BAD_EXPERT_ID 0x8u   /* routed expert id outside [0, E)    */
 #define Q4MOE_DEV_WAIT_TIMEOUT 0x10u   /* a bounded on-chip wait ran out     */
+
+/* ---- weight formats (q4moe_layout_t.weight_format) --------------------- */
+#define Q4MOE_FORMAT_Q4 0 /* packed nibbles, value = nibble - 8 (page 52, GATE_UP_SOURCE) */
+#define Q4MOE_FORMAT_Q8 1 /* signed bytes, value = the byte (page 52, Q8_GATE_UP_SOURCE) */
 
 /* ---- kernel selection (q4moe_options_t.kernel) -------------------------- */
 #define Q4MOE_KERNEL_AUTO 0   /* by rows per expert                          */
@@ -109,6 +113,12 @@ extern "C" {
  *   down_s_offset: f32 [H] row scales, 4-byte aligned.  Both negative: the
  *       slab has no down sections (the gate/up calls never read them; the
  *       down calls then fail with Q4MOE_ERR_INVALID_ARG).
+ *   weight_format Q4MOE_FORMAT_Q8 (page 52, Q8_GATE_UP_SOURCE and
+ *       Q8_DOWN_SOURCE): the weight sections hold one signed byte per
+ *       weight instead, int8 [I][H] (gate, up) and [H][I] (down), element k
+ *       of a row at byte k; H and I must then be multiples of 4 (the page
+ *       accepts any size; rows here start on 4-byte boundaries).  The tail,
+ *       the scales and every rounding are the same as for Q4.
  * Each section must lie inside [0, slab_bytes) (page 51, validateRange).
  */
 typedef struct q4moe_layout {
@@ -122,6 +132,7 @@ typedef struct q4moe_layout {
     int64_t up_s_offset;
     int64_t down_w_offset;
     int64_t down_s_offset;
+    int64_t weight_format;     /* Q4MOE_FORMAT_Q4 (0) or Q4MOE_FORMAT_Q8        */
 } q4moe_layout_t;
 
 /*
@@ -217,13 +228,22 @@ const char *q4moe_last_error(void);
  */
 int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout);
 
+/* The canonical layout for a weight format: Q4MOE_FORMAT_Q4 as above;
+ * Q4MOE_FORMAT_Q8 with the same order and the weight sections twice as
+ * large (gate bytes at 0, up at I*H, gate scales at 2*I*H, up scales at
+ * 2*I*H + 4*I, down bytes at (2*I*H + 8*I) rounded up to 256, down scales
+ * after them).  Host only. */
+int q4moe_canonical_layout_format(int64_t H, int64_t I, int32_t format,
+                                  q4moe_layout_t *layout);
+
 /* Check a layout: dimensions (page 52, validateCall), section alignment and
  * ranges (page 51, validateRange).  Host only. */
 int q4moe_validate_layout(const q4moe_layout_t *layout);
 
 /*
  * Copy one expert's sections into a host slab buffer of layout->slab_bytes
- * bytes, zeroing the rest.  gate_w/up_w: host uint32 [I][H/8]; gate_s/up_s:
+ * bytes, zeroing the rest.  gate_w/up_w: host uint32 [I][H/8] (Q8 layouts:
+ * the int8 [I][H] bytes, passed through the same pointer type); gate_s/up_s:
  * host f32 [I]; slab_host: host buffer.  Host only (copy the slab to the
  * device yourself).
  */
@@ -233,8 +253,8 @@ int q4moe_pack_slab(const q4moe_layout_t *layout, const uint32_t *gate_w,
 
 /*
  * Copy one expert's down sections into a host slab buffer already filled by
- * q4moe_pack_slab (nothing else is touched).  down_w: host uint32 [H][I/8];
- * down_s: host f32 [H].  Host only.
+ * q4moe_pack_slab (nothing else is touched).  down_w: host uint32 [H][I/8]
+ * (Q8: the int8 [H][I] bytes); down_s: host f32 [H].  Host only.
  */
 int q4moe_pack_slab_down(const q4moe_layout_t *layout, const uint32_t *down_w,
                          const float *down_s, void *slab_host);

@@ -307,3 +307,64 @@ def down_scales(p: Problem, offs: np.ndarray):
     """down scale of every output element [M, H] (grouped order)."""
     e_of_row = np.repeat(np.arange(p.E), np.diff(offs))
     return p.down_s[e_of_row]
+
+
+def q8_layout(p: Problem):
+    return q.q4moe_canonical_layout_format(p.H, p.I, q.FORMAT_Q8)
+
+
+def q8_problem(seed, E, I, H, T, k, exact=False, routing="uniform",
+               with_down=True):
+    """A Q8 problem (int8 weights) with its down sections."""
+    if exact:
+        x, gw, uw, gs, us = syn.exact_q8_case(seed, T, H, E, I)
+    else:
+        x = syn.normal_x(seed, T, H)
+        gw, uw, gs, us = syn.q8_weights(seed, E, I, H)
+    topk = syn.route_uniform(seed, T, k, E) if routing == "uniform" else \
+        syn.route_zipf(seed, T, k, E, 1.1)
+    p = Problem(x, gw, uw, gs, us, topk)
+    if with_down:
+        p.down_w, p.down_s = syn.q8_down_weights(seed, E, H, I)
+        if exact:
+            ks = (syn.u64(seed, syn.S_EXACT_DS, E * H) % np.uint64(6)) \
+                .astype(np.int64) + 8
+            p.down_s = np.ldexp(np.float32(1.0), -ks).astype(
+                np.float32).reshape(E, H)
+    return p
+
+
+def q8_counts_problem(seed, counts, I, H, exact=False):
+    """Q8, one token per routed row, expert e getting counts[e] rows."""
+    E = len(counts)
+    T = int(sum(counts))
+    ids = np.concatenate([np.full(c, e, np.int32)
+                          for e, c in enumerate(counts)])
+    ids = ids[np.random.default_rng(seed).permutation(T)] if T else ids
+    p = q8_problem(seed, E, I, H, max(T, 1), 1, exact=exact)
+    p.x = p.x[:T]
+    p.topk = ids.reshape(T, 1)
+    return p
+
+
+def q8_down_only_problem(seed, counts, K, N, exact=False, mid_std=0.1):
+    """Q8 down projection on its own (see down_only_problem)."""
+    E, M = len(counts), int(sum(counts))
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    if exact:
+        mi = (syn.u64(seed, syn.S_EXACT_MID, max(M, 1) * K) %
+              np.uint64(17)).astype(np.int64) - 8
+        mid = syn.f32_to_bf16_bits(mi.astype(np.float32)).reshape(-1, K)[:M]
+    else:
+        mid = syn.normal_x(seed, max(M, 1), K, std=mid_std,
+                           stream=syn.S_MID)[:M]
+    dw, ds = syn.q8_down_weights(seed, E, N, K)
+    if exact:
+        ks = (syn.u64(seed, syn.S_EXACT_DS, E * N) % np.uint64(6)).astype(
+            np.int64) + 8
+        ds = np.ldexp(np.float32(1.0), -ks).astype(np.float32).reshape(E, N)
+    gw = np.zeros((E, K, N), np.int8)
+    gs = np.zeros((E, K), np.float32)
+    p = Problem(np.zeros((1, N), np.uint16), gw, gw, gs, gs,
+                np.zeros((1, 1), np.int32), dw, ds)
+    return p, mid, offs

@@ -76,6 +76,52 @@ def test_validate_layout_ranges_and_alignment():
     assert ei.value.code == q.ERR_ALIGNMENT
 
 
+def test_canonical_layout_q8_and_packing():
+    H, I = 64, 12
+    L = q.q4moe_canonical_layout_format(H, I, q.FORMAT_Q8)
+    assert L.weight_format == q.FORMAT_Q8
+    assert (L.gate_w_offset, L.up_w_offset) == (0, I * H)
+    assert (L.gate_s_offset, L.up_s_offset) == (2 * I * H, 2 * I * H + 4 * I)
+    assert L.down_w_offset == (2 * I * H + 8 * I + 255) // 256 * 256
+    assert L.down_s_offset == L.down_w_offset + H * I
+    assert L.slab_bytes == 4096
+    assert q.q4moe_canonical_layout_format(5120, 1536, q.FORMAT_Q8) \
+        .slab_bytes == (2 * 1536 * 5120 + 8 * 1536 + 5120 * 1536 + 4 * 5120
+                        + 4095) // 4096 * 4096
+    rng = np.random.default_rng(1)
+    gw = rng.integers(-128, 128, size=(I, H)).astype(np.int8)
+    uw = rng.integers(-128, 128, size=(I, H)).astype(np.int8)
+    dw = rng.integers(-128, 128, size=(H, I)).astype(np.int8)
+    gs, us, ds = (rng.random(n).astype(np.float32) for n in (I, I, H))
+    slab = np.full(L.slab_bytes, 0xAB, np.uint8)
+    q.q4moe_pack_slab(L, gw, uw, gs, us, slab)
+    q.q4moe_pack_slab_down(L, dw, ds, slab)
+    assert np.array_equal(slab[:I * H].view(np.int8).reshape(I, H), gw)
+    assert np.array_equal(slab[I * H:2 * I * H].view(np.int8).reshape(I, H),
+                          uw)
+    assert np.array_equal(slab[L.down_w_offset:L.down_w_offset + H * I]
+                          .view(np.int8).reshape(H, I), dw)
+    assert np.array_equal(slab[L.down_s_offset:L.down_s_offset + 4 * H]
+                          .view(np.float32), ds)
+    for H2, I2 in ((6, 4), (8, 6)):               # not multiples of 4
+        with pytest.raises(q.Q4moeError):
+            q.q4moe_canonical_layout_format(H2, I2, q.FORMAT_Q8)
+    with pytest.raises(q.Q4moeError):
+        q.q4moe_canonical_layout_format(64, 8, 7)   # unknown format
+    bad = q.q4moe_layout_t.from_buffer_copy(L)
+    bad.weight_format = 2
+    with pytest.raises(q.Q4moeError):
+        q.q4moe_validate_layout(bad)
+    # a Q4 layout read as Q8 needs twice the weight bytes: the down words
+    # run past the slab
+    bad = q.q4moe_layout_t.from_buffer_copy(
+        q.q4moe_canonical_layout(5120, 1536))
+    bad.weight_format = q.FORMAT_Q8
+    with pytest.raises(q.Q4moeError) as ei:
+        q.q4moe_validate_layout(bad)
+    assert ei.value.code == q.ERR_RANGE
+
+
 def test_validate_layout_down_sections():
     L = q.q4moe_canonical_layout(64, 8)
     bad = q.q4moe_layout_t.from_buffer_copy(L)

@@ -137,12 +137,17 @@ int validate_layout(const q4moe_layout_t *L) {
     if (L == nullptr)
         return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
     const int64_t H = L->hidden_size, I = L->intermediate_size;
+    const bool q8 = L->weight_format == Q4MOE_FORMAT_Q8;
+    if (L->weight_format != Q4MOE_FORMAT_Q4 && !q8)
+        return fail(Q4MOE_ERR_INVALID_ARG, "unknown weight format %lld",
+                    (long long)L->weight_format);
     if (H <= 0 || I <= 0)
         return fail(Q4MOE_ERR_INVALID_ARG,
                     "hidden and intermediate sizes must be positive");
-    if (H % 8 != 0)
+    if (H % (q8 ? 4 : 8) != 0)
         return fail(Q4MOE_ERR_INVALID_ARG,
-                    "Q4 hidden size must be divisible by 8");
+                    q8 ? "Q8 hidden size must be divisible by 4"
+                       : "Q4 hidden size must be divisible by 8");
     if (I % 4 != 0)
         return fail(Q4MOE_ERR_INVALID_ARG,
                     "intermediate size must be divisible by 4");
@@ -151,7 +156,7 @@ int validate_layout(const q4moe_layout_t *L) {
     if (L->slab_bytes <= 0)
         return fail(Q4MOE_ERR_INVALID_ARG, "slab bytes must be positive");
     int rc;
-    const int64_t wbytes = I * (H / 2), sbytes = I * 4;
+    const int64_t wbytes = q8 ? I * H : I * (H / 2), sbytes = I * 4;
     if ((rc = check_range(L->gate_w_offset, wbytes, L->slab_bytes,
                           "gate weights")) ||
         (rc = check_range(L->up_w_offset, wbytes, L->slab_bytes,
@@ -171,10 +176,11 @@ int validate_layout(const q4moe_layout_t *L) {
                     "down weights and down scales must both be present or "
                     "both absent (negative offsets)");
     if (L->down_w_offset >= 0) {
-        if (I % 8 != 0)
+        if (!q8 && I % 8 != 0)
             return fail(Q4MOE_ERR_INVALID_ARG,
                         "Q4 down sections need I divisible by 8");
-        if ((rc = check_range(L->down_w_offset, H * (I / 2), L->slab_bytes,
+        if ((rc = check_range(L->down_w_offset, q8 ? H * I : H * (I / 2),
+                              L->slab_bytes,
                               "down weights")) ||
             (rc = check_range(L->down_s_offset, H * 4, L->slab_bytes,
                               "down scales")))
@@ -291,6 +297,7 @@ q4moe::GateUpArgs base_args(const q4moe_slabs_t *slabs, int64_t M,
     a.num_sms = d->num_sms;
     a.matvec_tile = o.matvec_tile;
     a.sigmoid = d->sigmoid;
+    a.q8 = slabs->layout.weight_format == Q4MOE_FORMAT_Q8;
     return a;
 }
 
@@ -362,26 +369,37 @@ int64_t q4moe_workspace_bytes(int64_t M, int64_t H) {
 }
 
 int q4moe_canonical_layout(int64_t H, int64_t I, q4moe_layout_t *layout) {
+    return q4moe_canonical_layout_format(H, I, Q4MOE_FORMAT_Q4, layout);
+}
+
+int q4moe_canonical_layout_format(int64_t H, int64_t I, int32_t format,
+                                  q4moe_layout_t *layout) {
     if (layout == nullptr)
         return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
+    const bool q8 = format == Q4MOE_FORMAT_Q8;
+    if (format != Q4MOE_FORMAT_Q4 && !q8)
+        return fail(Q4MOE_ERR_INVALID_ARG, "unknown weight format %d",
+                    (int)format);
     q4moe_layout_t L{};
     L.hidden_size = H;
     L.intermediate_size = I;
-    if (H <= 0 || I <= 0 || H % 8 != 0 || I % 4 != 0)
+    L.weight_format = format;
+    if (H <= 0 || I <= 0 || H % (q8 ? 4 : 8) != 0 || I % 4 != 0)
         return fail(Q4MOE_ERR_INVALID_ARG,
-                    "need H > 0, H %% 8 == 0, I > 0, I %% 4 == 0");
+                    "need H > 0, H %% %d == 0, I > 0, I %% 4 == 0",
+                    q8 ? 4 : 8);
     if (H > (INT64_C(1) << 24) || I > (INT64_C(1) << 24))
         return fail(Q4MOE_ERR_INVALID_ARG, "dimensions above 2^24");
-    const int64_t wbytes = I * (H / 2);
+    const int64_t wbytes = q8 ? I * H : I * (H / 2);
     L.gate_w_offset = 0;
     L.up_w_offset = wbytes;
     L.gate_s_offset = 2 * wbytes;
     L.up_s_offset = 2 * wbytes + 4 * I;
     int64_t used = 2 * wbytes + 8 * I;
     L.down_w_offset = L.down_s_offset = -1;
-    if (I % 8 == 0) {
+    if (q8 || I % 8 == 0) {
         L.down_w_offset = (used + 255) / 256 * 256;
-        L.down_s_offset = L.down_w_offset + H * (I / 2);
+        L.down_s_offset = L.down_w_offset + wbytes;
         used = L.down_s_offset + 4 * H;
     }
     L.slab_bytes = (used + Q4MOE_SLAB_ALIGNMENT - 1) /
@@ -404,10 +422,12 @@ int q4moe_pack_slab(const q4moe_layout_t *L, const uint32_t *gate_w,
     if (!gate_w || !up_w || !gate_s || !up_s || !slab_host)
         return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
     const int64_t H = L->hidden_size, I = L->intermediate_size;
+    const int64_t wbytes =
+        L->weight_format == Q4MOE_FORMAT_Q8 ? I * H : I * (H / 2);
     uint8_t *s = static_cast<uint8_t *>(slab_host);
     memset(s, 0, (size_t)L->slab_bytes);
-    memcpy(s + L->gate_w_offset, gate_w, (size_t)(I * (H / 2)));
-    memcpy(s + L->up_w_offset, up_w, (size_t)(I * (H / 2)));
+    memcpy(s + L->gate_w_offset, gate_w, (size_t)wbytes);
+    memcpy(s + L->up_w_offset, up_w, (size_t)wbytes);
     memcpy(s + L->gate_s_offset, gate_s, (size_t)(I * 4));
     memcpy(s + L->up_s_offset, up_s, (size_t)(I * 4));
     return ok();
@@ -424,7 +444,9 @@ int q4moe_pack_slab_down(const q4moe_layout_t *L, const uint32_t *down_w,
         return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
     const int64_t H = L->hidden_size, I = L->intermediate_size;
     uint8_t *s = static_cast<uint8_t *>(slab_host);
-    memcpy(s + L->down_w_offset, down_w, (size_t)(H * (I / 2)));
+    memcpy(s + L->down_w_offset, down_w,
+           (size_t)(L->weight_format == Q4MOE_FORMAT_Q8 ? H * I
+                                                        : H * (I / 2)));
     memcpy(s + L->down_s_offset, down_s, (size_t)(H * 4));
     return ok();
 }

@@ -168,6 +168,27 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// Two words of four signed bytes each (K order) -> 8 bf16, exact (|b| <=
+// 128 needs 8 significant bits): each byte with its sign bit flipped is
+// b + 128, placed in the mantissa of 2^23 and reduced by 2^23 + 128 in f32.
+__device__ __forceinline__ uint4 dequant_bytes8(uint32_t w0, uint32_t w1) {
+    uint32_t r[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t t = (h ? w1 : w0) ^ 0x80808080u;
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            f[j] = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7650 + j)) -
+                   8388736.0f;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+        r[2 * h] = *reinterpret_cast<const uint32_t *>(&lo);
+        r[2 * h + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
 // K-major tile.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
@@ -228,7 +249,7 @@ gather_rows_kernel(GateUpArgs a) {
     }
 }
 
-template <bool kTma, bool kDown>
+template <bool kTma, bool kDown, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
     static_assert(kTma || !kDown, "the down projection reads mid by TMA");
@@ -419,28 +440,37 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
             const int64_t row = (int64_t)ti.iblk * tile_rows + r;
             // the second half's row exists (always, for gate/up)
             const bool uok = slab && (!kDown || row + hi_row < a.I);
+            // a k-block (64 K) of one row is kVecs 16-byte vectors: 32
+            // bytes of nibbles (Q4) or 64 of signed bytes (Q8)
+            constexpr int kVecs = kQ8 ? 4 : 2;
+            constexpr int kDepth = kQ8 ? 2 : kPrefetch;  // k-blocks in flight
+            const int64_t rb = weight_row_bytes(a, a.H);
             const uint4 *gp = slab ? reinterpret_cast<const uint4 *>(
-                                         slab + a.gate_w_off + row * (a.H / 2))
+                                         slab + a.gate_w_off + row * rb)
                                    : nullptr;
             const uint4 *up = uok ? reinterpret_cast<const uint4 *>(
-                                        slab + a.up_w_off +
-                                        (row + hi_row) * (a.H / 2))
+                                        slab + a.up_w_off + (row + hi_row) * rb)
                                   : nullptr;
-            uint4 ring[kPrefetch][4];
-            const uint4 kZero = make_uint4(0x88888888u, 0x88888888u,
-                                           0x88888888u, 0x88888888u);
+            uint4 ring[kDepth][2 * kVecs];
+            // weight zero: nibble 8 (Q4) or byte 0 (Q8)
+            const uint32_t z = kQ8 ? 0u : 0x88888888u;
+            const uint4 kZero = make_uint4(z, z, z, z);
 #pragma unroll
-            for (int d = 0; d < kPrefetch; ++d) {
+            for (int d = 0; d < kDepth; ++d) {
                 const bool in = d < KB;
-                ring[d][0] = (in && slab) ? __ldg(gp + 2 * d) : kZero;
-                ring[d][1] = (in && slab) ? __ldg(gp + 2 * d + 1) : kZero;
-                ring[d][2] = (in && uok) ? __ldg(up + 2 * d) : kZero;
-                ring[d][3] = (in && uok) ? __ldg(up + 2 * d + 1) : kZero;
+#pragma unroll
+                for (int v = 0; v < kVecs; ++v) {
+                    ring[d][v] = (in && slab) ? __ldg(gp + kVecs * d + v)
+                                              : kZero;
+                    ring[d][kVecs + v] = (in && uok)
+                                             ? __ldg(up + kVecs * d + v)
+                                             : kZero;
+                }
             }
             bool ok = true;
-            for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+            for (int kb0 = 0; kb0 < KB && ok; kb0 += kDepth) {
 #pragma unroll
-                for (int d = 0; d < kPrefetch; ++d) {
+                for (int d = 0; d < kDepth; ++d) {
                     const int kb = kb0 + d;
                     if (kb >= KB)
                         break;
@@ -455,24 +485,31 @@ gemm_tcgen05_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                     uint8_t *au = ag + A_BYTES;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint32_t wg =
-                            reinterpret_cast<const uint32_t *>(
-                                &ring[d][c >> 2])[c & 3];
-                        const uint32_t wu =
-                            reinterpret_cast<const uint32_t *>(
-                                &ring[d][2 + (c >> 2)])[c & 3];
+                        // 16-byte chunk c of the row's 64 K: 8 values
+                        const uint32_t *rg =
+                            reinterpret_cast<const uint32_t *>(&ring[d][0]);
+                        const uint32_t *ru =
+                            reinterpret_cast<const uint32_t *>(&ring[d][kVecs]);
+                        uint4 vg, vu;
+                        if (kQ8) {
+                            vg = dequant_bytes8(rg[2 * c], rg[2 * c + 1]);
+                            vu = dequant_bytes8(ru[2 * c], ru[2 * c + 1]);
+                        } else {
+                            vg = dequant_word(rg[c]);
+                            vu = dequant_word(ru[c]);
+                        }
                         *reinterpret_cast<uint4 *>(ag + sw128_offset(r, c)) =
-                            dequant_word(wg);
+                            vg;
                         *reinterpret_cast<uint4 *>(au + sw128_offset(r, c)) =
-                            dequant_word(wu);
+                            vu;
                     }
-                    const int kn = kb + kPrefetch;
+                    const int kn = kb + kDepth;
                     if (kn < KB && slab) {
-                        ring[d][0] = __ldg(gp + 2 * kn);
-                        ring[d][1] = __ldg(gp + 2 * kn + 1);
-                        if (uok) {
-                            ring[d][2] = __ldg(up + 2 * kn);
-                            ring[d][3] = __ldg(up + 2 * kn + 1);
+#pragma unroll
+                        for (int v = 0; v < kVecs; ++v) {
+                            ring[d][v] = __ldg(gp + kVecs * kn + v);
+                            if (uok)
+                                ring[d][kVecs + v] = __ldg(up + kVecs * kn + v);
                         }
                     }
                     fence_proxy_async_smem();
@@ -689,18 +726,25 @@ cudaError_t encode_xg_maps(const GateUpArgs &a, const uint16_t *rows,
     return cudaSuccess;
 }
 
-template <bool kTma, bool kDown>
-cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
-                               cudaStream_t s) {
+template <bool kTma, bool kDown, bool kQ8>
+cudaError_t launch_gemm_fmt(const GateUpArgs &a, const XgMaps &maps,
+                            cudaStream_t s) {
     const size_t smem = smem_bytes(a.E);
     cudaError_t err = cudaFuncSetAttribute(
-        gemm_tcgen05_kernel<kTma, kDown>,
+        gemm_tcgen05_kernel<kTma, kDown, kQ8>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
-    return launch_pdl(gemm_tcgen05_kernel<kTma, kDown>,
+    return launch_pdl(gemm_tcgen05_kernel<kTma, kDown, kQ8>,
                       dim3((unsigned)a.num_sms), dim3(kThreads), smem, s, a,
                       maps);
+}
+
+template <bool kTma, bool kDown>
+cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
+                               cudaStream_t s) {
+    return a.q8 ? launch_gemm_fmt<kTma, kDown, true>(a, maps, s)
+                : launch_gemm_fmt<kTma, kDown, false>(a, maps, s);
 }
 
 }  // namespace

@@ -44,7 +44,14 @@ struct GateUpArgs {
                                  // the bf16 bits of gateT
     int32_t down;                // 1: the down projection (above)
     int32_t invariant;           // 1: batch-invariant matvec versions only
+    int32_t q8;                  // 1: signed-byte weights (rows of H bytes)
 };
+
+// Bytes of one weight row of K values.
+__host__ __device__ __forceinline__ int64_t weight_row_bytes(
+    const GateUpArgs &a, int64_t K) {
+    return a.q8 ? K : K / 2;
+}
 
 // Host-side count of kernel launches (q4moe_launch_count).
 void count_launches(int n);

@@ -39,8 +39,37 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Weight `place` of packed word w: nibble place minus 8 (Q4, 8 per word)
+// or signed byte place (Q8, 4 per word), as f32.
+template <bool kQ8>
+__device__ __forceinline__ float weight_at(uint32_t w, int place) {
+    if (kQ8)
+        return (float)(int)(int8_t)(w >> (8 * place));
+    return (float)((int)((w >> (4 * place)) & 0xFu) - 8);
+}
+
+// The activations matching word w of a row: 8 bf16 (Q4) or 4 (Q8).
+template <bool kQ8>
+__device__ __forceinline__ void load_acts(const uint16_t *row, int64_t w,
+                                          uint32_t (&v)[4]) {
+    if (kQ8) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(row + w * 4);
+        v[0] = t.x;
+        v[1] = t.y;
+        v[2] = v[3] = 0;
+    } else {
+        const uint4 t = *reinterpret_cast<const uint4 *>(row + w * 8);
+        v[0] = t.x;
+        v[1] = t.y;
+        v[2] = t.z;
+        v[3] = t.w;
+    }
+}
+
+template <bool kQ8>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 matvec_generic_kernel(GateUpArgs a) {
+    constexpr int kPer = kQ8 ? 4 : 8;            // weights per 32-bit word
     __shared__ int32_t s_off[Q4MOE_MAX_EXPERTS + 1];
     grid_dependency_wait();
     if (!stage_row_offsets(a, s_off))
@@ -55,7 +84,7 @@ matvec_generic_kernel(GateUpArgs a) {
     if (slab == nullptr)
         return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t words = a.H / 8;
+    const int64_t words = a.H / kPer;
     const float *gs = reinterpret_cast<const float *>(slab + a.gate_s_off);
     const float *us = reinterpret_cast<const float *>(slab + a.up_s_off);
 
@@ -84,19 +113,14 @@ matvec_generic_kernel(GateUpArgs a) {
                 for (int j = 0; j < kChunk; ++j) {
                     if (tok[j] < 0)
                         continue;
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(
-                        a.x + tok[j] * a.H + w * 8);
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t xw[4];
+                    load_acts<kQ8>(a.x + tok[j] * a.H, w, xw);
 #pragma unroll
-                    for (int place = 0; place < 8; ++place) {
+                    for (int place = 0; place < kPer; ++place) {
                         const float xf = bf16_f32(
                             (xw[place >> 1] >> (16 * (place & 1))) & 0xFFFFu);
-                        const float wg =
-                            (float)((int)((g >> (4 * place)) & 0xFu) - 8);
-                        const float wu =
-                            (float)((int)((u >> (4 * place)) & 0xFu) - 8);
-                        ag[j] = __fmaf_rn(wg, xf, ag[j]);
-                        au[j] = __fmaf_rn(wu, xf, au[j]);
+                        ag[j] = __fmaf_rn(weight_at<kQ8>(g, place), xf, ag[j]);
+                        au[j] = __fmaf_rn(weight_at<kQ8>(u, place), xf, au[j]);
                     }
                 }
             }
@@ -122,8 +146,10 @@ matvec_generic_kernel(GateUpArgs a) {
 // Down projection, generic: warp per output row h (a.I of them) of one
 // expert, lanes over the row's K/8 words, up to 8 grouped rows of mid at a
 // time; out = bf16(sum * scale).
+template <bool kQ8>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 down_generic_kernel(GateUpArgs a) {
+    constexpr int kPer = kQ8 ? 4 : 8;
     __shared__ int32_t s_off[Q4MOE_MAX_EXPERTS + 1];
     grid_dependency_wait();
     if (!stage_row_offsets(a, s_off))
@@ -138,7 +164,7 @@ down_generic_kernel(GateUpArgs a) {
     if (slab == nullptr)
         return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t words = a.H / 8;
+    const int64_t words = a.H / kPer;
     const float *ds = reinterpret_cast<const float *>(slab + a.gate_s_off);
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const int64_t h = (int64_t)blockIdx.x * kRowsPerBlock +
@@ -159,16 +185,14 @@ down_generic_kernel(GateUpArgs a) {
                 for (int j = 0; j < kChunk; ++j) {
                     if (j >= nt)
                         continue;
-                    const uint4 mv = *reinterpret_cast<const uint4 *>(
-                        a.x + (int64_t)(p0 + j) * a.H + w * 8);
-                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+                    uint32_t mw[4];
+                    load_acts<kQ8>(a.x + (int64_t)(p0 + j) * a.H, w, mw);
 #pragma unroll
-                    for (int place = 0; place < 8; ++place) {
+                    for (int place = 0; place < kPer; ++place) {
                         const float mf = bf16_f32(
                             (mw[place >> 1] >> (16 * (place & 1))) & 0xFFFFu);
-                        const float wq =
-                            (float)((int)((q >> (4 * place)) & 0xFu) - 8);
-                        acc[j] = __fmaf_rn(wq, mf, acc[j]);
+                        acc[j] = __fmaf_rn(weight_at<kQ8>(q, place), mf,
+                                           acc[j]);
                     }
                 }
             }
@@ -210,15 +234,19 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
         return launch_matvec_tma(a, s);
     const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),
                     (unsigned)a.E);
+    const dim3 block(kWarpsPerBlock * 32);
     if (a.down)
-        return launch_pdl(down_generic_kernel, grid,
-                          dim3(kWarpsPerBlock * 32), 0, s, a);
+        return a.q8 ? launch_pdl(down_generic_kernel<true>, grid, block, 0, s,
+                                 a)
+                    : launch_pdl(down_generic_kernel<false>, grid, block, 0,
+                                 s, a);
     // (the cp.async version's reduction depends on the call's size: not
-    // used when the call must be batch-invariant)
-    if (!a.invariant && matvec_mma_supported(a))
+    // used when the call must be batch-invariant; Q4 only)
+    if (!a.invariant && !a.q8 && matvec_mma_supported(a))
         return launch_matvec_mma(a, s);
-    return launch_pdl(matvec_generic_kernel, grid, dim3(kWarpsPerBlock * 32),
-                      0, s, a);
+    return a.q8 ? launch_pdl(matvec_generic_kernel<true>, grid, block, 0, s, a)
+                : launch_pdl(matvec_generic_kernel<false>, grid, block, 0, s,
+                             a);
 }
 
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,

@@ -64,8 +64,13 @@ constexpr int kWarps = 16;                   // consumer warps
 constexpr int kCThreads = kWarps * 32;
 constexpr int kThreads = kCThreads + 32;     // + the producer warp
 constexpr int kTok = 8;                      // grouped rows per chunk
-constexpr int kStepK = 128;                  // K per consumer warp per stage
-constexpr int kBoxK = 256;                   // K per box row (128 bytes)
+// K values per 32-bit word, per box row (128 bytes) and per consumer warp
+// and stage (half a box row), for packed nibbles (Q4) or bytes (Q8)
+template <bool kQ8> struct Fmt {
+    static constexpr int kPerWord = kQ8 ? 4 : 8;
+    static constexpr int kBoxK = 32 * kPerWord;
+    static constexpr int kStepK = kBoxK / 2;
+};
 constexpr uint32_t kStageBytes = 32768;
 constexpr int kMaxStages = 4;
 
@@ -107,6 +112,18 @@ __device__ __forceinline__ Unit unit_of(int u, const int32_t *off,
 // apart) hit eight different bank groups.
 __device__ __forceinline__ int xs_chunk(int q, int n) {
     return q ^ ((((q >> 3) & 3) << 1) | (n & 1));
+}
+
+// Q8: the same role for the activations of a byte-weight stage, whose
+// threads read chunks 4 apart (tq); the XOR keeps the eight threads of a
+// shared-memory phase on eight different bank groups.
+__device__ __forceinline__ int xs_chunk_q8(int q, int n) {
+    return q ^ ((((q >> 2) & 3) << 1) | (n & 1));
+}
+
+template <bool kQ8>
+__device__ __forceinline__ int xs_phys(int q, int n) {
+    return kQ8 ? xs_chunk_q8(q, n) : xs_chunk(q, n);
 }
 
 // 8 consecutive 16-bit values (uint4) -> K order (0,4,1,5,2,6,3,7).
@@ -215,6 +232,65 @@ __device__ __forceinline__ void step_mma(float (&acc)[2][4],
     }
 }
 
+// The two pairs {b0, b1}, {b2, b3} of a word of four signed bytes, as f16x2
+// (exact): with the sign bits flipped each byte is b + 128, placed under the
+// exponent of 1024.0 it reads 1152 + b, and one fma subtracts 1152.
+__device__ __forceinline__ void byte_pairs_f16(uint32_t w, uint32_t (&r)[2]) {
+    const uint32_t t = w ^ 0x80808080u;
+    const uint32_t kOne = 0x3C003C00u, kM1152 = 0xE480E480u;   // 1, -1152
+    r[0] = fma_f16x2(__byte_perm(t, 0x64646464u, 0x5140), kOne, kM1152);
+    r[1] = fma_f16x2(__byte_perm(t, 0x64646464u, 0x7362), kOne, kM1152);
+}
+
+// The same pairs as bf16x2 (exact: |b| <= 128 needs 8 significant bits):
+// each byte placed in the mantissa of 2^23 (as b + 128) and reduced by
+// 2^23 + 128 in f32, then packed.
+__device__ __forceinline__ void byte_pairs_bf16(uint32_t w, uint32_t (&r)[2]) {
+    const uint32_t t = w ^ 0x80808080u;
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        f[j] = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7650 + j)) -
+               8388736.0f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+    r[0] = *reinterpret_cast<const uint32_t *>(&lo);
+    r[1] = *reinterpret_cast<const uint32_t *>(&hi);
+}
+
+// One Q8 K step: w[0..3] = 16 bytes (16 K) of gate row g, up row g, gate
+// row 8+g, up row 8+g; xb = the matching two 16-byte activation chunks
+// (natural K order).  One mma per word and row pair.
+template <bool kF16>
+__device__ __forceinline__ void step_mma_q8(float (&acc)[2][4],
+                                            const uint4 (&w)[4],
+                                            const uint4 (&xb)[2]) {
+    const uint32_t *wg0 = reinterpret_cast<const uint32_t *>(&w[0]);
+    const uint32_t *wu0 = reinterpret_cast<const uint32_t *>(&w[1]);
+    const uint32_t *wg1 = reinterpret_cast<const uint32_t *>(&w[2]);
+    const uint32_t *wu1 = reinterpret_cast<const uint32_t *>(&w[3]);
+    const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xb[0]);
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        uint32_t g0[2], u0[2], g1[2], u1[2];
+        if (kF16) {
+            byte_pairs_f16(wg0[wd], g0);
+            byte_pairs_f16(wu0[wd], u0);
+            byte_pairs_f16(wg1[wd], g1);
+            byte_pairs_f16(wu1[wd], u1);
+        } else {
+            byte_pairs_bf16(wg0[wd], g0);
+            byte_pairs_bf16(wu0[wd], u0);
+            byte_pairs_bf16(wg1[wd], g1);
+            byte_pairs_bf16(wu1[wd], u1);
+        }
+        mma_16816<kF16>(acc[0], g0[0], u0[0], g0[1], u0[1], xw[2 * wd],
+                        xw[2 * wd + 1]);
+        mma_16816<kF16>(acc[1], g1[0], u1[0], g1[1], u1[1], xw[2 * wd],
+                        xw[2 * wd + 1]);
+    }
+}
+
 // bf16 pair -> f16 pair, both scaled by 2^s (s such that the result is a
 // normal f32 below 2^16 for every nonzero half, checked by the caller):
 // the exponent field is raised by s, then rounded to f16, exactly.
@@ -265,11 +341,14 @@ __host__ __device__ __forceinline__ size_t red_bytes(int NB) {
     return (size_t)(kWarps - NB) * 32 * 2 * 16;
 }
 
-template <int NB, bool kDown>
+template <int NB, bool kDown, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
 matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                   const __grid_constant__ CUtensorMap tm_up, int tok_cap,
                   int D) {
+    constexpr int kPerWord = Fmt<kQ8>::kPerWord;
+    constexpr int kBoxK = Fmt<kQ8>::kBoxK;
+    constexpr int kStepK = Fmt<kQ8>::kStepK;
     constexpr int P = kWarps / NB;           // K parts per block
     constexpr int kBoxes = P / 2;            // boxes per matrix per stage
     constexpr int kRows = NB * 16;           // rows per box
@@ -380,7 +459,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                                           (hi ? 2u : 1u) * nbox * kBoxBytes);
                     const uint32_t dst = smem_u32(ring) + slot * kStageBytes;
                     for (int bx = 0; bx < nbox; ++bx) {
-                        const int c0 = (k0 + bx * kBoxK) / 8;
+                        const int c0 = (k0 + bx * kBoxK) / kPerWord;
                         tma_load_3d(dst + bx * kBoxBytes, &tm_gate, c0, row0,
                                     e, &full[slot]);
                         if (hi)
@@ -400,7 +479,10 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
         const int xrow = min(g, tok_cap - 1);    // rows past the chunk read a
                                                  // stale row; never stored
         const int xsw = (tq << 1) | (xrow & 1);
-        const uint8_t *xbase = xs + (size_t)xrow * H * 2 + tq * 128;
+        // the thread's activations: K from (2 tq + h) * kStepK / 4 within a
+        // box row, in 16-byte chunks of the row staged at xrow
+        const uint8_t *xbase = xs + (size_t)xrow * H * 2 +
+                               (kQ8 ? (tq >> 1) : tq) * 128;
         const int wc = ((2 * tq + h) ^ g) << 4;  // swizzled chunk in a row
         const int r0 = b * 16 + g;
         int staged_e = -1, staged_chunk = -1;
@@ -446,7 +528,8 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     exp_range(v.z, emax, emin, sub);
                     exp_range(v.w, emax, emin, sub);
                     *reinterpret_cast<uint4 *>(xs + (size_t)n * H * 2 +
-                                               xs_chunk(q, n) * 16) = permute8(v);
+                                               xs_phys<kQ8>(q, n) * 16) =
+                        kQ8 ? v : permute8(v);
                 }
 #pragma unroll
                 for (int d = 16; d > 0; d >>= 1) {
@@ -477,7 +560,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                     for (int idx = tid; idx < t.nt * qn; idx += kCThreads) {
                         const int n = idx / qn, q = idx - n * qn;
                         uint4 *p = reinterpret_cast<uint4 *>(
-                            xs + (size_t)n * H * 2 + xs_chunk(q, n) * 16);
+                            xs + (size_t)n * H * 2 + xs_phys<kQ8>(q, n) * 16);
                         const uint4 v = *p;
                         *p = make_uint4(bf16x2_to_f16x2(v.x, sc),
                                         bf16x2_to_f16x2(v.y, sc),
@@ -506,7 +589,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                         const uint8_t *wb =
                             ring + slot * kStageBytes + bx * kBoxBytes;
                         const uint8_t *ub = wb + kBoxes * kBoxBytes;
-                        uint4 w[4], xb[4];
+                        uint4 w[4];
                         w[0] = *reinterpret_cast<const uint4 *>(wb + r0 * 128 + wc);
                         w[1] = *reinterpret_cast<const uint4 *>(ub + r0 * 128 + wc);
                         w[2] = *reinterpret_cast<const uint4 *>(
@@ -514,14 +597,28 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                         w[3] = *reinterpret_cast<const uint4 *>(
                             ub + (r0 + 8) * 128 + wc);
                         const uint8_t *xk = xbase + kb * 2;
+                        if (kQ8) {
+                            uint4 xb[2];
 #pragma unroll
-                        for (int wd = 0; wd < 4; ++wd)
-                            xb[wd] = *reinterpret_cast<const uint4 *>(
-                                xk + (((4 * h + wd) ^ xsw) << 4));
-                        if (xf16)
-                            step_mma<true>(acc, w, xb);
-                        else
-                            step_mma<false>(acc, w, xb);
+                            for (int jj = 0; jj < 2; ++jj)
+                                xb[jj] = *reinterpret_cast<const uint4 *>(
+                                    xk + (((4 * (tq & 1) + 2 * h + jj) ^ xsw)
+                                          << 4));
+                            if (xf16)
+                                step_mma_q8<true>(acc, w, xb);
+                            else
+                                step_mma_q8<false>(acc, w, xb);
+                        } else {
+                            uint4 xb[4];
+#pragma unroll
+                            for (int wd = 0; wd < 4; ++wd)
+                                xb[wd] = *reinterpret_cast<const uint4 *>(
+                                    xk + (((4 * h + wd) ^ xsw) << 4));
+                            if (xf16)
+                                step_mma<true>(acc, w, xb);
+                            else
+                                step_mma<false>(acc, w, xb);
+                        }
                     }
                     mbar_arrive(&empty[slot]);   // this thread's reads are done
                 }
@@ -617,9 +714,9 @@ cudaError_t encode_weight_map(const GateUpArgs &a, int64_t section_off,
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
         return cudaErrorNotSupported;
-    const int64_t row_bytes = a.H / 2;
+    const int64_t row_bytes = weight_row_bytes(a, a.H);
     const int64_t sec_bytes = (a.I * row_bytes + 15) / 16 * 16;
-    const cuuint64_t dims[3] = {(cuuint64_t)(a.H / 8), (cuuint64_t)a.I,
+    const cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)a.I,
                                 (cuuint64_t)a.E};
     const cuuint64_t strides[2] = {
         (cuuint64_t)row_bytes,
@@ -636,7 +733,7 @@ cudaError_t encode_weight_map(const GateUpArgs &a, int64_t section_off,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NB, bool kDown>
+template <int NB, bool kDown, bool kQ8>
 cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
     int D = kMaxStages;
     while (D > 2 && tma_smem(a, NB, D, tok_cap) > kSmemLimit)
@@ -650,7 +747,7 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
         err = encode_weight_map(a, a.up_w_off, NB * 16, &mu);
     if (err != cudaSuccess)
         return err;
-    err = cudaFuncSetAttribute(matvec_tma_kernel<NB, kDown>,
+    err = cudaFuncSetAttribute(matvec_tma_kernel<NB, kDown, kQ8>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess)
@@ -658,24 +755,29 @@ cudaError_t launch_nb(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
     // a single expert's rows all above the matvec's limit: nothing to do
     if (a.E == 1 && a.M > a.matvec_max_rows)
         return cudaSuccess;
-    return launch_pdl(matvec_tma_kernel<NB, kDown>, dim3((unsigned)a.num_sms),
-                      dim3(kThreads), smem, s, a, mg, mu, tok_cap, D);
+    return launch_pdl(matvec_tma_kernel<NB, kDown, kQ8>,
+                      dim3((unsigned)a.num_sms), dim3(kThreads), smem, s, a,
+                      mg, mu, tok_cap, D);
 }
 
 template <int NB>
 cudaError_t launch_mode(const GateUpArgs &a, int tok_cap, cudaStream_t s) {
-    return a.down ? launch_nb<NB, true>(a, tok_cap, s)
-                  : launch_nb<NB, false>(a, tok_cap, s);
+    if (a.q8)
+        return a.down ? launch_nb<NB, true, true>(a, tok_cap, s)
+                      : launch_nb<NB, false, true>(a, tok_cap, s);
+    return a.down ? launch_nb<NB, true, false>(a, tok_cap, s)
+                  : launch_nb<NB, false, false>(a, tok_cap, s);
 }
 
 }  // namespace
 
 bool matvec_tma_supported(const GateUpArgs &a) {
     const int tok_cap = (int)std::min<int64_t>(kTok, a.M);
-    return a.slab_ptrs == nullptr && a.H % kBoxK == 0 && a.I % 16 == 0 &&
+    const int box_k = a.q8 ? Fmt<true>::kBoxK : Fmt<false>::kBoxK;
+    return a.slab_ptrs == nullptr && a.H % box_k == 0 && a.I % 16 == 0 &&
            a.gate_w_off % 16 == 0 && a.up_w_off % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(a.base) & 15) == 0 &&
-           a.H / 8 < (1ll << 31) && a.I < (1ll << 31) &&
+           a.H < (1ll << 31) && a.I < (1ll << 31) &&
            tensor_map_encoder() != nullptr &&
            tma_smem(a, 1, 2, tok_cap) <= kSmemLimit &&
            tma_smem(a, 8, 2, tok_cap) <= kSmemLimit;

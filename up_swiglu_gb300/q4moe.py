@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 4
+ABI_VERSION = 5
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -31,6 +31,9 @@ DEV_BAD_SLAB_PTR = 0x4
 DEV_BAD_EXPERT_ID = 0x8
 DEV_WAIT_TIMEOUT = 0x10
 
+FORMAT_Q4 = 0
+FORMAT_Q8 = 1
+
 KERNEL_AUTO = 0
 KERNEL_MATVEC = 1
 KERNEL_GEMM = 2
@@ -43,7 +46,7 @@ EXPORTS = (
     "q4moe_gate_up_swiglu", "q4moe_gate_up_swiglu_ex", "q4moe_device_status",
     "q4moe_debug_tail", "q4moe_launch_count", "q4moe_workspace_bytes",
     "q4moe_gate_up_swiglu_noalloc", "q4moe_pack_slab_down",
-    "q4moe_down_proj", "q4moe_expert_mlp",
+    "q4moe_down_proj", "q4moe_expert_mlp", "q4moe_canonical_layout_format",
 )
 
 # Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
@@ -65,7 +68,8 @@ class q4moe_layout_t(ctypes.Structure):
                 ("gate_s_offset", ctypes.c_int64),
                 ("up_s_offset", ctypes.c_int64),
                 ("down_w_offset", ctypes.c_int64),
-                ("down_s_offset", ctypes.c_int64)]
+                ("down_s_offset", ctypes.c_int64),
+                ("weight_format", ctypes.c_int64)]
 
 
 class q4moe_slabs_t(ctypes.Structure):
@@ -116,6 +120,8 @@ def load(build_if_missing: bool = True):
             "q4moe_abi_version": (ctypes.c_int, []),
             "q4moe_last_error": (ctypes.c_char_p, []),
             "q4moe_canonical_layout": (ctypes.c_int, [_I64, _I64, _P]),
+            "q4moe_canonical_layout_format": (ctypes.c_int,
+                                              [_I64, _I64, _I32, _P]),
             "q4moe_validate_layout": (ctypes.c_int, [_P]),
             "q4moe_pack_slab": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
             "q4moe_group_rows": (ctypes.c_int,
@@ -193,6 +199,13 @@ def q4moe_last_error() -> str:
 def q4moe_canonical_layout(H: int, I: int) -> q4moe_layout_t:
     L = q4moe_layout_t()
     _check(load().q4moe_canonical_layout(H, I, ctypes.byref(L)))
+    return L
+
+
+def q4moe_canonical_layout_format(H: int, I: int,
+                                  fmt: int) -> q4moe_layout_t:
+    L = q4moe_layout_t()
+    _check(load().q4moe_canonical_layout_format(H, I, fmt, ctypes.byref(L)))
     return L
 
 

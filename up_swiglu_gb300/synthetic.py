@@ -26,7 +26,11 @@ Recipe (the workloads' shapes and value distributions):
   streams); its exact case draws the intermediate activations as integers
   in [-8, 8] and the scales as ``2**-k``, k uniform in 4..9; measured on
   its own, its input (the intermediate activations) is a Box-Muller normal
-  with standard deviation 0.1, rounded to bf16.
+  with standard deviation 0.1, rounded to bf16;
+- Q8 weights: uniform signed bytes (-128..127, own streams), row scales of
+  the Q4 recipe divided by 16 (so that weight times scale spans the same
+  range as Q4's nibble - 8 times its scale); the Q8 exact case draws the
+  scales as ``2**-k``, k uniform in 8..13.
 """
 from __future__ import annotations
 
@@ -43,6 +47,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 S_X, S_GATE_W, S_UP_W, S_GATE_S, S_UP_S, S_ROUTE, S_EXACT_X, S_EXACT_S = \
     range(1, 9)
 S_DOWN_W, S_DOWN_S, S_EXACT_MID, S_EXACT_DS, S_MID = range(9, 14)
+S_Q8_GATE_W, S_Q8_UP_W, S_Q8_DOWN_W = range(14, 17)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -250,21 +255,59 @@ def routing(w: Workload) -> np.ndarray:
     raise ValueError(w.routing)
 
 
-def generate(w: Workload, experts: int | None = None):
-    """x bits [T, H], weights for ``experts`` experts (default w.E) and the
-    top-k ids [T, topk]."""
+def generate(w: Workload, experts: int | None = None, fmt: str = "q4"):
+    """x bits [T, H], weights for ``experts`` experts (default w.E; Q4
+    words, or Q8 bytes with fmt "q8") and the top-k ids [T, topk]."""
     E = w.E if experts is None else experts
     x = normal_x(w.seed, w.T, w.H, w.x_std)
-    gate_w, up_w, gate_s, up_s = weights(w.seed, E, w.I, w.H)
+    gate_w, up_w, gate_s, up_s = (q8_weights if fmt == "q8" else weights)(
+        w.seed, E, w.I, w.H)
     return dict(x=x, gate_w=gate_w, up_w=up_w, gate_s=gate_s, up_s=up_s,
                 topk=routing(w))
 
 
-def generate_down(w: Workload, experts: int | None = None):
+def generate_down(w: Workload, experts: int | None = None, fmt: str = "q4"):
     """The down projection's weights for ``experts`` experts (default w.E)
     and, for measuring it on its own, grouped intermediate activations
     (bf16 bits [routed rows, I], normal with standard deviation 0.1)."""
     E = w.E if experts is None else experts
-    down_w, down_s = down_weights(w.seed, E, w.H, w.I)
+    down_w, down_s = (q8_down_weights if fmt == "q8" else down_weights)(
+        w.seed, E, w.H, w.I)
     mid = normal_x(w.seed, w.routed_rows, w.I, std=0.1, stream=S_MID)
     return dict(down_w=down_w, down_s=down_s, mid=mid)
+
+
+def _bytes_i8(seed: int, stream: int, n: int) -> np.ndarray:
+    return words_u32(seed, stream, (n + 3) // 4).view(np.int8)[:n]
+
+
+def q8_weights(seed: int, E: int, I: int, H: int):
+    """(gate_w, up_w) int8 [E, I, H] and (gate_s, up_s) f32 [E, I]."""
+    n = E * I * H
+    gate_w = _bytes_i8(seed, S_Q8_GATE_W, n).reshape(E, I, H)
+    up_w = _bytes_i8(seed, S_Q8_UP_W, n).reshape(E, I, H)
+    gate_s = ((0.002 + 0.018 * uniform(seed, S_GATE_S, E * I)) / 16).astype(
+        np.float32).reshape(E, I)
+    up_s = ((0.002 + 0.018 * uniform(seed, S_UP_S, E * I)) / 16).astype(
+        np.float32).reshape(E, I)
+    return gate_w, up_w, gate_s, up_s
+
+
+def q8_down_weights(seed: int, E: int, H: int, I: int):
+    """down_w int8 [E, H, I] and down_s f32 [E, H]."""
+    down_w = _bytes_i8(seed, S_Q8_DOWN_W, E * H * I).reshape(E, H, I)
+    down_s = ((0.002 + 0.018 * uniform(seed, S_DOWN_S, E * H)) / 16).astype(
+        np.float32).reshape(E, H)
+    return down_w, down_s
+
+
+def exact_q8_case(seed: int, T: int, H: int, E: int, I: int):
+    """Integer activations in [-8, 8] (bf16 bits [T, H]), the Q8 weights of
+    ``q8_weights`` and power-of-two scales 2**-k, k in 8..13: every dot
+    product is an integer below 2**24 in magnitude for H <= 16384."""
+    xi = (u64(seed, S_EXACT_X, T * H) % np.uint64(17)).astype(np.int64) - 8
+    x = f32_to_bf16_bits(xi.astype(np.float32)).reshape(T, H)
+    ks = (u64(seed, S_EXACT_S, 2 * E * I) % np.uint64(6)).astype(np.int64) + 8
+    sc = np.ldexp(np.float32(1.0), -ks).astype(np.float32)
+    gate_w, up_w, _, _ = q8_weights(seed, E, I, H)
+    return x, gate_w, up_w, sc[: E * I].reshape(E, I), sc[E * I:].reshape(E, I)
