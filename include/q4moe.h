@@ -1,6 +1,8 @@
 /*
  * q4moe.h -- C ABI of the fused 4-bit MoE expert gate/up projection with
- * SwiGLU for one NVIDIA GB300 GPU (sm_103a).
+ * SwiGLU for one NVIDIA GB300 GPU (sm_103a), with the down projection that
+ * completes the expert MLP and the signed 8-bit weight format of the same
+ * page.
  *
  * The operation follows "@mlx-bun/inference 0.0.0-stage -> 1.0.0", page 52,
  * src/kernels/glm52/streamed-experts.ts, GATE_UP_SOURCE (and the
