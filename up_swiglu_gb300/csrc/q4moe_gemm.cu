@@ -168,25 +168,25 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Two words of four signed bytes each (K order) -> 8 bf16, exact (|b| <=
-// 128 needs 8 significant bits): each byte with its sign bit flipped is
-// b + 128, placed in the mantissa of 2^23 and reduced by 2^23 + 128 in f32.
+// Two signed bytes, given as t = {b0, 0x43, b1, 0x43} (bytes, low first),
+// -> bf16x2 {b0, b1}, exact: under the bf16 exponent byte 0x43 the low
+// seven bits m of a byte read 128 + m, its sign bit reads 128 or 256, and
+// b = (128 + m) - (128 + 128 * sign); the difference is an integer of at
+// most 8 bits, so the bf16 subtraction is exact.
+__device__ __forceinline__ uint32_t byte_pair_bf16(uint32_t t) {
+    const uint32_t m = t & 0x437F437Fu, c = t & 0x43804380u;
+    const __nv_bfloat162 r =
+        __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&m),
+                *reinterpret_cast<const __nv_bfloat162 *>(&c));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// Two words of four signed bytes each (K order) -> 8 bf16, exact.
 __device__ __forceinline__ uint4 dequant_bytes8(uint32_t w0, uint32_t w1) {
-    uint32_t r[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t t = (h ? w1 : w0) ^ 0x80808080u;
-        float f[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            f[j] = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7650 + j)) -
-                   8388736.0f;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
-        r[2 * h] = *reinterpret_cast<const uint32_t *>(&lo);
-        r[2 * h + 1] = *reinterpret_cast<const uint32_t *>(&hi);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
+    return make_uint4(byte_pair_bf16(__byte_perm(w0, 0x43434343u, 0x4140)),
+                      byte_pair_bf16(__byte_perm(w0, 0x43434343u, 0x4342)),
+                      byte_pair_bf16(__byte_perm(w1, 0x43434343u, 0x4140)),
+                      byte_pair_bf16(__byte_perm(w1, 0x43434343u, 0x4342)));
 }
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled

@@ -242,20 +242,19 @@ __device__ __forceinline__ void byte_pairs_f16(uint32_t w, uint32_t (&r)[2]) {
     r[1] = fma_f16x2(__byte_perm(t, 0x64646464u, 0x7362), kOne, kM1152);
 }
 
-// The same pairs as bf16x2 (exact: |b| <= 128 needs 8 significant bits):
-// each byte placed in the mantissa of 2^23 (as b + 128) and reduced by
-// 2^23 + 128 in f32, then packed.
+// The same pairs as bf16x2, exact: under the bf16 exponent byte 0x43 the
+// low seven bits m of a byte read 128 + m and its sign bit 128 or 256, and
+// b = (128 + m) - (128 + 128 * sign) is exact in bf16 (at most 8 bits).
 __device__ __forceinline__ void byte_pairs_bf16(uint32_t w, uint32_t (&r)[2]) {
-    const uint32_t t = w ^ 0x80808080u;
-    float f[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        f[j] = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7650 + j)) -
-               8388736.0f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
-    r[0] = *reinterpret_cast<const uint32_t *>(&lo);
-    r[1] = *reinterpret_cast<const uint32_t *>(&hi);
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t t = __byte_perm(w, 0x43434343u, j ? 0x4342 : 0x4140);
+        const uint32_t m = t & 0x437F437Fu, c = t & 0x43804380u;
+        const __nv_bfloat162 d =
+            __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&m),
+                    *reinterpret_cast<const __nv_bfloat162 *>(&c));
+        r[j] = *reinterpret_cast<const uint32_t *>(&d);
+    }
 }
 
 // One Q8 K step: w[0..3] = 16 bytes (16 K) of gate row g, up row g, gate
