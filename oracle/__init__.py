@@ -86,6 +86,18 @@ def _load():
         lib.q4o_q8_down_proj.argtypes = [
             _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
             _INT]
+        lib.q4o_trellis_gate_up_swiglu.restype = _INT
+        lib.q4o_trellis_gate_up_swiglu.argtypes = [
+            _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _INT, _INT, _INT,
+            _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT]
+        lib.q4o_trellis_y.restype = _INT
+        lib.q4o_trellis_y.argtypes = [ctypes.c_uint32]
+        lib.q4o_trellis_scale.restype = ctypes.c_float
+        lib.q4o_trellis_scale.argtypes = [ctypes.c_uint16]
+        lib.q4o_trellis_block_codes.restype = _INT
+        lib.q4o_trellis_block_codes.argtypes = [_P, _I64, _INT, _INT, _P]
+        lib.q4o_trellis_block_states.restype = _INT
+        lib.q4o_trellis_block_states.argtypes = [_P, _I64, _INT, _INT, _P]
         lib.q4o_group_rows.restype = _INT
         lib.q4o_group_rows.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
         lib.q4o_max_threads.restype = _INT
@@ -341,6 +353,65 @@ def q8_down_proj(mid_bits, down_w, down_s, row_offsets, rows=None,
         None if r is None else _ptr(r), None if c is None else _ptr(c),
         _ptr(res["out"]), _ptr(res["out32"]), _ptr(res["dabs"]),
         int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return res
+
+
+def trellis_y(state: int) -> int:
+    """Code value of one trellis state (page 54, codebook.ts)."""
+    return int(_load().q4o_trellis_y(int(state) & 0xFFFFFFFF))
+
+
+def trellis_scale(scale_f16_bits: int) -> float:
+    """The factored row scale RN32(scale * RN32(1/147.800537109375))."""
+    return float(_load().q4o_trellis_scale(int(scale_f16_bits)))
+
+
+def trellis_block(words, Tb: int, k: int, L: int):
+    """(states, code values) of the Tb weights of one block of words."""
+    w = _c(words, np.uint32)
+    st = np.zeros(Tb, np.uint32)
+    y = np.zeros(Tb, np.int32)
+    lib = _load()
+    if (lib.q4o_trellis_block_states(_ptr(w), Tb, k, L, _ptr(st)) != 0 or
+            lib.q4o_trellis_block_codes(_ptr(w), Tb, k, L, _ptr(y)) != 0):
+        raise ValueError("oracle rejected the block geometry")
+    return st, y
+
+
+def trellis_gate_up_swiglu(x_bits, gate_codes, up_codes, gate_s_f16,
+                           up_s_f16, kg: int, ku: int, L: int, Tb: int,
+                           row_offsets, token_of_row, rows=None, cols=None,
+                           nthreads: int = 0):
+    """Trellis gate/up + SwiGLU with factored row scales (page 57,
+    gate-up-mma.ts / mixed-gate-up-factored.ts arithmetic, page 52 tail).
+    gate_codes uint32 [E, I, words], up_codes likewise (widths kg, ku);
+    scales f16 bit patterns [E, I].  All M x I outputs or the (rows, cols)
+    elements; a dict with out, gate32, up32, gabs, uabs."""
+    x = _c(x_bits, np.uint16)
+    gc, uc = _c(gate_codes, np.uint32), _c(up_codes, np.uint32)
+    gs, us = _c(gate_s_f16, np.uint16), _c(up_s_f16, np.uint16)
+    offs, tok = _c(row_offsets, np.int32), _c(token_of_row, np.int32)
+    T, H = x.shape
+    E, I, _ = gc.shape
+    M = tok.shape[0]
+    if rows is None:
+        shape, n, r, c = (M, I), M * I, None, None
+    else:
+        r, c = _c(rows, np.int64), _c(cols, np.int64)
+        shape, n = (r.shape[0],), r.shape[0]
+    res = dict(out=np.zeros(shape, np.uint16),
+               gate32=np.zeros(shape, np.float32),
+               up32=np.zeros(shape, np.float32),
+               gabs=np.zeros(shape, np.float64),
+               uabs=np.zeros(shape, np.float64))
+    rc = _load().q4o_trellis_gate_up_swiglu(
+        _ptr(x), T, H, I, E, _ptr(gc), _ptr(uc), _ptr(gs), _ptr(us),
+        int(kg), int(ku), int(L), int(Tb), _ptr(offs), _ptr(tok), M, n,
+        None if r is None else _ptr(r), None if c is None else _ptr(c),
+        _ptr(res["out"]), _ptr(res["gate32"]), _ptr(res["up32"]),
+        _ptr(res["gabs"]), _ptr(res["uabs"]), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return res

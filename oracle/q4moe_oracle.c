@@ -22,6 +22,12 @@
  *  - page 52, Q8_GATE_UP_SOURCE and Q8_DOWN_SOURCE: the same two
  *    operations on signed int8 weights (one byte per weight, row-major, the
  *    byte's two's-complement value, no zero point);
+ *  - page 57 (trellis/gate-up-mma.ts, mixed-gate-up-factored.ts) and page
+ *    54 (trellis/codebook.ts): the trellis (QTIP 1MAD) gate/up with the row
+ *    scale factored out of the sum: code value y of state s is the byte sum
+ *    of s * 34038481 + 76625530 (mod 2^32) minus 510, the state of weight t
+ *    of a block is the L-bit window at bit (T - 1 - t) * k of the block's
+ *    bits (wrapping), and gate = (sum_k y_k x_k) * (scale * (1/147.800537109375));
  *  - page 51, src/kernels/glm52/layout.ts: the per-expert section layout
  *    (the oracle takes the sections as separate arrays, so it never parses
  *    a slab).
@@ -494,6 +500,171 @@ int q4o_q8_down_proj(const uint16_t *mid, int64_t M, int64_t I, int64_t H,
         if (dabs) dabs[j] = a;
     }
     (void)nthreads;
+    return 0;
+}
+
+/* ---- trellis (QTIP 1MAD) gate/up, factored row scale ---------------------
+ * Codes of one row: H / Tb blocks of Tb * k / 32 words each (axis 1: coded
+ * along the input); bit b of a block is bit b % 32 of word b / 32.  Scales
+ * are f16 bit patterns, one per row. */
+
+/* The L-bit state of weight t of a block of nbits = Tb * k bits: the bits
+ * [p, p + L) with p = (Tb - 1 - t) * k, taken modulo nbits (page 54,
+ * codebook.ts, trellis_state). */
+static uint32_t q4o_trellis_state(const uint32_t *blk, int64_t nbits,
+                                  int64_t t, int64_t Tb, int k, int L)
+{
+    const int64_t p = (Tb - 1 - t) * k;
+    uint32_t s = 0;
+    for (int j = 0; j < L; ++j) {
+        const int64_t b = (p + j) % nbits;
+        s |= ((blk[b >> 5] >> (b & 31)) & 1u) << j;
+    }
+    return s;
+}
+
+/* Code value of state s (page 54, codebook.ts, trellis_y): the sum of the
+ * four bytes of s * 34038481 + 76625530 (mod 2^32), minus 510. */
+int q4o_trellis_y(uint32_t s)
+{
+    const uint32_t x = s * 34038481u + 76625530u;
+    return (int)(x & 255u) + (int)((x >> 8) & 255u) + (int)((x >> 16) & 255u) +
+           (int)(x >> 24) - 510;
+}
+
+/* f16 bits -> f32 (exact). */
+static float q4o_f16_to_f32(uint16_t h)
+{
+    const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return (float)(sign ? -v : v);
+}
+
+/* The factored scale of a row: RN32(s * RN32(1 / 147.800537109375)) (page
+ * 57, gate-up-mma.ts: float(scale) * TRELLIS_RCP). */
+float q4o_trellis_scale(uint16_t s_f16)
+{
+    const float rcp = (float)(1.0 / 147.800537109375);
+    return (float)((double)q4o_f16_to_f32(s_f16) * (double)rcp);
+}
+
+/* sum_k y_k x_k over one row (f64: exact), and sum_k |y_k x_k|. */
+static double q4o_trellis_dot(const uint32_t *row, const uint16_t *xrow,
+                              int64_t H, int64_t Tb, int k, int L,
+                              double *absdot)
+{
+    const int64_t wpb = Tb * k / 32, nbits = Tb * k;
+    double s = 0.0, a = 0.0;
+    for (int64_t c = 0; c < H; ++c) {
+        const int64_t blk = c / Tb, t = c % Tb;
+        const int y = q4o_trellis_y(
+            q4o_trellis_state(row + blk * wpb, nbits, t, Tb, k, L));
+        const double prod = (double)y * (double)q4o_bf16_to_f32(xrow[c]);
+        s += prod;
+        a += fabs(prod);
+    }
+    *absdot = a;
+    return s;
+}
+
+/* All M x I outputs, or (rows != NULL) the n elements (rows[j], cols[j]).
+ * gate_codes: uint32 [E, I, H / Tb * Tb * kg / 32], up_codes likewise with
+ * ku; gate_s/up_s: f16 bits [E, I].  Outputs as q4o_gate_up_swiglu
+ * (gate32 = RN32(G * gate scale), the page 52 tail).  Needs H % Tb == 0,
+ * Tb * k % 32 == 0, 1 <= L <= 24, L <= Tb * k. */
+int q4o_trellis_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H,
+                               int64_t I, int32_t E,
+                               const uint32_t *gate_codes,
+                               const uint32_t *up_codes,
+                               const uint16_t *gate_s, const uint16_t *up_s,
+                               int kg, int ku, int L, int64_t Tb,
+                               const int32_t *row_offsets,
+                               const int32_t *token_of_row, int64_t M,
+                               int64_t n, const int64_t *rows,
+                               const int64_t *cols, uint16_t *out,
+                               float *gate32, float *up32, double *gabs,
+                               double *uabs, int nthreads)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || M < 0 || Tb <= 0 ||
+        H % Tb != 0 || kg < 1 || ku < 1 || kg > 8 || ku > 8 ||
+        (Tb * kg) % 32 != 0 || (Tb * ku) % 32 != 0 || L < 1 || L > 24 ||
+        L > Tb * kg || L > Tb * ku)
+        return -1;
+    if (row_offsets[0] != 0 || row_offsets[E] != M)
+        return -2;
+    for (int32_t e = 0; e < E; ++e)
+        if (row_offsets[e + 1] < row_offsets[e])
+            return -2;
+    for (int64_t p = 0; p < M; ++p)
+        if (token_of_row[p] < 0 || token_of_row[p] >= T)
+            return -3;
+    if (rows == 0)
+        n = M * I;
+    else
+        for (int64_t j = 0; j < n; ++j)
+            if (rows[j] < 0 || rows[j] >= M || cols[j] < 0 || cols[j] >= I)
+                return -4;
+    const int64_t gwords = H / Tb * (Tb * kg / 32);
+    const int64_t uwords = H / Tb * (Tb * ku / 32);
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = rows ? rows[j] : j / I, i = rows ? cols[j] : j % I;
+        const int32_t e = q4o_expert_of_row(row_offsets, E, p);
+        const uint16_t *xrow = x + (int64_t)token_of_row[p] * H;
+        double ga, ua;
+        const double G = q4o_trellis_dot(
+            gate_codes + ((int64_t)e * I + i) * gwords, xrow, H, Tb, kg, L,
+            &ga);
+        const double U = q4o_trellis_dot(
+            up_codes + ((int64_t)e * I + i) * uwords, xrow, H, Tb, ku, L,
+            &ua);
+        const float g32 = (float)(G * (double)q4o_trellis_scale(
+                                          gate_s[(int64_t)e * I + i]));
+        const float u32 = (float)(U * (double)q4o_trellis_scale(
+                                          up_s[(int64_t)e * I + i]));
+        uint16_t res[5];
+        q4o_tail(g32, u32, 0, res);
+        out[j] = res[4];
+        if (gate32) gate32[j] = g32;
+        if (up32) up32[j] = u32;
+        if (gabs) gabs[j] = ga;
+        if (uabs) uabs[j] = ua;
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* The code values of one block (debug/pin helper): y[t] for t < Tb. */
+int q4o_trellis_block_codes(const uint32_t *blk, int64_t Tb, int k, int L,
+                            int32_t *y)
+{
+    if (Tb <= 0 || k < 1 || (Tb * k) % 32 != 0 || L < 1 || L > 24 ||
+        L > Tb * k)
+        return -1;
+    for (int64_t t = 0; t < Tb; ++t)
+        y[t] = q4o_trellis_y(q4o_trellis_state(blk, Tb * k, t, Tb, k, L));
+    return 0;
+}
+
+/* The states of one block (pin helper). */
+int q4o_trellis_block_states(const uint32_t *blk, int64_t Tb, int k, int L,
+                             uint32_t *st)
+{
+    if (Tb <= 0 || k < 1 || (Tb * k) % 32 != 0 || L < 1 || L > 24 ||
+        L > Tb * k)
+        return -1;
+    for (int64_t t = 0; t < Tb; ++t)
+        st[t] = q4o_trellis_state(blk, Tb * k, t, Tb, k, L);
     return 0;
 }
 
