@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 5
+#define Q4MOE_ABI_VERSION 6
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -354,6 +354,80 @@ int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *expert_slabs,
                      const int32_t *token_to_expert_map, int64_t M, int64_t H,
                      int64_t I, void *mid, void *out,
                      const q4moe_options_t *opts, cudaStream_t stream);
+
+/*
+ * Trellis-coded experts (QTIP "1MAD" code; pages 57 and 54: trellis/
+ * gate-up-mma.ts, mixed-gate-up-factored.ts, codebook.ts), gate and up
+ * coded along the input (the pages' axis 1).  A row's H weights form H / T
+ * blocks of T weights at k bits each: T * k / 32 uint32 words per block,
+ * bit b of a block is bit b % 32 of word b / 32.  Weight t of a block has
+ * the state s = the L bits at (T - 1 - t) * k of the block, taken modulo
+ * T * k (wrapping), and the code value
+ *   y(s) = (sum of the four bytes of s * 34038481 + 76625530 mod 2^32) - 510.
+ * For grouped row p of expert e (token x[t]) and output row i:
+ *   G = sum_k y_k * x[t][k]                      (f32 accumulate)
+ *   gate32 = G * RN32(f32(gate_scale[i]) * RN32(1 / 147.800537109375))
+ * (the row scale factored out of the sum, as on the pages), up likewise
+ * with its own width, then the same SwiGLU tail as Q4.
+ */
+typedef struct q4moe_trellis_layout {
+    int64_t hidden_size;       /* H: a multiple of block_size                 */
+    int64_t intermediate_size; /* I > 0                                       */
+    int32_t block_size;        /* T: weights per block, a multiple of 32 (the
+                                  pages use 256)                              */
+    int32_t window_bits;       /* L: state bits, 1..24, L <= T * k (pages: 12) */
+    int32_t gate_bits;         /* k of gate, 1..8                             */
+    int32_t up_bits;           /* k of up, 1..8 (may differ from gate's)      */
+    int64_t slab_bytes;        /* bytes of one expert's slab                  */
+    int64_t gate_codes_offset; /* uint32 [I][H/T * T*k/32], 4-byte aligned     */
+    int64_t up_codes_offset;
+    int64_t gate_scales_offset; /* f16 [I], 2-byte aligned                     */
+    int64_t up_scales_offset;
+} q4moe_trellis_layout_t;
+
+/* Where trellis expert slabs live: as q4moe_slabs_t. */
+typedef struct q4moe_trellis_slabs {
+    int32_t num_experts; /* E: 1 .. Q4MOE_MAX_EXPERTS */
+    int32_t reserved0;   /* must be 0                 */
+    const void *base;
+    int64_t slab_stride;
+    const void *const *slab_ptrs;
+    q4moe_trellis_layout_t layout;
+} q4moe_trellis_slabs_t;
+
+/* Canonical trellis slab: gate codes at 0, up codes, gate scales, up scales,
+ * each section starting on a 256-byte boundary; size rounded up to
+ * Q4MOE_SLAB_ALIGNMENT.  Host only. */
+int q4moe_trellis_canonical_layout(int64_t H, int64_t I, int32_t block_size,
+                                   int32_t window_bits, int32_t gate_bits,
+                                   int32_t up_bits,
+                                   q4moe_trellis_layout_t *layout);
+
+/* Copy one expert's trellis sections into a host slab buffer (zeroing the
+ * rest).  gate_codes/up_codes: host uint32 rows as described above;
+ * gate_scales/up_scales: host f16 bit patterns [I].  Host only. */
+int q4moe_trellis_pack_slab(const q4moe_trellis_layout_t *layout,
+                            const uint32_t *gate_codes,
+                            const uint32_t *up_codes,
+                            const uint16_t *gate_scales,
+                            const uint16_t *up_scales, void *slab_host);
+
+/*
+ * The fused trellis gate/up + SwiGLU over grouped rows (formula above).
+ * Arguments as q4moe_gate_up_swiglu_ex: x device bf16 [T][H] (16-byte
+ * aligned), row offsets and the token map on the device, out device bf16
+ * [M][I].  opts may be NULL; num_tokens, gate_f32 and up_f32 as for Q4;
+ * kernel, matvec_tile and workspace must be 0.  One kernel (a warp per
+ * output row, each decoded weight serving up to 8 grouped rows); decoding
+ * is integer arithmetic, so the kernel is bound by the integer pipe.
+ */
+int q4moe_trellis_gate_up_swiglu(const void *x,
+                                 const q4moe_trellis_slabs_t *expert_slabs,
+                                 const int32_t *row_offsets_per_expert,
+                                 const int32_t *token_to_expert_map,
+                                 int64_t M, int64_t H, int64_t I, void *out,
+                                 const q4moe_options_t *opts,
+                                 cudaStream_t stream);
 
 /*
  * Wait for `stream`, then read the current device's status word into

@@ -192,6 +192,71 @@ int validate_layout(const q4moe_layout_t *L) {
     return Q4MOE_OK;
 }
 
+// Slab placement (base + e * stride or a pointer table), shared by the Q4/Q8
+// and trellis slab descriptors.
+int check_placement(int32_t num_experts, int32_t reserved0, const void *base,
+                    int64_t stride, const void *const *ptrs,
+                    int64_t slab_bytes) {
+    if (num_experts <= 0 || num_experts > Q4MOE_MAX_EXPERTS)
+        return fail(Q4MOE_ERR_INVALID_ARG, "num_experts must be in 1..%d",
+                    Q4MOE_MAX_EXPERTS);
+    if (reserved0 != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "reserved field must be 0");
+    if (ptrs == nullptr) {
+        if (base == nullptr)
+            return fail(Q4MOE_ERR_INVALID_ARG,
+                        "slab base is null and no pointer table given");
+        if (!aligned(base, Q4MOE_SLAB_ALIGNMENT))
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab base must be %d-byte aligned",
+                        Q4MOE_SLAB_ALIGNMENT);
+        if (stride % Q4MOE_SLAB_ALIGNMENT != 0 ||
+            (num_experts > 1 && stride < slab_bytes) || stride < 0)
+            return fail(Q4MOE_ERR_ALIGNMENT,
+                        "slab stride must be a multiple of %d and at least "
+                        "the slab size", Q4MOE_SLAB_ALIGNMENT);
+    } else if (!aligned(ptrs, 8)) {
+        return fail(Q4MOE_ERR_ALIGNMENT, "slab pointer table misaligned");
+    }
+    return Q4MOE_OK;
+}
+
+// Trellis layout: geometry and section ranges.
+int validate_trellis_layout(const q4moe_trellis_layout_t *L) {
+    if (L == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
+    const int64_t H = L->hidden_size, I = L->intermediate_size;
+    const int64_t T = L->block_size;
+    if (H <= 0 || I <= 0 || T <= 0 || T % 32 != 0 || H % T != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "need H, I > 0, block size a multiple of 32 dividing H");
+    if (H > (INT64_C(1) << 24) || I > (INT64_C(1) << 24) || T > 65536)
+        return fail(Q4MOE_ERR_INVALID_ARG, "dimensions too large");
+    if (L->gate_bits < 1 || L->gate_bits > 8 || L->up_bits < 1 ||
+        L->up_bits > 8)
+        return fail(Q4MOE_ERR_INVALID_ARG, "code widths must be 1..8 bits");
+    if (L->window_bits < 1 || L->window_bits > 24 ||
+        L->window_bits > T * L->gate_bits || L->window_bits > T * L->up_bits)
+        return fail(Q4MOE_ERR_INVALID_ARG, "window bits must be 1..24");
+    if (L->slab_bytes <= 0)
+        return fail(Q4MOE_ERR_INVALID_ARG, "slab bytes must be positive");
+    int rc;
+    if ((rc = check_range(L->gate_codes_offset, I * H * L->gate_bits / 8,
+                          L->slab_bytes, "gate codes")) ||
+        (rc = check_range(L->up_codes_offset, I * H * L->up_bits / 8,
+                          L->slab_bytes, "up codes")) ||
+        (rc = check_range(L->gate_scales_offset, I * 2, L->slab_bytes,
+                          "gate scales")) ||
+        (rc = check_range(L->up_scales_offset, I * 2, L->slab_bytes,
+                          "up scales")))
+        return rc;
+    if ((L->gate_codes_offset | L->up_codes_offset) % 4 != 0 ||
+        (L->gate_scales_offset | L->up_scales_offset) % 2 != 0)
+        return fail(Q4MOE_ERR_ALIGNMENT,
+                    "codes must start on 4-byte, scales on 2-byte boundaries");
+    return Q4MOE_OK;
+}
+
 // Checks of the slab placement and the call's dimensions shared by every
 // call that reads expert slabs.
 int check_slabs(const q4moe_slabs_t *slabs, int64_t H, int64_t I,
@@ -208,32 +273,14 @@ int check_slabs(const q4moe_slabs_t *slabs, int64_t H, int64_t I,
                     "(%lld, %lld)", (long long)H, (long long)I,
                     (long long)L.hidden_size,
                     (long long)L.intermediate_size);
-    if (slabs->num_experts <= 0 || slabs->num_experts > Q4MOE_MAX_EXPERTS)
-        return fail(Q4MOE_ERR_INVALID_ARG, "num_experts must be in 1..%d",
-                    Q4MOE_MAX_EXPERTS);
-    if (slabs->reserved0 != 0)
-        return fail(Q4MOE_ERR_INVALID_ARG, "reserved field must be 0");
+    if ((rc = check_placement(slabs->num_experts, slabs->reserved0,
+                              slabs->base, slabs->slab_stride,
+                              slabs->slab_ptrs, L.slab_bytes)))
+        return rc;
     if (M < 0 || M > INT32_MAX)
         return fail(Q4MOE_ERR_INVALID_ARG, "M must be in 0..2^31-1");
     if (M > 0 && M * std::max(H, I) > (INT64_C(1) << 40))
         return fail(Q4MOE_ERR_INVALID_ARG, "output too large");
-    if (slabs->slab_ptrs == nullptr) {
-        if (slabs->base == nullptr)
-            return fail(Q4MOE_ERR_INVALID_ARG,
-                        "slab base is null and no pointer table given");
-        if (!aligned(slabs->base, Q4MOE_SLAB_ALIGNMENT))
-            return fail(Q4MOE_ERR_ALIGNMENT,
-                        "slab base must be %d-byte aligned",
-                        Q4MOE_SLAB_ALIGNMENT);
-        if (slabs->slab_stride % Q4MOE_SLAB_ALIGNMENT != 0 ||
-            (slabs->num_experts > 1 && slabs->slab_stride < L.slab_bytes) ||
-            slabs->slab_stride < 0)
-            return fail(Q4MOE_ERR_ALIGNMENT,
-                        "slab stride must be a multiple of %d and at least "
-                        "the slab size", Q4MOE_SLAB_ALIGNMENT);
-    } else if (!aligned(slabs->slab_ptrs, 8)) {
-        return fail(Q4MOE_ERR_ALIGNMENT, "slab pointer table misaligned");
-    }
     return Q4MOE_OK;
 }
 
@@ -448,6 +495,140 @@ int q4moe_pack_slab_down(const q4moe_layout_t *L, const uint32_t *down_w,
            (size_t)(L->weight_format == Q4MOE_FORMAT_Q8 ? H * I
                                                         : H * (I / 2)));
     memcpy(s + L->down_s_offset, down_s, (size_t)(H * 4));
+    return ok();
+}
+
+int q4moe_trellis_canonical_layout(int64_t H, int64_t I, int32_t block_size,
+                                   int32_t window_bits, int32_t gate_bits,
+                                   int32_t up_bits,
+                                   q4moe_trellis_layout_t *layout) {
+    if (layout == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "layout is null");
+    q4moe_trellis_layout_t L{};
+    L.hidden_size = H;
+    L.intermediate_size = I;
+    L.block_size = block_size;
+    L.window_bits = window_bits;
+    L.gate_bits = gate_bits;
+    L.up_bits = up_bits;
+    L.slab_bytes = 1;
+    // the geometry checks of validate_trellis_layout, before any size
+    if (H <= 0 || I <= 0 || block_size <= 0 || block_size % 32 != 0 ||
+        H % block_size != 0 || H > (INT64_C(1) << 24) ||
+        I > (INT64_C(1) << 24) || gate_bits < 1 || gate_bits > 8 ||
+        up_bits < 1 || up_bits > 8)
+        return fail(Q4MOE_ERR_INVALID_ARG, "bad trellis geometry");
+    auto up256 = [](int64_t v) { return (v + 255) / 256 * 256; };
+    L.gate_codes_offset = 0;
+    L.up_codes_offset = up256(I * H * gate_bits / 8);
+    L.gate_scales_offset = up256(L.up_codes_offset + I * H * up_bits / 8);
+    L.up_scales_offset = up256(L.gate_scales_offset + 2 * I);
+    const int64_t used = L.up_scales_offset + 2 * I;
+    L.slab_bytes = (used + Q4MOE_SLAB_ALIGNMENT - 1) / Q4MOE_SLAB_ALIGNMENT *
+                   Q4MOE_SLAB_ALIGNMENT;
+    const int rc = validate_trellis_layout(&L);
+    if (rc)
+        return rc;
+    *layout = L;
+    return ok();
+}
+
+int q4moe_trellis_pack_slab(const q4moe_trellis_layout_t *L,
+                            const uint32_t *gate_codes,
+                            const uint32_t *up_codes,
+                            const uint16_t *gate_scales,
+                            const uint16_t *up_scales, void *slab_host) {
+    int rc = validate_trellis_layout(L);
+    if (rc)
+        return rc;
+    if (!gate_codes || !up_codes || !gate_scales || !up_scales || !slab_host)
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    const int64_t H = L->hidden_size, I = L->intermediate_size;
+    uint8_t *s = static_cast<uint8_t *>(slab_host);
+    memset(s, 0, (size_t)L->slab_bytes);
+    memcpy(s + L->gate_codes_offset, gate_codes,
+           (size_t)(I * H * L->gate_bits / 8));
+    memcpy(s + L->up_codes_offset, up_codes, (size_t)(I * H * L->up_bits / 8));
+    memcpy(s + L->gate_scales_offset, gate_scales, (size_t)(2 * I));
+    memcpy(s + L->up_scales_offset, up_scales, (size_t)(2 * I));
+    return ok();
+}
+
+int q4moe_trellis_gate_up_swiglu(const void *x,
+                                 const q4moe_trellis_slabs_t *slabs,
+                                 const int32_t *row_offsets,
+                                 const int32_t *token_of_row, int64_t M,
+                                 int64_t H, int64_t I, void *out,
+                                 const q4moe_options_t *opts,
+                                 cudaStream_t stream) {
+    if (slabs == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "expert_slabs is null");
+    int rc = validate_trellis_layout(&slabs->layout);
+    if (rc)
+        return rc;
+    const q4moe_trellis_layout_t &L = slabs->layout;
+    if (H != L.hidden_size || I != L.intermediate_size)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "H, I differ from the trellis layout's");
+    if ((rc = check_placement(slabs->num_experts, slabs->reserved0,
+                              slabs->base, slabs->slab_stride,
+                              slabs->slab_ptrs, L.slab_bytes)))
+        return rc;
+    if (M < 0 || M > INT32_MAX || (M > 0 && M * I > (INT64_C(1) << 40)))
+        return fail(Q4MOE_ERR_INVALID_ARG, "M out of range");
+    if (row_offsets == nullptr)
+        return fail(Q4MOE_ERR_INVALID_ARG, "row_offsets_per_expert is null");
+    if (M > 0 && (x == nullptr || token_of_row == nullptr || out == nullptr))
+        return fail(Q4MOE_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(x, 16))
+        return fail(Q4MOE_ERR_ALIGNMENT, "x must be 16-byte aligned");
+    if (!aligned(out, 2))
+        return fail(Q4MOE_ERR_ALIGNMENT, "out must be 2-byte aligned");
+    q4moe_options_t o{};
+    if (opts != nullptr)
+        o = *opts;
+    if ((rc = check_kernel_options(o)))
+        return rc;
+    if (o.kernel != Q4MOE_KERNEL_AUTO || o.matvec_tile != 0 ||
+        o.workspace != nullptr || o.workspace_bytes != 0)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "trellis calls take no kernel choice, tile or workspace");
+    DeviceInfo *d = nullptr;
+    rc = device_info(&d);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return ok();
+    q4moe::GateUpArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.base = static_cast<const uint8_t *>(slabs->base);
+    a.stride = slabs->slab_stride;
+    a.slab_ptrs = reinterpret_cast<const uint8_t *const *>(slabs->slab_ptrs);
+    a.gate_w_off = L.gate_codes_offset;
+    a.up_w_off = L.up_codes_offset;
+    a.gate_s_off = L.gate_scales_offset;
+    a.up_s_off = L.up_scales_offset;
+    a.row_offsets = row_offsets;
+    a.token_of_row = token_of_row;
+    a.M = M;
+    a.H = H;
+    a.I = I;
+    a.T = o.num_tokens;
+    a.E = slabs->num_experts;
+    a.out = static_cast<uint16_t *>(out);
+    a.gate_f32 = o.gate_f32;
+    a.up_f32 = o.up_f32;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
+    a.sigmoid = d->sigmoid;
+    a.tr_block = L.block_size;
+    a.tr_window = L.window_bits;
+    a.tr_kg = L.gate_bits;
+    a.tr_ku = L.up_bits;
+    a.matvec_max_rows = INT32_MAX;
+    const cudaError_t err = q4moe::launch_trellis_gate_up(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "trellis launch");
     return ok();
 }
 

@@ -45,6 +45,9 @@ struct GateUpArgs {
     int32_t down;                // 1: the down projection (above)
     int32_t invariant;           // 1: batch-invariant matvec versions only
     int32_t q8;                  // 1: signed-byte weights (rows of H bytes)
+    // trellis experts: block size, window bits, gate and up widths (the
+    // gate/up word and scale offsets then name codes and f16 scales)
+    int32_t tr_block, tr_window, tr_kg, tr_ku;
 };
 
 // Bytes of one weight row of K values.
@@ -99,6 +102,7 @@ cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
 bool matvec_tma_supported(const GateUpArgs &a);
 cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
+cudaError_t launch_trellis_gate_up(const GateUpArgs &a, cudaStream_t s);
 // GEMM tiles over the output rows of one expert's 256 grouped rows: 128
 // intermediate rows (gate and up) per tile, or 256 output rows (two halves
 // of 128) for the down projection.

@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 5
+ABI_VERSION = 6
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -47,6 +47,8 @@ EXPORTS = (
     "q4moe_debug_tail", "q4moe_launch_count", "q4moe_workspace_bytes",
     "q4moe_gate_up_swiglu_noalloc", "q4moe_pack_slab_down",
     "q4moe_down_proj", "q4moe_expert_mlp", "q4moe_canonical_layout_format",
+    "q4moe_trellis_canonical_layout", "q4moe_trellis_pack_slab",
+    "q4moe_trellis_gate_up_swiglu",
 )
 
 # Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
@@ -79,6 +81,29 @@ class q4moe_slabs_t(ctypes.Structure):
                 ("slab_stride", ctypes.c_int64),
                 ("slab_ptrs", ctypes.c_void_p),
                 ("layout", q4moe_layout_t)]
+
+
+class q4moe_trellis_layout_t(ctypes.Structure):
+    _fields_ = [("hidden_size", ctypes.c_int64),
+                ("intermediate_size", ctypes.c_int64),
+                ("block_size", ctypes.c_int32),
+                ("window_bits", ctypes.c_int32),
+                ("gate_bits", ctypes.c_int32),
+                ("up_bits", ctypes.c_int32),
+                ("slab_bytes", ctypes.c_int64),
+                ("gate_codes_offset", ctypes.c_int64),
+                ("up_codes_offset", ctypes.c_int64),
+                ("gate_scales_offset", ctypes.c_int64),
+                ("up_scales_offset", ctypes.c_int64)]
+
+
+class q4moe_trellis_slabs_t(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32),
+                ("base", ctypes.c_void_p),
+                ("slab_stride", ctypes.c_int64),
+                ("slab_ptrs", ctypes.c_void_p),
+                ("layout", q4moe_trellis_layout_t)]
 
 
 class q4moe_options_t(ctypes.Structure):
@@ -142,6 +167,13 @@ def load(build_if_missing: bool = True):
                                              [_P, _P, _P, _P, _I64, _I64,
                                               _I64, _P, _P]),
             "q4moe_pack_slab_down": (ctypes.c_int, [_P, _P, _P, _P]),
+            "q4moe_trellis_canonical_layout": (
+                ctypes.c_int, [_I64, _I64, _I32, _I32, _I32, _I32, _P]),
+            "q4moe_trellis_pack_slab": (ctypes.c_int,
+                                        [_P, _P, _P, _P, _P, _P]),
+            "q4moe_trellis_gate_up_swiglu": (
+                ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P,
+                               _P]),
             "q4moe_down_proj": (ctypes.c_int,
                                 [_P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
             "q4moe_expert_mlp": (ctypes.c_int,
@@ -222,6 +254,30 @@ def q4moe_pack_slab(layout, gate_w, up_w, gate_s, up_s, slab_host) -> None:
 def q4moe_pack_slab_down(layout, down_w, down_s, slab_host) -> None:
     _check(load().q4moe_pack_slab_down(ctypes.byref(layout), _ptr(down_w),
                                        _ptr(down_s), _ptr(slab_host)))
+
+
+def q4moe_trellis_canonical_layout(H, I, block_size, window_bits, gate_bits,
+                                   up_bits) -> q4moe_trellis_layout_t:
+    L = q4moe_trellis_layout_t()
+    _check(load().q4moe_trellis_canonical_layout(
+        H, I, block_size, window_bits, gate_bits, up_bits, ctypes.byref(L)))
+    return L
+
+
+def q4moe_trellis_pack_slab(layout, gate_codes, up_codes, gate_scales,
+                            up_scales, slab_host) -> None:
+    _check(load().q4moe_trellis_pack_slab(
+        ctypes.byref(layout), _ptr(gate_codes), _ptr(up_codes),
+        _ptr(gate_scales), _ptr(up_scales), _ptr(slab_host)))
+
+
+def q4moe_trellis_gate_up_swiglu(x, expert_slabs, row_offsets_per_expert,
+                                 token_to_expert_map, M, H, I, out, opts=None,
+                                 stream=None) -> None:
+    _check(load().q4moe_trellis_gate_up_swiglu(
+        _ptr(x), ctypes.byref(expert_slabs), _ptr(row_offsets_per_expert),
+        _ptr(token_to_expert_map), M, H, I, _ptr(out),
+        None if opts is None else ctypes.byref(opts), _stream(stream)))
 
 
 def q4moe_group_rows(topk_ids, T, k, E, row_offsets, token_of_row,
@@ -316,6 +372,34 @@ def make_slabs(num_experts: int, layout: q4moe_layout_t, base=None,
     s.slab_ptrs = _ptr(slab_ptrs)
     s.layout = layout
     return s
+
+
+def make_trellis_slabs(num_experts: int, layout: q4moe_trellis_layout_t,
+                       base=None, slab_stride: int | None = None,
+                       slab_ptrs=None) -> q4moe_trellis_slabs_t:
+    s = q4moe_trellis_slabs_t()
+    s.num_experts = num_experts
+    s.reserved0 = 0
+    s.base = _ptr(base)
+    s.slab_stride = layout.slab_bytes if slab_stride is None else slab_stride
+    s.slab_ptrs = _ptr(slab_ptrs)
+    s.layout = layout
+    return s
+
+
+def pack_trellis_pool(layout: q4moe_trellis_layout_t, gate_codes, up_codes,
+                      gate_scales, up_scales):
+    """Host uint8 array [E, slab_bytes] of trellis slabs (codes uint32
+    [E, I, words], f16 scale bit patterns [E, I])."""
+    import numpy as np
+    E = gate_codes.shape[0]
+    pool = np.empty((E, layout.slab_bytes), dtype=np.uint8)
+    for e in range(E):
+        q4moe_trellis_pack_slab(layout, np.ascontiguousarray(gate_codes[e]),
+                                np.ascontiguousarray(up_codes[e]),
+                                np.ascontiguousarray(gate_scales[e]),
+                                np.ascontiguousarray(up_scales[e]), pool[e])
+    return pool
 
 
 def pack_slab_pool(layout: q4moe_layout_t, gate_w, up_w, gate_s, up_s,
