@@ -49,6 +49,8 @@ OP_METRIC = {
 
 def op_metric(op: str, fmt: str) -> str:
     m = OP_METRIC[op]
+    if fmt.startswith("trellis"):
+        return m.replace("Q4", "trellis-coded")
     return m.replace("Q4", "Q8") if fmt == "q8" else m
 
 
@@ -68,9 +70,12 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(syn.WORKLOADS))
-    ap.add_argument("--format", default="q4", choices=["q4", "q8"],
-                    help="weight format: packed nibbles (q4) or signed "
-                         "bytes (q8)")
+    ap.add_argument("--format", default="q4",
+                    choices=["q4", "q8", "trellis"],
+                    help="weight format: packed nibbles (q4), signed bytes "
+                         "(q8) or trellis codes (gate/up only)")
+    ap.add_argument("--trellis-bits", default="4,4",
+                    help="gate,up code widths of the trellis format")
     ap.add_argument("--op", default="gate_up",
                     choices=["gate_up", "down", "mlp"],
                     help="the gate/up call (default), the down projection, "
@@ -101,6 +106,9 @@ def workload_units(w: syn.Workload, topk: np.ndarray, E_pool: int,
     back.  Q8: one byte per weight instead of half a byte."""
     per_byte = 1 if fmt == "q8" else 2           # weights per byte
     gu = w.I * (2 * w.H // per_byte + 8)
+    if fmt.startswith("trellis"):                # trellis:kg,ku
+        kg, ku = (int(v) for v in fmt.split(":")[1].split(","))
+        gu = w.I * (w.H * (kg + ku) // 8 + 4)
     dn = w.H * (w.I // per_byte + 4)
     per_expert = {"gate_up": gu, "down": dn, "mlp": gu + dn}[op]
     rows = w.routed_rows
@@ -235,8 +243,13 @@ class GpuWorkload:
                        "invariant": q.KERNEL_BATCH_INVARIANT}[kernel]
         self.dev = torch.device("cuda", device)
         self.stream = torch.cuda.current_stream(self.dev)
-        L = q.q4moe_canonical_layout_format(
-            w.H, w.I, q.FORMAT_Q8 if fmt == "q8" else q.FORMAT_Q4)
+        self.trellis = fmt.startswith("trellis")
+        if self.trellis:
+            kg, ku = (int(v) for v in fmt.split(":")[1].split(","))
+            L = q.q4moe_trellis_canonical_layout(w.H, w.I, 256, 12, kg, ku)
+        else:
+            L = q.q4moe_canonical_layout_format(
+                w.H, w.I, q.FORMAT_Q8 if fmt == "q8" else q.FORMAT_Q4)
         self.layout = L
         if w.repeats > 1:
             # distinct expert slabs, more than 4x L2 in total
@@ -245,14 +258,22 @@ class GpuWorkload:
         else:
             pool_experts = w.E
         self.pool_experts = pool_experts
-        g = syn.generate(w, experts=pool_experts, fmt=fmt)
-        if op != "gate_up":
-            g.update(syn.generate_down(w, experts=pool_experts, fmt=fmt))
+        if self.trellis:
+            g = syn.generate(w, experts=1)
+            (g["gate_w"], g["up_w"], g["gate_s"],
+             g["up_s"]) = syn.trellis_weights(w.seed, pool_experts, w.I, w.H,
+                                              L.gate_bits, L.up_bits)
+            host_pool = q.pack_trellis_pool(L, g["gate_w"], g["up_w"],
+                                            g["gate_s"], g["up_s"])
+        else:
+            g = syn.generate(w, experts=pool_experts, fmt=fmt)
+            if op != "gate_up":
+                g.update(syn.generate_down(w, experts=pool_experts, fmt=fmt))
+            host_pool = q.pack_slab_pool(L, g["gate_w"], g["up_w"],
+                                         g["gate_s"], g["up_s"],
+                                         g.get("down_w"), g.get("down_s"))
         self.host = g
         self.topk_host = g["topk"]
-        host_pool = q.pack_slab_pool(L, g["gate_w"], g["up_w"], g["gate_s"],
-                                     g["up_s"], g.get("down_w"),
-                                     g.get("down_s"))
         nbytes = host_pool.size
         self._buf = torch.empty(nbytes + 4096, dtype=torch.uint8,
                                 device=self.dev)
@@ -279,18 +300,22 @@ class GpuWorkload:
             # single expert, single row: the grouping is the identity
             self.offs.copy_(torch.tensor([0, self.M], dtype=torch.int32))
             self.tok.zero_()
-            self.slabs = [q.make_slabs(1, L, base=self.pool.data_ptr() +
-                                       (r % pool_experts) * L.slab_bytes)
+            mk = q.make_trellis_slabs if self.trellis else q.make_slabs
+            self.slabs = [mk(1, L, base=self.pool.data_ptr() +
+                             (r % pool_experts) * L.slab_bytes)
                           for r in range(self.calls)]
         else:
-            self.slabs = [q.make_slabs(w.E, L, base=self.pool)]
+            mk = q.make_trellis_slabs if self.trellis else q.make_slabs
+            self.slabs = [mk(w.E, L, base=self.pool)]
         self.opts = q.q4moe_options_t()
         self.opts.kernel = self.kernel
         self.opts.matvec_tile = matvec_tile
         self.opts_down = q.q4moe_options_t()
         self.opts_down.kernel = self.kernel
         self.opts_down.matvec_tile = matvec_tile
-        if use_workspace and op != "down":
+        if self.trellis:
+            self.opts = q.q4moe_options_t()     # no kernel choice, no scratch
+        elif use_workspace and op != "down":
             # scratch for the grouped activations the tensor-core GEMM reads
             nbytes = q.q4moe_workspace_bytes(self.M, w.H)
             self._ws = torch.empty(nbytes + 256, dtype=torch.uint8,
@@ -306,7 +331,11 @@ class GpuWorkload:
         point for the measured operation."""
         q, w = self.q, self.w
         out = self.out.data_ptr() + r * self.M * self.out_cols * 2
-        if self.op == "gate_up":
+        if self.trellis:
+            q.q4moe_trellis_gate_up_swiglu(self.x, self.slabs[r], self.offs,
+                                           self.tok, self.M, w.H, w.I, out,
+                                           self.opts, self.stream)
+        elif self.op == "gate_up":
             q.q4moe_gate_up_swiglu_ex(self.x, self.slabs[r], self.offs,
                                       self.tok, self.M, w.H, w.I, out,
                                       self.opts, self.stream)
@@ -392,7 +421,13 @@ def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0,
         rh = np.repeat(rows, w.H)
         ch = np.tile(np.arange(w.H), rows.size)
         t0 = time.perf_counter()
-        if op in ("gate_up", "mlp"):
+        if fmt.startswith("trellis"):
+            kg, ku = (int(v) for v in fmt.split(":")[1].split(","))
+            r = oracle.trellis_gate_up_swiglu(
+                g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
+                g["up_s"][:Ew], kg, ku, 12, 256, offs, tok, rr, cols,
+                nthreads=nthreads)
+        elif op in ("gate_up", "mlp"):
             gu = oracle.q8_gate_up_swiglu if fmt == "q8" else \
                 oracle.gate_up_swiglu_sampled
             r = gu(g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
@@ -450,7 +485,15 @@ def run_reference(args, w, rank, world):
         return 0
     op = args.op
     fmt = args.format
-    g = syn.generate(w, experts=w.E if w.repeats == 1 else 1, fmt=fmt)
+    if fmt == "trellis":
+        fmt = f"trellis:{args.trellis_bits}"
+        kg, ku = (int(v) for v in args.trellis_bits.split(","))
+        g = syn.generate(w, experts=1)
+        (g["gate_w"], g["up_w"], g["gate_s"],
+         g["up_s"]) = syn.trellis_weights(w.seed, w.E if w.repeats == 1
+                                          else 1, w.I, w.H, kg, ku)
+    else:
+        g = syn.generate(w, experts=w.E if w.repeats == 1 else 1, fmt=fmt)
     if op != "gate_up":
         g.update(syn.generate_down(w, experts=w.E if w.repeats == 1 else 1,
                                    fmt=fmt))
@@ -511,6 +554,11 @@ def main():
     q.load()
 
     op, fmt = args.op, args.format
+    if fmt == "trellis":
+        if op != "gate_up":
+            print(json.dumps({"error": "the trellis format has gate/up only"}))
+            return 1
+        fmt = f"trellis:{args.trellis_bits}"
     gw = GpuWorkload(w, args.kernel, local,
                      use_workspace=not args.no_workspace,
                      matvec_tile=args.matvec_tile, op=op, fmt=fmt)
@@ -572,10 +620,12 @@ def main():
     per_launch_ms = gu_ms / gw.calls
     rows_per_expert = (w.routed_rows if w.repeats > 1 else
                        w.routed_rows / units["touched_experts"])
-    decode = rows_per_expert < 64
+    # (the trellis kernel decodes every weight once per 8 rows at any size:
+    # its roofline is always the weight stream's)
+    decode = rows_per_expert < 64 or fmt.startswith("trellis")
     traffic_key = w.name if op == "gate_up" else f"{w.name}:{op}"
-    if fmt == "q8":
-        traffic_key += ":q8"
+    if fmt != "q4":
+        traffic_key += ":" + fmt.split(":")[0]
     if decode:
         bytes_per_launch = units["bytes"] / gw.calls
         achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
@@ -583,8 +633,12 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(traffic_key, "q4moe_matvec_tma.cu"),
-                "kernel": f"{OP_ENTRY[op]} matvec",
+                "traffic": load_traffic(
+                    traffic_key, "q4moe_trellis.cu" if gw.trellis
+                    else "q4moe_matvec_tma.cu"),
+                "kernel": ("q4moe_trellis_gate_up_swiglu (integer-bound "
+                           "decode)" if gw.trellis
+                           else f"{OP_ENTRY[op]} matvec"),
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
         flops_per_launch = units["flops"] / gw.calls

@@ -48,6 +48,7 @@ struct GateUpArgs {
     // trellis experts: block size, window bits, gate and up widths (the
     // gate/up word and scale offsets then name codes and f16 scales)
     int32_t tr_block, tr_window, tr_kg, tr_ku;
+    int32_t tr_rows_per_warp;    // output rows one warp of the kernel takes
 };
 
 // Bytes of one weight row of K values.

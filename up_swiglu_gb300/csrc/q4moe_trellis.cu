@@ -16,18 +16,18 @@
 // l, l+32, ... of 32 consecutive weights of a block, loads the k+1 words that
 // hold their windows (as on the page, the words of a run end where the next
 // run's start: the window of position j of the run starts at bit (31-j)*k of
-// them) and decodes each weight once.  The code value y (-510..510) is
-// formed in f32 without a conversion: y + 510 in the mantissa of 2^23 minus
-// 2^23 + 510.  Decoding is integer arithmetic (about a dozen operations a
-// weight): the kernel is bound by the integer pipe, not by HBM.
+// them) and decodes each weight once: a funnel shift and a mask for the
+// state, a multiply-add for the hash, one dp4a for its byte sum placed in
+// the mantissa of 2^23, one f32 subtraction for y (-510..510).  Decoding is
+// integer arithmetic: the kernel is bound by the instruction issue rate,
+// not by HBM.
 #include "q4moe_internal.cuh"
 
 namespace q4moe {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kRowsPerWarp = 2;
-constexpr int kRowsPerBlock = kWarps * kRowsPerWarp;
+constexpr int kMaxRowsPerWarp = 8;
 constexpr int kChunk = 8;
 constexpr int kMaxBits = 8;
 
@@ -38,22 +38,23 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// y(state) as f32 (exact).
+// y(state) as f32 (exact): the byte sum of x comes from one dp4a (bytes
+// times 1, unsigned) whose accumulator 0x4B000000 places it in the
+// mantissa of 2^23 (the sum is below 1021, so the exponent is untouched);
+// subtracting 2^23 + 510 leaves y.
 __device__ __forceinline__ float trellis_y(uint32_t s) {
     const uint32_t x = s * 34038481u + 76625530u;
-    const uint32_t p = (x & 0x00FF00FFu) + ((x >> 8) & 0x00FF00FFu);
-    const uint32_t y510 = (p & 0xFFFFu) + (p >> 16);        // y + 510
-    return __uint_as_float(0x4B000000u | y510) - 8389118.0f;
+    const uint32_t v = __dp4a(x, 0x01010101u, 0x4B000000u);
+    return __uint_as_float(v) - 8389118.0f;
 }
 
-// The L-bit window at bit b of the words w[0..k] (b + L <= 32 * (k + 1)).
+// The window at bit b of the words w[0..k], masked to L bits: one funnel
+// shift of the two words it can touch (b < 32 * k, so word b/32 + 1 is
+// always loaded).
 __device__ __forceinline__ uint32_t window(const uint32_t (&w)[kMaxBits + 1],
-                                          int b, int L) {
-    const int wi = b >> 5, off = b & 31;
-    uint32_t v = w[wi] >> off;
-    if (off + L > 32)
-        v |= w[wi + 1] << (32 - off);
-    return v & ((1u << L) - 1u);
+                                          int b, uint32_t mask) {
+    const int wi = b >> 5;
+    return __funnelshift_r(w[wi], w[wi + 1], b & 31) & mask;
 }
 
 // The k+1 words of a run: words w0 .. w0 + k of the block, wrapping.
@@ -66,6 +67,61 @@ __device__ __forceinline__ void load_run(const uint32_t *blk, int wpb, int w0,
             w[i] = __ldg(blk + (wi >= wpb ? wi - wpb : wi));
         } else {
             w[i] = 0;
+        }
+    }
+}
+
+// This lane's part of the sums of one chunk of NT grouped rows (tok[m] the
+// x row of chunk row m, or -1 for a row left out) over its runs of one
+// output row: ag[m] = sum y_gate * x[m], au[m] likewise for up.
+template <int KG, int KU, int NT>
+__device__ __forceinline__ void chunk_sums(const GateUpArgs &a,
+                                           const uint32_t *grow,
+                                           const uint32_t *urow,
+                                           const int32_t (&tok)[kChunk],
+                                           uint32_t lmask, float (&ag)[kChunk],
+                                           float (&au)[kChunk]) {
+    const int lane = threadIdx.x & 31;
+    const int Tb = a.tr_block;
+    const int kg = KG ? KG : a.tr_kg, ku = KU ? KU : a.tr_ku;
+    const int gwpb = Tb * kg / 32, uwpb = Tb * ku / 32;
+    const int runs_per_block = Tb / 32;
+    const int nruns = (int)(a.H / 32);
+#pragma unroll
+    for (int m = 0; m < kChunk; ++m)
+        ag[m] = au[m] = 0.0f;
+    for (int run = lane; run < nruns; run += 32) {
+        const int blk = run / runs_per_block;
+        const int t0 = (run - blk * runs_per_block) * 32;
+        uint32_t gw[kMaxBits + 1], uw[kMaxBits + 1];
+        load_run(grow + (int64_t)blk * gwpb, gwpb, (Tb - 32 - t0) * kg / 32,
+                 kg, gw);
+        load_run(urow + (int64_t)blk * uwpb, uwpb, (Tb - 32 - t0) * ku / 32,
+                 ku, uw);
+        const int64_t c0 = (int64_t)blk * Tb + t0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 xv[NT];
+#pragma unroll
+            for (int m = 0; m < NT; ++m)
+                xv[m] = tok[m] >= 0
+                            ? __ldg(reinterpret_cast<const uint4 *>(
+                                        a.x + (int64_t)tok[m] * a.H + c0) + q)
+                            : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = q * 8 + jj;
+                const float yg = trellis_y(window(gw, (31 - j) * kg, lmask));
+                const float yu = trellis_y(window(uw, (31 - j) * ku, lmask));
+#pragma unroll
+                for (int m = 0; m < NT; ++m) {
+                    const uint32_t h = (&xv[m].x)[jj >> 1];
+                    const float xf = __uint_as_float(
+                        (jj & 1) ? (h & 0xFFFF0000u) : (h << 16));
+                    ag[m] = __fmaf_rn(yg, xf, ag[m]);
+                    au[m] = __fmaf_rn(yu, xf, au[m]);
+                }
+            }
         }
     }
 }
@@ -88,19 +144,18 @@ trellis_gate_up_kernel(GateUpArgs a) {
     if (slab == nullptr)
         return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int Tb = a.tr_block, L = a.tr_window;
+    const int Tb = a.tr_block;
+    const uint32_t lmask = (1u << a.tr_window) - 1u;   // L <= 24
     const int kg = KG ? KG : a.tr_kg, ku = KU ? KU : a.tr_ku;
-    const int gwpb = Tb * kg / 32, uwpb = Tb * ku / 32;
-    const int runs_per_block = Tb / 32;
-    const int nruns = (int)(a.H / 32);
-    const int64_t grow_words = a.H / Tb * gwpb, urow_words = a.H / Tb * uwpb;
+    const int64_t grow_words = a.H / Tb * (Tb * kg / 32);
+    const int64_t urow_words = a.H / Tb * (Tb * ku / 32);
     const uint16_t *gs = reinterpret_cast<const uint16_t *>(slab + a.gate_s_off);
     const uint16_t *us = reinterpret_cast<const uint16_t *>(slab + a.up_s_off);
     const float rcp = __uint_as_float(0x3BDDB447u);   // RN32(1/147.800537109375)
 
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        const int64_t i = (int64_t)blockIdx.x * kRowsPerBlock +
-                          warp * kRowsPerWarp + rr;
+    const int rpw = a.tr_rows_per_warp;
+    for (int rr = 0; rr < rpw; ++rr) {
+        const int64_t i = ((int64_t)blockIdx.x * kWarps + warp) * rpw + rr;
         if (i >= a.I)
             break;
         const uint32_t *grow = reinterpret_cast<const uint32_t *>(
@@ -116,48 +171,20 @@ trellis_gate_up_kernel(GateUpArgs a) {
             for (int m = 0; m < kChunk; ++m)
                 tok[m] = m < nt ? (int32_t)row_token(a, p0 + m) : -1;
             float ag[kChunk], au[kChunk];
-#pragma unroll
-            for (int m = 0; m < kChunk; ++m)
-                ag[m] = au[m] = 0.0f;
-            for (int run = lane; run < nruns; run += 32) {
-                const int blk = run / runs_per_block;
-                const int t0 = (run - blk * runs_per_block) * 32;
-                uint32_t gw[kMaxBits + 1], uw[kMaxBits + 1];
-                load_run(grow + (int64_t)blk * gwpb, gwpb,
-                         (Tb - 32 - t0) * kg / 32, kg, gw);
-                load_run(urow + (int64_t)blk * uwpb, uwpb,
-                         (Tb - 32 - t0) * ku / 32, ku, uw);
-                const int64_t c0 = (int64_t)blk * Tb + t0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 xv[kChunk];
-#pragma unroll
-                    for (int m = 0; m < kChunk; ++m)
-                        xv[m] = tok[m] >= 0
-                                    ? __ldg(reinterpret_cast<const uint4 *>(
-                                                a.x + (int64_t)tok[m] * a.H +
-                                                c0) + q)
-                                    : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = q * 8 + jj;
-                        const float yg = trellis_y(window(gw, (31 - j) * kg, L));
-                        const float yu = trellis_y(window(uw, (31 - j) * ku, L));
-#pragma unroll
-                        for (int m = 0; m < kChunk; ++m) {
-                            if (m >= nt)
-                                continue;
-                            const uint32_t h =
-                                (&xv[m].x)[jj >> 1] >> (16 * (jj & 1));
-                            const float xf = bf16_f32(h & 0xFFFFu);
-                            ag[m] = __fmaf_rn(yg, xf, ag[m]);
-                            au[m] = __fmaf_rn(yu, xf, au[m]);
-                        }
-                    }
-                }
+            switch (nt) {
+            case 1: chunk_sums<KG, KU, 1>(a, grow, urow, tok, lmask, ag, au); break;
+            case 2: chunk_sums<KG, KU, 2>(a, grow, urow, tok, lmask, ag, au); break;
+            case 3: chunk_sums<KG, KU, 3>(a, grow, urow, tok, lmask, ag, au); break;
+            case 4: chunk_sums<KG, KU, 4>(a, grow, urow, tok, lmask, ag, au); break;
+            case 5: chunk_sums<KG, KU, 5>(a, grow, urow, tok, lmask, ag, au); break;
+            case 6: chunk_sums<KG, KU, 6>(a, grow, urow, tok, lmask, ag, au); break;
+            case 7: chunk_sums<KG, KU, 7>(a, grow, urow, tok, lmask, ag, au); break;
+            default: chunk_sums<KG, KU, 8>(a, grow, urow, tok, lmask, ag, au); break;
             }
 #pragma unroll
             for (int m = 0; m < kChunk; ++m) {
+                if (m >= nt)                     // warp-uniform
+                    break;
                 const float G = warp_sum(ag[m]);
                 const float U = warp_sum(au[m]);
                 if (lane == m && tok[m] >= 0) {
@@ -175,9 +202,17 @@ trellis_gate_up_kernel(GateUpArgs a) {
     }
 }
 
+// Rows per warp: the most (up to 8, amortising each block's set-up) that
+// still leave two blocks per SM for the experts of the call.
 template <int KG, int KU>
-cudaError_t launch_widths(const GateUpArgs &a, cudaStream_t s) {
-    const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),
+cudaError_t launch_widths(const GateUpArgs &a0, cudaStream_t s) {
+    GateUpArgs a = a0;
+    int rpw = kMaxRowsPerWarp;
+    while (rpw > 1 && (a.I + kWarps * rpw - 1) / (kWarps * rpw) * a.E <
+                          2ll * a.num_sms)
+        rpw /= 2;
+    a.tr_rows_per_warp = rpw;
+    const dim3 grid((unsigned)((a.I + kWarps * rpw - 1) / (kWarps * rpw)),
                     (unsigned)a.E);
     return launch_pdl(trellis_gate_up_kernel<KG, KU>, grid, dim3(kWarps * 32),
                       0, s, a);

@@ -30,7 +30,9 @@ Recipe (the workloads' shapes and value distributions):
 - Q8 weights: uniform signed bytes (-128..127, own streams), row scales of
   the Q4 recipe divided by 16 (so that weight times scale spans the same
   range as Q4's nibble - 8 times its scale); the Q8 exact case draws the
-  scales as ``2**-k``, k uniform in 8..13.
+  scales as ``2**-k``, k uniform in 8..13;
+- trellis codes: uniform 32-bit words (every bit pattern is a valid code
+  stream), f16 row scales of the Q4 recipe.
 """
 from __future__ import annotations
 
@@ -48,6 +50,7 @@ S_X, S_GATE_W, S_UP_W, S_GATE_S, S_UP_S, S_ROUTE, S_EXACT_X, S_EXACT_S = \
     range(1, 9)
 S_DOWN_W, S_DOWN_S, S_EXACT_MID, S_EXACT_DS, S_MID = range(9, 14)
 S_Q8_GATE_W, S_Q8_UP_W, S_Q8_DOWN_W = range(14, 17)
+S_TR_GATE, S_TR_UP = range(17, 19)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -311,3 +314,16 @@ def exact_q8_case(seed: int, T: int, H: int, E: int, I: int):
     sc = np.ldexp(np.float32(1.0), -ks).astype(np.float32)
     gate_w, up_w, _, _ = q8_weights(seed, E, I, H)
     return x, gate_w, up_w, sc[: E * I].reshape(E, I), sc[E * I:].reshape(E, I)
+
+
+def trellis_weights(seed: int, E: int, I: int, H: int, kg: int, ku: int,
+                    block: int = 256):
+    """Trellis codes uint32 [E, I, H/block * block*k/32] for gate (kg bits)
+    and up (ku bits), and f16 scale bit patterns [E, I] each."""
+    gate = words_u32(seed, S_TR_GATE, E * I * (H * kg // 32)).reshape(E, I, -1)
+    up = words_u32(seed, S_TR_UP, E * I * (H * ku // 32)).reshape(E, I, -1)
+    gs = (0.002 + 0.018 * uniform(seed, S_GATE_S, E * I)).astype(
+        np.float16).reshape(E, I).view(np.uint16)
+    us = (0.002 + 0.018 * uniform(seed, S_UP_S, E * I)).astype(
+        np.float16).reshape(E, I).view(np.uint16)
+    return gate, up, gs, us
