@@ -1,8 +1,9 @@
 /*
  * q4moe.h -- C ABI of the fused 4-bit MoE expert gate/up projection with
  * SwiGLU for one NVIDIA GB300 GPU (sm_103a), with the down projection that
- * completes the expert MLP and the signed 8-bit weight format of the same
- * page.
+ * completes the expert MLP, the signed 8-bit weight format of the same page
+ * and trellis-coded (QTIP 1MAD) experts of pages 54 and 57
+ * (q4moe_trellis_gate_up_swiglu, formula at its declaration).
  *
  * The operation follows "@mlx-bun/inference 0.0.0-stage -> 1.0.0", page 52,
  * src/kernels/glm52/streamed-experts.ts, GATE_UP_SOURCE (and the
@@ -45,8 +46,9 @@
  *    They never synchronise the host, except once per device: the first
  *    call on a device fills a 128 KB table in the library's own device
  *    memory (the bf16 sigmoid of every bf16 value) and waits for it, so
- *    that first call must not be made while a stream is being captured.  Argument errors the host can see are
- *    returned before anything is launched.  Inconsistent data that only the
+ *    that first call must not be made while a stream is being captured.
+ *    Argument errors the host can see are returned before anything is
+ *    launched.  Inconsistent data that only the
  *    GPU can see (row offsets, token indices, expert ids, slab pointers) sets
  *    a bit in the device status word (Q4MOE_DEV_*) and the affected rows are
  *    skipped; read it with q4moe_device_status().  Nothing traps the GPU.
