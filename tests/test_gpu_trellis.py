@@ -35,7 +35,8 @@ def _gpu():
 
 
 def _problem(seed, counts, I, H, kg, ku, exact=False):
-    """One token per grouped row, expert e getting counts[e] rows."""
+    """One token per grouped row, expert e getting counts[e] rows (a row's
+    codes are H * k / 32 words whatever the block size)."""
     E, M = len(counts), int(sum(counts))
     rng = np.random.default_rng(seed)
     gc = syn.words_u32(seed, 40, E * I * (H * kg // 32)).reshape(E, I, -1)
@@ -54,10 +55,10 @@ def _problem(seed, counts, I, H, kg, ku, exact=False):
                 ku=ku)
 
 
-def _run(p, L=12, ptr_table=False, debug=True):
+def _run(p, L=12, ptr_table=False, debug=True, tb=TB):
     import torch
     E = p["gc"].shape[0]
-    lay = q.q4moe_trellis_canonical_layout(p["H"], p["I"], TB, L, p["kg"],
+    lay = q.q4moe_trellis_canonical_layout(p["H"], p["I"], tb, L, p["kg"],
                                            p["ku"])
     host = q.pack_trellis_pool(lay, p["gc"], p["uc"], p["gs"], p["us"])
     buf, pool = hz.aligned_device_buffer(host.size)
@@ -98,9 +99,9 @@ def _run(p, L=12, ptr_table=False, debug=True):
     return res
 
 
-def _compare(p, gpu, L=12, exact=False):
+def _compare(p, gpu, L=12, exact=False, tb=TB):
     orc = oracle.trellis_gate_up_swiglu(p["x"], p["gc"], p["uc"], p["gs"],
-                                        p["us"], p["kg"], p["ku"], L, TB,
+                                        p["us"], p["kg"], p["ku"], L, tb,
                                         p["offs"], p["tok"])
     e_of = np.repeat(np.arange(len(p["offs"]) - 1), np.diff(p["offs"]))
     rcp = np.float32(1.0 / 147.800537109375)
@@ -126,6 +127,18 @@ def test_trellis_exact_bit_exact(kg, ku):
 def test_trellis_real_valued(kg, ku, L):
     p = _problem(100 + kg + ku + L, [1, 7, 2, 13], 96, 1024, kg, ku)
     _compare(p, _run(p, L=L), L=L)
+
+
+@pytest.mark.parametrize("tb,kg,ku,L", [(32, 4, 4, 12), (128, 2, 3, 12),
+                                        (64, 2, 2, 24), (512, 3, 4, 12)])
+def test_trellis_block_sizes_and_windows(tb, kg, ku, L):
+    """Blocks of 32 (one run a block), 128, 64 with a 24-bit window over
+    2-bit codes (the window spans more than one block's worth of words of
+    a run), and 512."""
+    p = _problem(tb + L, [4, 9, 0, 2], 48, 1024, kg, ku, exact=True)
+    _compare(p, _run(p, L=L, tb=tb), L=L, exact=True, tb=tb)
+    p = _problem(tb + L + 1, [4, 9, 0, 2], 48, 1024, kg, ku)
+    _compare(p, _run(p, L=L, tb=tb), L=L, tb=tb)
 
 
 def test_trellis_pointer_table_and_bad_offsets():
