@@ -282,3 +282,62 @@ def test_valid_call_without_gpu_reports_device_error():
         pytest.skip("a GPU is present")
     rc = _call()
     assert rc in (q.ERR_CUDA, q.ERR_DEVICE)
+
+
+def test_trellis_layout_and_host_errors():
+    """Trellis slabs: canonical section offsets (256-byte boundaries, size
+    rounded to 4096), geometry checks, packing, and host argument errors of
+    the trellis entry point (no GPU needed)."""
+    H, I, T, L, kg, ku = 512, 40, 256, 12, 4, 3
+    lay = q.q4moe_trellis_canonical_layout(H, I, T, L, kg, ku)
+    gb, ub = I * H * kg // 8, I * H * ku // 8
+    up256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert lay.gate_codes_offset == 0
+    assert lay.up_codes_offset == up256(gb)
+    assert lay.gate_scales_offset == up256(lay.up_codes_offset + ub)
+    assert lay.up_scales_offset == up256(lay.gate_scales_offset + 2 * I)
+    assert lay.slab_bytes % 4096 == 0
+    assert lay.slab_bytes >= lay.up_scales_offset + 2 * I
+    for args in ((H, I, 100, L, kg, ku),       # block not a multiple of 32
+                 (H, I, 384, L, kg, ku),       # block does not divide H
+                 (H, I, T, 25, kg, ku),        # window too wide
+                 (H, I, T, L, 9, ku),          # width above 8
+                 (H, 0, T, L, kg, ku)):
+        with pytest.raises(q.Q4moeError):
+            q.q4moe_trellis_canonical_layout(*args)
+    rng = np.random.default_rng(2)
+    gc = rng.integers(0, 2**32, size=(I, H * kg // 32),
+                      dtype=np.uint64).astype(np.uint32)
+    uc = rng.integers(0, 2**32, size=(I, H * ku // 32),
+                      dtype=np.uint64).astype(np.uint32)
+    gs = rng.integers(0, 2**16, size=I).astype(np.uint16)
+    us = rng.integers(0, 2**16, size=I).astype(np.uint16)
+    slab = np.full(lay.slab_bytes, 0xCD, np.uint8)
+    q.q4moe_trellis_pack_slab(lay, gc, uc, gs, us, slab)
+    assert np.array_equal(slab[:gb].view(np.uint32).reshape(I, -1), gc)
+    o = lay.up_codes_offset
+    assert np.array_equal(slab[o:o + ub].view(np.uint32).reshape(I, -1), uc)
+    o = lay.up_scales_offset
+    assert np.array_equal(slab[o:o + 2 * I].view(np.uint16), us)
+    lib = q.load()
+    s = q.make_trellis_slabs(2, lay, base=FAKE)
+
+    def call(x=FAKE, slabs=s, M=4, Hc=H, opts=None):
+        return lib.q4moe_trellis_gate_up_swiglu(
+            x, ctypes.byref(slabs), FAKE, FAKE, M, Hc, I, FAKE,
+            None if opts is None else ctypes.byref(opts), None)
+
+    assert call(Hc=1024) == q.ERR_INVALID_ARG          # differs from layout
+    assert call(x=FAKE + 8) == q.ERR_ALIGNMENT
+    assert call(slabs=q.make_trellis_slabs(2, lay, base=FAKE + 64)) == \
+        q.ERR_ALIGNMENT
+    o = q.q4moe_options_t()
+    o.kernel = q.KERNEL_GEMM
+    assert call(opts=o) == q.ERR_INVALID_ARG           # no kernel choice
+    bad = q.q4moe_trellis_layout_t.from_buffer_copy(lay)
+    bad.up_scales_offset = lay.slab_bytes - 2
+    assert call(slabs=q.make_trellis_slabs(2, bad, base=FAKE)) == \
+        q.ERR_RANGE
+    import torch
+    if not torch.cuda.is_available():
+        assert call() in (q.ERR_CUDA, q.ERR_DEVICE)
