@@ -333,6 +333,17 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
 }
 
+// Unit u of a call with one expert: the rows follow from M alone.
+__device__ __forceinline__ Unit unit_single(int u, int M, int NT) {
+    Unit t;
+    t.e = 0;
+    t.chunk = u / NT;
+    t.tile = u - t.chunk * NT;
+    t.p0 = t.chunk * kTok;
+    t.nt = min(kTok, M - t.p0);
+    return t;
+}
+
 // Shared memory after the 1024-byte aligned ring: staged x, reduction
 // buffer, barriers, per-warp exponent ranges, row offsets and unit prefix,
 // abort flag, stage count.
@@ -389,12 +400,29 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
         tma_desc_prefetch(&tm_gate);
         tma_desc_prefetch(&tm_up);
     }
+    __shared__ int s_single_bad;             // one expert: offsets != {0, M}
+    __syncthreads();                         // barriers initialised
     if (a.matvec_last)
         grid_launch_dependents();
     grid_dependency_wait();
 
     int u0 = 0, u1 = 0;
-    if (stage_row_offsets(a, s_off)) {       // (synchronises the block)
+    // One expert: the units, and each unit's rows, follow from M; thread 0
+    // loads the two offsets now and checks them before the first store
+    // (an inconsistent pair stores nothing), so no block-wide barrier or
+    // dependent load stands between the dependency release and the work.
+    int32_t off_lo = 0, off_hi = 0;
+    if (E == 1) {
+        const unsigned nunits = (unsigned)(ceil_div((int)a.M, kTok) * NT);
+        const unsigned G = gridDim.x, bb = blockIdx.x, q = nunits / G,
+                       r = nunits - q * G;
+        u0 = (int)(bb * q + min(bb, r));
+        u1 = u0 + (int)q + (bb < r ? 1 : 0);
+        if (tid == 0) {
+            off_lo = __ldg(a.row_offsets);
+            off_hi = __ldg(a.row_offsets + 1);
+        }
+    } else if (stage_row_offsets(a, s_off)) {  // (synchronises the block)
         const int32_t mvmax = matvec_limit(a, s_off);
         if (warp == 0) {
             const int per = ceil_div(E, 32);
@@ -490,7 +518,8 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
         int j = 0;                               // stage counter
         bool ok = true;
         for (int u = u0; u < u1 && ok; ++u) {
-            const Unit t = unit_of(u, s_off, s_pre, E, NT);
+            const Unit t = E == 1 ? unit_single(u, (int)a.M, NT)
+                                  : unit_of(u, s_off, s_pre, E, NT);
             const int rbase = t.tile * kTileRows + b * 16;  // block's 1st row
             const bool live = rbase < (int)a.I;
             const bool live_hi = kDown ? rbase + kHiRow < (int)a.I : live;
@@ -627,6 +656,14 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
             if (!ok)
                 break;
             // the unit is complete: sum the K parts of each block in order
+            // (one expert: the offsets' check lands before the first store)
+            if (E == 1 && tid == 0 && u == u0) {
+                const bool bad = off_lo != 0 || off_hi != (int32_t)a.M;
+                s_single_bad = bad;
+                if (bad && blockIdx.x == 0)
+                    atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
+            }
+            static_assert(P > 1, "the K parts' reduction orders the check");
             if (P > 1) {
                 if (kp != 0) {
                     const int ri = (b * (P - 1) + kp - 1) * 32 + lane;
@@ -651,7 +688,7 @@ matvec_tma_kernel(GateUpArgs a, const __grid_constant__ CUtensorMap tm_gate,
                 }
                 consumer_sync();
             }
-            if (kp == 0 && live) {
+            if (kp == 0 && live && !(E == 1 && s_single_bad)) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int64_t row = (int64_t)rbase + 8 * i + g;
