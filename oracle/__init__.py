@@ -8,7 +8,8 @@ The arithmetic lives in ``q4moe_oracle.c`` (plain C, f64 accumulation); this
 module compiles it with gcc on first use and marshals numpy arrays.  Every
 function cites the passage it follows in the C source.  ``group_rows``,
 ``tail``, ``gate_up_swiglu``, ``down_proj`` and ``expert_mlp`` are pinned by the ``-m "not gpu"`` tests in
-``tests/test_oracle_pins.py``.
+``tests/test_oracle_pins.py`` (and the ``test_oracle_*_pins.py`` files beside
+it for the down projection, Q8, trellis codes and the MLX tail).
 """
 from __future__ import annotations
 
@@ -89,7 +90,12 @@ def _load():
         lib.q4o_trellis_gate_up_swiglu.restype = _INT
         lib.q4o_trellis_gate_up_swiglu.argtypes = [
             _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _INT, _INT, _INT,
-            _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT]
+            _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT,
+            _INT]
+        lib.q4o_tail_mlx.restype = None
+        lib.q4o_tail_mlx.argtypes = [ctypes.c_float, ctypes.c_float, _P]
+        lib.q4o_tail_mlx_array.restype = None
+        lib.q4o_tail_mlx_array.argtypes = [_I64, _P, _P, _P]
         lib.q4o_trellis_y.restype = _INT
         lib.q4o_trellis_y.argtypes = [ctypes.c_uint32]
         lib.q4o_trellis_scale.restype = ctypes.c_float
@@ -137,6 +143,26 @@ def tail(gate32: float, up32: float, silu_mode: int = 0):
     _load().q4o_tail(ctypes.c_float(gate32), ctypes.c_float(up32),
                      int(silu_mode), _ptr(res))
     return tuple(int(v) for v in res)
+
+
+def tail_mlx(gate32: float, up32: float):
+    """(gateT, upT, sigmoidT, siluT, out) bf16 bits for one element through
+    MLX's compiled SwiGLU in bf16 arithmetic, the tail of the pages'
+    mixed-width trellis kernel (page 57, mixed-gate-up-factored.ts)."""
+    res = np.zeros(5, dtype=np.uint16)
+    _load().q4o_tail_mlx(ctypes.c_float(gate32), ctypes.c_float(up32),
+                         _ptr(res))
+    return tuple(int(v) for v in res)
+
+
+def tail_mlx_array(gate32, up32) -> np.ndarray:
+    """tail_mlx() over arrays of f32 gate/up values; uint16 [n, 5]."""
+    g = _c(gate32, np.float32).ravel()
+    u = _c(up32, np.float32).ravel()
+    assert g.shape == u.shape
+    res = np.zeros((g.shape[0], 5), dtype=np.uint16)
+    _load().q4o_tail_mlx_array(g.shape[0], _ptr(g), _ptr(u), _ptr(res))
+    return res
 
 
 def tail_array(gate32, up32, silu_mode: int = 0) -> np.ndarray:
@@ -383,9 +409,11 @@ def trellis_block(words, Tb: int, k: int, L: int):
 def trellis_gate_up_swiglu(x_bits, gate_codes, up_codes, gate_s_f16,
                            up_s_f16, kg: int, ku: int, L: int, Tb: int,
                            row_offsets, token_of_row, rows=None, cols=None,
-                           nthreads: int = 0):
+                           nthreads: int = 0, tail: str = "page"):
     """Trellis gate/up + SwiGLU with factored row scales (page 57,
-    gate-up-mma.ts / mixed-gate-up-factored.ts arithmetic, page 52 tail).
+    gate-up-mma.ts / mixed-gate-up-factored.ts arithmetic).  tail "page":
+    the page 52 tail (the pages' equal-width kernels); "mlx": MLX's compiled
+    SwiGLU in bf16 arithmetic (the mixed-width kernel).
     gate_codes uint32 [E, I, words], up_codes likewise (widths kg, ku);
     scales f16 bit patterns [E, I].  All M x I outputs or the (rows, cols)
     elements; a dict with out, gate32, up32, gabs, uabs."""
@@ -411,7 +439,8 @@ def trellis_gate_up_swiglu(x_bits, gate_codes, up_codes, gate_s_f16,
         int(kg), int(ku), int(L), int(Tb), _ptr(offs), _ptr(tok), M, n,
         None if r is None else _ptr(r), None if c is None else _ptr(c),
         _ptr(res["out"]), _ptr(res["gate32"]), _ptr(res["up32"]),
-        _ptr(res["gabs"]), _ptr(res["uabs"]), int(nthreads))
+        _ptr(res["gabs"]), _ptr(res["uabs"]),
+        {"page": 0, "mlx": 1}[tail], int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return res

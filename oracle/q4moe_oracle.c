@@ -43,7 +43,12 @@
  *    f64, which gives the correctly rounded f32 result (double has more than
  *    2*24+2 bits, so the double rounding is innocuous);
  *  - silu_mode 1 keeps the sigmoid in f32 (no bf16 rounding of s), the
- *    alternative reading of "bf16(silu(gate))"; mode 0 follows the page.
+ *    alternative reading of "bf16(silu(gate))"; mode 0 follows the page;
+ *  - the second tail, MLX's compiled SwiGLU that the pages' mixed-width
+ *    trellis kernel ends with (page 57, mixed-gate-up-factored.ts), works
+ *    "in T" (bf16): every step is evaluated in f32, correctly rounded, and
+ *    its result rounded to bf16 before the next step uses it; the sigmoid
+ *    is 1 / (1 + exp(|g|)) for negative g and one minus that otherwise.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no fast-math).
  */
@@ -113,6 +118,51 @@ void q4o_tail(float gate32, float up32, int silu_mode, uint16_t res[5])
     res[2] = sT;
     res[3] = siluT;
     res[4] = q4o_bf16_rne(o32);
+}
+
+/* The tail of the pages' mixed-width trellis kernel (page 57,
+ * mixed-gate-up-factored.ts): MLX's compiled SwiGLU over the bf16 gate and
+ * up, each step computed in f32 (correctly rounded) and rounded to bf16:
+ *   eT = bf16(RN32(exp(|gateT|)))      (+inf once exp passes FLT_MAX)
+ *   dT = bf16(RN32(1 + eT)),  yT = bf16(RN32(1 / dT))
+ *   sigT = yT if gateT < 0 (false for -0), else bf16(1 - yT)
+ *   siluT = bf16(gateT * sigT),  out = bf16(siluT * upT).
+ * res[0..4] as q4o_tail: gateT, upT, sigT, siluT, out. */
+void q4o_tail_mlx(float gate32, float up32, uint16_t res[5])
+{
+    const uint16_t gT = q4o_bf16_rne(gate32);
+    const uint16_t uT = q4o_bf16_rne(up32);
+    const float g = q4o_bf16_to_f32(gT);
+    const float a = fabsf(g);
+    const float e = q4o_bf16_to_f32(q4o_bf16_rne((float)exp((double)a)));
+    const float d = q4o_bf16_to_f32(q4o_bf16_rne((float)(1.0 + (double)e)));
+    const uint16_t yT = q4o_bf16_rne((float)(1.0 / (double)d));
+    const uint16_t sT =
+        g < 0.0f ? yT
+                 : q4o_bf16_rne((float)(1.0 - (double)q4o_bf16_to_f32(yT)));
+    const uint16_t siluT = q4o_bf16_rne(g * q4o_bf16_to_f32(sT));
+    res[0] = gT;
+    res[1] = uT;
+    res[2] = sT;
+    res[3] = siluT;
+    res[4] = q4o_bf16_rne(q4o_bf16_to_f32(siluT) * q4o_bf16_to_f32(uT));
+}
+
+/* q4o_tail (tail 0, page 52) or q4o_tail_mlx (tail 1) of one element. */
+static void q4o_tail_of(int tail, float gate32, float up32, uint16_t res[5])
+{
+    if (tail == 1)
+        q4o_tail_mlx(gate32, up32, res);
+    else
+        q4o_tail(gate32, up32, 0, res);
+}
+
+/* q4o_tail_mlx over n elements: res is [n][5]. */
+void q4o_tail_mlx_array(int64_t n, const float *gate32, const float *up32,
+                        uint16_t *res)
+{
+    for (int64_t j = 0; j < n; ++j)
+        q4o_tail_mlx(gate32[j], up32[j], res + 5 * j);
 }
 
 /* q4o_tail over n elements: res is [n][5] (gateT, upT, sigT, siluT, out). */
@@ -576,7 +626,9 @@ static double q4o_trellis_dot(const uint32_t *row, const uint16_t *xrow,
 /* All M x I outputs, or (rows != NULL) the n elements (rows[j], cols[j]).
  * gate_codes: uint32 [E, I, H / Tb * Tb * kg / 32], up_codes likewise with
  * ku; gate_s/up_s: f16 bits [E, I].  Outputs as q4o_gate_up_swiglu
- * (gate32 = RN32(G * gate scale), the page 52 tail).  Needs H % Tb == 0,
+ * (gate32 = RN32(G * gate scale)); tail 0 ends with the page 52 tail (the
+ * pages' equal-width kernels, gate-up-mma.ts), tail 1 with MLX's
+ * (q4o_tail_mlx, the mixed-width kernel).  Needs H % Tb == 0,
  * Tb * k % 32 == 0, 1 <= L <= 24, L <= Tb * k. */
 int q4o_trellis_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H,
                                int64_t I, int32_t E,
@@ -589,8 +641,10 @@ int q4o_trellis_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H,
                                int64_t n, const int64_t *rows,
                                const int64_t *cols, uint16_t *out,
                                float *gate32, float *up32, double *gabs,
-                               double *uabs, int nthreads)
+                               double *uabs, int tail, int nthreads)
 {
+    if (tail != 0 && tail != 1)
+        return -1;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || M < 0 || Tb <= 0 ||
         H % Tb != 0 || kg < 1 || ku < 1 || kg > 8 || ku > 8 ||
         (Tb * kg) % 32 != 0 || (Tb * ku) % 32 != 0 || L < 1 || L > 24 ||
@@ -633,7 +687,7 @@ int q4o_trellis_gate_up_swiglu(const uint16_t *x, int64_t T, int64_t H,
         const float u32 = (float)(U * (double)q4o_trellis_scale(
                                           up_s[(int64_t)e * I + i]));
         uint16_t res[5];
-        q4o_tail(g32, u32, 0, res);
+        q4o_tail_of(tail, g32, u32, res);
         out[j] = res[4];
         if (gate32) gate32[j] = g32;
         if (up32) up32[j] = u32;

@@ -137,3 +137,59 @@ def exact_out_bits(gate32: float, up32: float) -> int:
     _, silu = exact_tail_tables()
     siluT = bf16_value(int(silu[bf16_bits(gT)]))
     return bf16_bits(round_bf16(mul_f32(siluT, uT)))
+
+
+def exact_exp_f32(a: float) -> float:
+    """RN32(exp(a)) from a 300-bit exp: +inf past f32 overflow, +0 below the
+    f32 subnormal range."""
+    import mpmath
+    if a > 90.0:                  # exp(a) > 1.2e39
+        return math.inf
+    if a < -104.0:                # exp(a) < 2^-150
+        return 0.0
+    with mpmath.workprec(300):
+        ev = mpmath.exp(mpmath.mpf(a))
+        man, ex = int(ev.man), int(ev.exp)
+    return round_f32_frac(Fraction(man) * (Fraction(2) ** ex))
+
+
+def exact_mlx_sigmoid_bf16(g: float) -> float:
+    """Sigmoid of MLX's compiled SwiGLU in bf16 arithmetic: every step's
+    exact result rounded to f32 and then to bf16; 1 / (1 + exp(|g|)) for
+    negative g (not for -0), one minus it otherwise."""
+    e = round_bf16(exact_exp_f32(abs(g)))
+    if math.isinf(e):
+        y = 0.0
+    else:
+        d = round_bf16(round_f32_frac(Fraction(1) + Fraction(e)))
+        y = round_bf16(round_f32_frac(Fraction(1) / Fraction(d)))
+    if g < 0:
+        return y
+    return round_bf16(round_f32_frac(Fraction(1) - Fraction(y)))
+
+
+@functools.lru_cache(maxsize=1)
+def exact_mlx_tail_tables():
+    """For every finite bf16 gateT pattern b: (sigmoidT bits, siluT bits)
+    of the MLX tail, from the exact chain above.  Non-finite patterns hold
+    -1."""
+    sig = np.full(65536, -1, dtype=np.int64)
+    silu = np.full(65536, -1, dtype=np.int64)
+    for b in range(65536):
+        if (b >> 7) & 0xFF == 0xFF:
+            continue
+        g = bf16_value(b)
+        sT = exact_mlx_sigmoid_bf16(g)
+        siluT = round_bf16(mul_f32(g, sT))
+        sig[b] = bf16_bits(sT)
+        silu[b] = bf16_bits(siluT)
+    return sig, silu
+
+
+def exact_mlx_out_bits(gate32: float, up32: float) -> int:
+    """Final bf16 output of one element through the MLX tail."""
+    gT = round_bf16(gate32)
+    uT = round_bf16(up32)
+    _, silu = exact_mlx_tail_tables()
+    siluT = bf16_value(int(silu[bf16_bits(gT)]))
+    return bf16_bits(round_bf16(mul_f32(siluT, uT)))
