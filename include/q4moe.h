@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 6
+#define Q4MOE_ABI_VERSION 7
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -104,6 +104,24 @@ extern "C" {
  * for bit (page 52's matvec has this property: one SIMD group per row and
  * sample).  Large groups stream each expert's weights once per 8 rows. */
 #define Q4MOE_KERNEL_BATCH_INVARIANT 3
+
+/*
+ * SwiGLU tail (q4moe_options_t.tail), from the bf16 gateT and upT:
+ *   PAGE (page 52, streamed-experts.ts, GATE_UP_SOURCE): sigT =
+ *     bf16(1 / (1 + exp(-gateT))) in f32 (precise exp, IEEE add and divide),
+ *     siluT = bf16(gateT * sigT), out = bf16(siluT * upT);
+ *   MLX (page 57, mixed-gate-up-factored.ts: MLX's compiled SwiGLU "in T"),
+ *     every step rounded to bf16: e = bf16(exp(|gateT|)), d = bf16(1 + e),
+ *     y = bf16(1 / d), sigT = y if gateT < 0 else bf16(1 - y), then siluT
+ *     and out as above.  Trellis calls only;
+ *   AUTO: the pages' choice for the call (PAGE, except trellis calls whose
+ *     gate and up widths differ, which take MLX).
+ * Every value is exact against the definition (each operation correctly
+ * rounded, no flush to zero).
+ */
+#define Q4MOE_TAIL_AUTO 0
+#define Q4MOE_TAIL_PAGE 1
+#define Q4MOE_TAIL_MLX 2
 
 /*
  * Byte layout of one expert slab (page 51, layout.ts,
@@ -183,6 +201,9 @@ typedef struct q4moe_options {
                            are undefined after the call; calls that share a
                            workspace must be ordered on one stream.       */
     int64_t workspace_bytes; /* size of workspace                         */
+    int32_t tail;       /* Q4MOE_TAIL_*: the SwiGLU tail (Q4 and Q8 calls
+                           take AUTO or PAGE only)                         */
+    int32_t reserved1;  /* must be 0                                       */
 } q4moe_options_t;
 
 /*
@@ -370,7 +391,10 @@ int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *expert_slabs,
  *   G = sum_k y_k * x[t][k]                      (f32 accumulate)
  *   gate32 = G * RN32(f32(gate_scale[i]) * RN32(1 / 147.800537109375))
  * (the row scale factored out of the sum, as on the pages), up likewise
- * with its own width, then the same SwiGLU tail as Q4.
+ * with its own width, then the tail opts->tail selects: with
+ * Q4MOE_TAIL_AUTO the pages' choice, the page 52 tail of Q4 when gate and
+ * up share a width (page 57, gate-up-mma.ts) and MLX's compiled SwiGLU
+ * (Q4MOE_TAIL_MLX) when they differ (page 57, mixed-gate-up-factored.ts).
  */
 typedef struct q4moe_trellis_layout {
     int64_t hidden_size;       /* H: a multiple of block_size                 */
@@ -419,9 +443,10 @@ int q4moe_trellis_pack_slab(const q4moe_trellis_layout_t *layout,
  * Arguments as q4moe_gate_up_swiglu_ex: x device bf16 [T][H] (16-byte
  * aligned), row offsets and the token map on the device, out device bf16
  * [M][I].  opts may be NULL; num_tokens, gate_f32 and up_f32 as for Q4;
- * kernel, matvec_tile and workspace must be 0.  One kernel (a warp per
- * output row, each decoded weight serving up to 8 grouped rows); decoding
- * is integer arithmetic, so the kernel is bound by the integer pipe.
+ * tail any Q4MOE_TAIL_*; kernel, matvec_tile and workspace must be 0.
+ * One kernel (a warp per output row, each decoded weight serving up to 8
+ * grouped rows); decoding is integer arithmetic, so the kernel is bound by
+ * the integer pipe.
  */
 int q4moe_trellis_gate_up_swiglu(const void *x,
                                  const q4moe_trellis_slabs_t *expert_slabs,
@@ -451,6 +476,11 @@ int64_t q4moe_launch_count(void);
  */
 int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
                      int64_t n, uint16_t *res, cudaStream_t stream);
+
+/* The same for the MLX tail (Q4MOE_TAIL_MLX), with the same arguments and
+ * result layout. */
+int q4moe_debug_tail_mlx(const uint16_t *gate_bf16, const uint16_t *up_bf16,
+                         int64_t n, uint16_t *res, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

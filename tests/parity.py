@@ -34,9 +34,10 @@ def _near_midpoint(v: np.ndarray, tol: np.ndarray) -> np.ndarray:
 
 
 def compare(gpu: dict, orc: dict, gs: np.ndarray, us: np.ndarray, H: int,
-            exact: bool = False) -> dict:
+            exact: bool = False, tail: str = "page") -> dict:
     """gpu: out (uint16), gate32/up32 (f32); orc: out, gate32, up32, gabs,
     uabs; gs/us: per-element row scales.  All arrays share one shape.
+    tail: the SwiGLU tail the call ended with ("page" or "mlx").
     Raises AssertionError with a summary on failure; returns statistics."""
     out_g, out_o = gpu["out"], orc["out"]
     assert out_g.shape == out_o.shape
@@ -75,14 +76,15 @@ def compare(gpu: dict, orc: dict, gs: np.ndarray, us: np.ndarray, H: int,
         np.sum(eg > 1e-5 * np.abs(og)) + np.sum(eu > 1e-5 * np.abs(ou)))
 
     # the tail given the GPU's own f32 values is exact
-    t = oracle.tail_array(g.ravel(), u.ravel())
+    tail_of = oracle.tail_mlx_array if tail == "mlx" else oracle.tail_array
+    t = tail_of(g.ravel(), u.ravel())
     bad = np.flatnonzero(t[:, 4] != out_g.ravel())
     assert bad.size == 0, f"tail: {bad.size} outputs differ from the " \
         f"oracle tail of the GPU's own gate/up"
 
     # output vs oracle: equal where the rounded inputs agree
     gT_g, uT_g = t[:, 0], t[:, 1]
-    to = oracle.tail_array(og.ravel(), ou.ravel())
+    to = tail_of(og.ravel(), ou.ravel())
     gT_o, uT_o = to[:, 0], to[:, 1]
     same = (gT_g == gT_o) & (uT_g == uT_o)
     dif = np.flatnonzero(out_g.ravel() != out_o.ravel())

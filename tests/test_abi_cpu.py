@@ -231,6 +231,19 @@ def test_host_argument_errors():
                                 FAKE, None) == q.ERR_INVALID_ARG
     assert lib.q4moe_debug_tail(None, None, 4, None, None) == \
         q.ERR_INVALID_ARG
+    assert lib.q4moe_debug_tail_mlx(None, None, 4, None, None) == \
+        q.ERR_INVALID_ARG
+    # the tail option: MLX's is for trellis codes only, values outside the
+    # three and a nonzero reserved field are refused
+    for tail, reserved in ((q.TAIL_MLX, 0), (3, 0), (-1, 0),
+                           (q.TAIL_PAGE, 1)):
+        o = q.q4moe_options_t()
+        o.tail, o.reserved1 = tail, reserved
+        assert _call(opts=o) == q.ERR_INVALID_ARG, (tail, reserved)
+    o = q.q4moe_options_t()
+    o.tail = q.TAIL_MLX
+    assert _call(opts=o) == q.ERR_INVALID_ARG
+    assert "MLX tail" in q.q4moe_last_error()
 
 
 def test_down_and_mlp_host_argument_errors():
@@ -260,7 +273,7 @@ def test_down_and_mlp_host_argument_errors():
     assert down(slabs=nd) == q.ERR_INVALID_ARG
     assert "down sections" in q.q4moe_last_error()
     for field, val in (("num_tokens", 4), ("up_f32", FAKE),
-                       ("workspace", FAKE)):
+                       ("workspace", FAKE), ("tail", q.TAIL_MLX)):
         o = q.q4moe_options_t()
         setattr(o, field, val)
         assert down(opts=o) == q.ERR_INVALID_ARG, field
@@ -334,6 +347,9 @@ def test_trellis_layout_and_host_errors():
     o = q.q4moe_options_t()
     o.kernel = q.KERNEL_GEMM
     assert call(opts=o) == q.ERR_INVALID_ARG           # no kernel choice
+    o = q.q4moe_options_t()
+    o.tail = 3
+    assert call(opts=o) == q.ERR_INVALID_ARG           # no such tail
     bad = q.q4moe_trellis_layout_t.from_buffer_copy(lay)
     bad.up_scales_offset = lay.slab_bytes - 2
     assert call(slabs=q.make_trellis_slabs(2, bad, base=FAKE)) == \
@@ -341,3 +357,7 @@ def test_trellis_layout_and_host_errors():
     import torch
     if not torch.cuda.is_available():
         assert call() in (q.ERR_CUDA, q.ERR_DEVICE)
+        for tail in (q.TAIL_AUTO, q.TAIL_PAGE, q.TAIL_MLX):
+            o = q.q4moe_options_t()
+            o.tail = tail                # accepted: fails only for the GPU
+            assert call(opts=o) in (q.ERR_CUDA, q.ERR_DEVICE)

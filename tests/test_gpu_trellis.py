@@ -2,10 +2,12 @@
 oracle, through the C ABI (q4moe_trellis_gate_up_swiglu).
 
 Pages of "@mlx-bun/inference 0.0.0-stage -> 1.0.0": page 57, trellis/
-gate-up-mma.ts and mixed-gate-up-factored.ts (factored row scale), page 54,
-trellis/codebook.ts (state and code value).  Integer activations in [-2, 2]
-make every sum exact, so those cases must give the oracle's bits; real
-inputs meet the bound of tests/parity.py."""
+gate-up-mma.ts and mixed-gate-up-factored.ts (factored row scale; the
+mixed-width kernel ends with MLX's compiled SwiGLU, the default tail when
+gate and up widths differ), page 54, trellis/codebook.ts (state and code
+value).  Integer activations in [-2, 2] make every sum exact, so those
+cases must give the oracle's bits; real inputs meet the bound of
+tests/parity.py."""
 from __future__ import annotations
 
 import numpy as np
@@ -55,7 +57,13 @@ def _problem(seed, counts, I, H, kg, ku, exact=False):
                 ku=ku)
 
 
-def _run(p, L=12, ptr_table=False, debug=True, tb=TB):
+def _auto_tail(p):
+    """The tail Q4MOE_TAIL_AUTO takes: the pages' mixed-width kernel's
+    (MLX) when the widths differ, page 52's otherwise."""
+    return "mlx" if p["kg"] != p["ku"] else "page"
+
+
+def _run(p, L=12, ptr_table=False, debug=True, tb=TB, tail=None):
     import torch
     E = p["gc"].shape[0]
     lay = q.q4moe_trellis_canonical_layout(p["H"], p["I"], tb, L, p["kg"],
@@ -84,6 +92,8 @@ def _run(p, L=12, ptr_table=False, debug=True, tb=TB):
     out = torch.full((max(M, 1), I), -1, dtype=torch.int16, device="cuda")
     o = q.q4moe_options_t()
     o.num_tokens = p["x"].shape[0]
+    if tail is not None:
+        o.tail = {"page": q.TAIL_PAGE, "mlx": q.TAIL_MLX}[tail]
     g32 = torch.full((max(M, 1), I), float("nan"), device="cuda")
     u32 = torch.full((max(M, 1), I), float("nan"), device="cuda")
     if debug:
@@ -99,16 +109,18 @@ def _run(p, L=12, ptr_table=False, debug=True, tb=TB):
     return res
 
 
-def _compare(p, gpu, L=12, exact=False, tb=TB):
+def _compare(p, gpu, L=12, exact=False, tb=TB, tail=None):
+    tail = tail or _auto_tail(p)
     orc = oracle.trellis_gate_up_swiglu(p["x"], p["gc"], p["uc"], p["gs"],
                                         p["us"], p["kg"], p["ku"], L, tb,
-                                        p["offs"], p["tok"])
+                                        p["offs"], p["tok"], tail=tail)
     e_of = np.repeat(np.arange(len(p["offs"]) - 1), np.diff(p["offs"]))
     rcp = np.float32(1.0 / 147.800537109375)
     fs = lambda s: (s.view(np.float16).astype(np.float32) * rcp  # noqa: E731
                     ).astype(np.float32)
     gsc, usc = fs(p["gs"])[e_of], fs(p["us"])[e_of]
-    return parity.compare(gpu, orc, gsc, usc, p["H"], exact=exact)
+    return parity.compare(gpu, orc, gsc, usc, p["H"], exact=exact,
+                          tail=tail)
 
 
 @pytest.mark.parametrize("kg,ku", [(4, 4), (2, 4), (3, 2), (3, 3), (2, 2),
@@ -173,10 +185,59 @@ def test_trellis_full_size_decode_sampled():
                            np.arange(I)])
     orc = oracle.trellis_gate_up_swiglu(p["x"], p["gc"], p["uc"], p["gs"],
                                         p["us"], 4, 3, 12, TB, offs, tok,
-                                        rows, cols)
+                                        rows, cols, tail="mlx")
     e_of = np.repeat(np.arange(w.E), counts)
     rcp = np.float32(1.0 / 147.800537109375)
     gsc = (p["gs"].view(np.float16).astype(np.float32) * rcp)[e_of]
     usc = (p["us"].view(np.float16).astype(np.float32) * rcp)[e_of]
     sel = {k: gpu[k][rows, cols] for k in ("out", "gate32", "up32")}
-    parity.compare(sel, orc, gsc[rows, cols], usc[rows, cols], w.H)
+    parity.compare(sel, orc, gsc[rows, cols], usc[rows, cols], w.H,
+                   tail="mlx")
+
+
+# ------------------------------------------------------------ MLX tail --
+
+def test_mlx_tail_exhaustive_bf16():
+    """All finite bf16 gate values, several up values: the device's MLX
+    tail (its sigmoid table) equals the oracle's bit for bit."""
+    import torch
+    g = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g = g[((g >> 7) & 0xFF) != 0xFF]
+    for up in (1.0, -3.0, 0.0078125, 250.0):
+        u = np.full(g.shape, syn.f32_to_bf16_bits(np.float32([up]))[0],
+                    np.uint16)
+        gd = torch.from_numpy(g.view(np.int16)).cuda()
+        ud = torch.from_numpy(u.view(np.int16)).cuda()
+        res = torch.empty((g.size, 4), dtype=torch.int16, device="cuda")
+        q.q4moe_debug_tail_mlx(gd, ud, g.size, res)
+        r = res.cpu().numpy().view(np.uint16)
+        t = oracle.tail_mlx_array(syn.bf16_bits_to_f32(g),
+                                  syn.bf16_bits_to_f32(u))
+        assert np.array_equal(r[:, 3], g)
+        for col, name in ((0, "sigmoid"), (1, "silu"), (2, "out")):
+            bad = np.flatnonzero(r[:, col] != t[:, col + 2])
+            assert bad.size == 0, f"{name}: {bad.size} differ, e.g. gate " \
+                f"{g[bad[:4]]}"
+
+
+@pytest.mark.parametrize("kg,ku,tail", [(4, 4, "mlx"), (3, 3, "mlx"),
+                                        (2, 4, "page"), (4, 3, "page"),
+                                        (4, 3, "mlx"), (2, 2, "page")])
+def test_trellis_tail_choice(kg, ku, tail):
+    """The tail asked for in the options, whatever the widths (AUTO's choice
+    is covered by every other test): bit-exact on exact inputs, within the
+    bound on real ones."""
+    p = _problem(kg * 10 + ku + 7, [3, 0, 9, 1, 20], 64, 512, kg, ku,
+                 exact=True)
+    _compare(p, _run(p, tail=tail), exact=True, tail=tail)
+    p = _problem(kg * 10 + ku + 8, [1, 7, 2, 13], 96, 1024, kg, ku)
+    _compare(p, _run(p, tail=tail), tail=tail)
+
+
+def test_mlx_and_page_tails_differ_on_device():
+    """The choice is live: with gate values spread over the sigmoid's curve,
+    the two tails give different outputs somewhere."""
+    p = _problem(91, [8, 8], 64, 512, 4, 3)
+    a = _run(p, tail="page", debug=False)["out"]
+    b = _run(p, tail="mlx", debug=False)["out"]
+    assert np.any(a != b)

@@ -40,8 +40,9 @@ int cuda_fail(cudaError_t err, const char *what) {
 // inconsistent device-side data.  One per device (a __device__ variable
 // exists once in every device context that loads the library).
 __device__ unsigned int g_status_word;
-// bf16 sigmoid of every bf16 gate value, built at the first call on a device
-__device__ uint16_t g_sigmoid_table[65536];
+// bf16 sigmoid of every bf16 gate value for each tail (page 52's, then
+// MLX's), built at the first call on a device
+__device__ uint16_t g_sigmoid_table[2 * q4moe::kSigmoidTable];
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -284,12 +285,17 @@ int check_slabs(const q4moe_slabs_t *slabs, int64_t H, int64_t I,
     return Q4MOE_OK;
 }
 
-int check_kernel_options(const q4moe_options_t &o) {
+int check_kernel_options(const q4moe_options_t &o, bool trellis = false) {
     if ((o.matvec_tile != 0 && o.matvec_tile != 16 && o.matvec_tile != 32 &&
          o.matvec_tile != 64 && o.matvec_tile != 128) ||
         o.kernel < Q4MOE_KERNEL_AUTO ||
-        o.kernel > Q4MOE_KERNEL_BATCH_INVARIANT || o.num_tokens < 0)
+        o.kernel > Q4MOE_KERNEL_BATCH_INVARIANT || o.num_tokens < 0 ||
+        o.tail < Q4MOE_TAIL_AUTO || o.tail > Q4MOE_TAIL_MLX ||
+        o.reserved1 != 0)
         return fail(Q4MOE_ERR_INVALID_ARG, "bad options");
+    if (!trellis && o.tail == Q4MOE_TAIL_MLX)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "the MLX tail is built for trellis codes only");
     if (!aligned(o.gate_f32, 4) || !aligned(o.up_f32, 4))
         return fail(Q4MOE_ERR_ALIGNMENT, "debug outputs must be 4-byte "
                                          "aligned");
@@ -587,7 +593,7 @@ int q4moe_trellis_gate_up_swiglu(const void *x,
     q4moe_options_t o{};
     if (opts != nullptr)
         o = *opts;
-    if ((rc = check_kernel_options(o)))
+    if ((rc = check_kernel_options(o, true)))
         return rc;
     if (o.kernel != Q4MOE_KERNEL_AUTO || o.matvec_tile != 0 ||
         o.workspace != nullptr || o.workspace_bytes != 0)
@@ -625,6 +631,10 @@ int q4moe_trellis_gate_up_swiglu(const void *x,
     a.tr_window = L.window_bits;
     a.tr_kg = L.gate_bits;
     a.tr_ku = L.up_bits;
+    // the pages' tail unless one is asked for: MLX's when the widths differ
+    // (the mixed-width kernel), page 52's otherwise
+    a.tail_mlx = o.tail == Q4MOE_TAIL_MLX ||
+                 (o.tail == Q4MOE_TAIL_AUTO && L.gate_bits != L.up_bits);
     a.matvec_max_rows = INT32_MAX;
     const cudaError_t err = q4moe::launch_trellis_gate_up(a, stream);
     if (err != cudaSuccess)
@@ -818,7 +828,22 @@ int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
     if (rc)
         return rc;
     cudaError_t err = q4moe::launch_debug_tail(gate_bf16, up_bf16, n, res,
-                                               d->sigmoid, stream);
+                                               d->sigmoid, false, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "debug tail launch");
+    return ok();
+}
+
+int q4moe_debug_tail_mlx(const uint16_t *gate_bf16, const uint16_t *up_bf16,
+                         int64_t n, uint16_t *res, cudaStream_t stream) {
+    if (n < 0 || (n > 0 && (!gate_bf16 || !up_bf16 || !res)))
+        return fail(Q4MOE_ERR_INVALID_ARG, "bad arguments");
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc)
+        return rc;
+    cudaError_t err = q4moe::launch_debug_tail(gate_bf16, up_bf16, n, res,
+                                               d->sigmoid, true, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, "debug tail launch");
     return ok();

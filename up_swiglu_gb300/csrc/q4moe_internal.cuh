@@ -40,8 +40,10 @@ struct GateUpArgs {
     int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
     int32_t matvec_last;         // no GEMM launch follows the matvec's
     int32_t gemm_min_tiles;      // > 0: the automatic choice (matvec_limit)
-    const uint16_t *sigmoid;     // sigmoid table: [65536] bf16, indexed by
-                                 // the bf16 bits of gateT
+    const uint16_t *sigmoid;     // sigmoid tables: [2][65536] bf16, indexed
+                                 // by the bf16 bits of gateT: the page 52
+                                 // tail's, then the MLX tail's
+    int32_t tail_mlx;            // 1: MLX's tail (trellis calls only)
     int32_t down;                // 1: the down projection (above)
     int32_t invariant;           // 1: batch-invariant matvec versions only
     int32_t q8;                  // 1: signed-byte weights (rows of H bytes)
@@ -118,13 +120,18 @@ cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                               cudaStream_t s);
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
                               int64_t n, uint16_t *res,
-                              const uint16_t *sigmoid, cudaStream_t s);
+                              const uint16_t *sigmoid, bool mlx,
+                              cudaStream_t s);
+// Fills both sigmoid tables (2 x 65,536 entries).
 cudaError_t launch_build_sigmoid_table(uint16_t *table, cudaStream_t s);
+// Entries of one sigmoid table; the MLX tail's table follows the page's.
+constexpr int kSigmoidTable = 65536;
 
 // ------------------------------------------------------------------------
 // bf16 helpers.  Rounding: nearest, ties to even (page 54, codebook.ts,
 // trellis_bf16), done by the hardware conversion (subnormals kept); every
-// value reaching it is finite.
+// value reaching it is finite, but for the MLX sigmoid's exponential past
+// FLT_MAX, an infinity, which converts to itself.
 __device__ __forceinline__ uint16_t bf16_rne(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
@@ -227,7 +234,24 @@ __device__ __forceinline__ uint16_t sigmoid_bf16_table(const uint16_t *table,
     return __ldg(table + gT);
 }
 
-// gateT, upT -> out (bf16 bits).  sig and silu are also returned.
+// The sigmoid of MLX's compiled SwiGLU in bf16 arithmetic, the tail of the
+// pages' mixed-width trellis kernel (page 57, mixed-gate-up-factored.ts):
+// every step evaluated in f32, correctly rounded, and rounded to bf16:
+// e = bf16(exp(|g|)), d = bf16(1 + e), y = bf16(1 / d), and the sigmoid is
+// y for negative g (not -0), else bf16(1 - y).  exp is taken in double and
+// rounded once to f32 (correctly rounded but for results within a double
+// ulp of an f32 rounding midpoint; all 65,536 inputs are tested against
+// the oracle).  Used only to fill the table, once per device.
+__device__ __forceinline__ uint16_t sigmoid_bf16_mlx(float g) {
+    const float e32 = __double2float_rn(exp((double)fabsf(g)));
+    const float e = bf16_f32(bf16_rne(e32));
+    const float d = bf16_f32(bf16_rne(__fadd_rn(1.0f, e)));
+    const uint16_t y = bf16_rne(__fdiv_rn(1.0f, d));
+    return g < 0.0f ? y : bf16_rne(__fsub_rn(1.0f, bf16_f32(y)));
+}
+
+// gateT, upT -> out (bf16 bits).  sig and silu are also returned.  Both
+// tails share the steps after the sigmoid; `table` selects the tail.
 __device__ __forceinline__ uint16_t swiglu_tail_bits(const uint16_t *table,
                                                      uint16_t gT, uint16_t uT,
                                                      uint16_t *sigT,

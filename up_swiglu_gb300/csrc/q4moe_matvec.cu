@@ -214,6 +214,7 @@ down_generic_kernel(GateUpArgs a) {
 __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
                                   int64_t n, uint16_t *res,
                                   const uint16_t *table) {
+    // (table: the page 52 tail's or the MLX tail's)
     grid_dependency_wait();
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
@@ -251,20 +252,25 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
 
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
                               uint16_t *res, const uint16_t *sigmoid,
-                              cudaStream_t s) {
+                              bool mlx, cudaStream_t s) {
     if (n == 0)
         return cudaSuccess;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
     return launch_pdl(debug_tail_kernel, dim3((unsigned)blocks), dim3(256), 0,
-                      s, g, u, n, res, sigmoid);
+                      s, g, u, n, res,
+                      mlx ? sigmoid + kSigmoidTable : sigmoid);
 }
 
 namespace {
-// sigmoid_bf16 of every bf16 value (the kernels' table)
+// The kernels' tables: sigmoid_bf16 (page 52 tail) and sigmoid_bf16_mlx
+// (MLX tail) of every bf16 value
 __global__ void build_sigmoid_table_kernel(uint16_t *table) {
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < 65536;
-         j += gridDim.x * blockDim.x)
-        table[j] = sigmoid_bf16(bf16_f32((uint16_t)j));
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < kSigmoidTable;
+         j += gridDim.x * blockDim.x) {
+        const float g = bf16_f32((uint16_t)j);
+        table[j] = sigmoid_bf16(g);
+        table[kSigmoidTable + j] = sigmoid_bf16_mlx(g);
+    }
 }
 }  // namespace
 

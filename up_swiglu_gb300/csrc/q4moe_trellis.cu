@@ -8,8 +8,10 @@
 //       block's T*k bits, wrapping (bit b is bit b%32 of word b/32);
 //   y(state) = the byte sum of state*34038481 + 76625530 (mod 2^32) - 510;
 //   G = sum_k y_k x_k in f32;  gate32 = G * (f32(scale) * RN32(1/147.8...));
-// then the page 52 SwiGLU tail on gate32/up32.  Gate and up may be coded at
-// different widths k.
+// then the SwiGLU tail on gate32/up32: page 52's, or MLX's compiled SwiGLU
+// in bf16 arithmetic, which the pages' mixed-width kernel ends with (the
+// sigmoid from a table of all bf16 gate values).  Gate and up may be coded
+// at different widths k.
 //
 // One warp owns an output row of one expert and up to 8 of its grouped rows
 // at a time (every decoded weight serves all of them); lane l owns runs
@@ -192,7 +194,13 @@ trellis_gate_up_kernel(GateUpArgs a) {
                     const float g32 = __fmul_rn(G, sg);
                     const float u32 = __fmul_rn(U, su);
                     const int64_t o = (int64_t)(p0 + m) * a.I + i;
-                    a.out[o] = swiglu_out(a.sigmoid, g32, u32);
+                    uint16_t sT, siluT;
+                    a.out[o] = a.tail_mlx
+                                   ? swiglu_tail_bits(
+                                         a.sigmoid + kSigmoidTable,
+                                         bf16_rne(g32), bf16_rne(u32), &sT,
+                                         &siluT)
+                                   : swiglu_out(a.sigmoid, g32, u32);
                     if (a.gate_f32)
                         a.gate_f32[o] = g32;
                     if (a.up_f32)

@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 6
+ABI_VERSION = 7
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -39,6 +39,13 @@ KERNEL_MATVEC = 1
 KERNEL_GEMM = 2
 KERNEL_BATCH_INVARIANT = 3
 
+# SwiGLU tail (q4moe_options_t.tail): AUTO = the pages' choice (page 52's,
+# MLX's for trellis codes whose gate and up widths differ), PAGE = page 52's,
+# MLX = MLX's compiled SwiGLU in bf16 arithmetic (trellis calls only).
+TAIL_AUTO = 0
+TAIL_PAGE = 1
+TAIL_MLX = 2
+
 # Every symbol include/q4moe.h declares (checked by the CPU tests).
 EXPORTS = (
     "q4moe_abi_version", "q4moe_last_error", "q4moe_canonical_layout",
@@ -48,7 +55,7 @@ EXPORTS = (
     "q4moe_gate_up_swiglu_noalloc", "q4moe_pack_slab_down",
     "q4moe_down_proj", "q4moe_expert_mlp", "q4moe_canonical_layout_format",
     "q4moe_trellis_canonical_layout", "q4moe_trellis_pack_slab",
-    "q4moe_trellis_gate_up_swiglu",
+    "q4moe_trellis_gate_up_swiglu", "q4moe_debug_tail_mlx",
 )
 
 # Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
@@ -113,7 +120,9 @@ class q4moe_options_t(ctypes.Structure):
                 ("kernel", ctypes.c_int32),
                 ("matvec_tile", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64),
+                ("tail", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -161,6 +170,7 @@ def load(build_if_missing: bool = True):
                                     [_P, ctypes.POINTER(ctypes.c_uint32),
                                      ctypes.c_int]),
             "q4moe_debug_tail": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+            "q4moe_debug_tail_mlx": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
             "q4moe_launch_count": (ctypes.c_int64, []),
             "q4moe_workspace_bytes": (ctypes.c_int64, [_I64, _I64]),
             "q4moe_gate_up_swiglu_noalloc": (ctypes.c_int,
@@ -357,6 +367,11 @@ def q4moe_launch_count() -> int:
 def q4moe_debug_tail(gate_bf16, up_bf16, n, res, stream=None) -> None:
     _check(load().q4moe_debug_tail(_ptr(gate_bf16), _ptr(up_bf16), n,
                                    _ptr(res), _stream(stream)))
+
+
+def q4moe_debug_tail_mlx(gate_bf16, up_bf16, n, res, stream=None) -> None:
+    _check(load().q4moe_debug_tail_mlx(_ptr(gate_bf16), _ptr(up_bf16), n,
+                                       _ptr(res), _stream(stream)))
 
 
 # ------------------------------------------------------- slab construction --
