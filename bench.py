@@ -47,6 +47,17 @@ OP_METRIC = {
 }
 
 
+def swiglu_tail(fmt: str) -> str:
+    """The tail a call in this format ends with under the default option
+    (the pages' choice): MLX's compiled SwiGLU for trellis codes whose gate
+    and up widths differ, page 52's otherwise."""
+    if fmt.startswith("trellis"):
+        kg, ku = fmt.split(":")[1].split(",")
+        if kg != ku:
+            return "mlx"
+    return "page"
+
+
 def op_metric(op: str, fmt: str) -> str:
     m = OP_METRIC[op]
     if fmt.startswith("trellis"):
@@ -426,7 +437,7 @@ def oracle_sample(w: syn.Workload, g: dict, budget_s: float, nthreads=0,
             r = oracle.trellis_gate_up_swiglu(
                 g["x"], g["gate_w"][:Ew], g["up_w"][:Ew], g["gate_s"][:Ew],
                 g["up_s"][:Ew], kg, ku, 12, 256, offs, tok, rr, cols,
-                nthreads=nthreads)
+                nthreads=nthreads, tail=swiglu_tail(fmt))
         elif op in ("gate_up", "mlp"):
             gu = oracle.q8_gate_up_swiglu if fmt == "q8" else \
                 oracle.gate_up_swiglu_sampled
@@ -519,7 +530,8 @@ def run_reference(args, w, rank, world):
         "dtype": "f64", "data": "synthetic (seeded generator)",
         "config": {"workload": w.name, "op": op, "format": fmt, "E": w.E,
                    "H": w.H, "I": w.I, "tokens": w.T, "top_k": w.topk,
-                   "routed_rows": w.routed_rows, "repeats": w.repeats},
+                   "routed_rows": w.routed_rows, "repeats": w.repeats,
+                   "tail": swiglu_tail(fmt) if op != "down" else None},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
                          "cores": threads, "kind": "oracle",
                          "sample": f"{rows} routed rows x all their outputs "
@@ -686,6 +698,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generator; no dataset)",
             "config": {"workload": w.name, "op": op, "format": fmt,
+                       "tail": swiglu_tail(fmt) if op != "down" else None,
                        "E": w.E, "H": w.H, "I": w.I,
                        "tokens": w.T, "top_k": w.topk,
                        "routed_rows": w.routed_rows, "repeats": w.repeats,
