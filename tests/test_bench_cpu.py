@@ -88,3 +88,14 @@ def test_reference_arm_rank0_prints_one_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s",
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_tail_reported_for_each_format():
+    """The config's tail is the library's default choice: MLX's for
+    trellis codes of different gate and up widths, page 52's otherwise."""
+    import bench
+    assert bench.swiglu_tail("q4") == "page"
+    assert bench.swiglu_tail("q8") == "page"
+    assert bench.swiglu_tail("trellis:4,4") == "page"
+    assert bench.swiglu_tail("trellis:4,3") == "mlx"
+    assert bench.swiglu_tail("trellis:2,4") == "mlx"
