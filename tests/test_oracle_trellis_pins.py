@@ -89,12 +89,15 @@ def _decode_rows(oracle_mod, codes, H, Tb, k, L):
     return out.reshape(*codes.shape[:-1], H)
 
 
-@pytest.mark.parametrize("kg,ku", [(4, 4), (2, 4), (3, 2)])
-def test_gate_up_exact_integer_brute_force(oracle_mod, kg, ku):
+@pytest.mark.parametrize("kg,ku,tail", [(4, 4, "page"), (2, 4, "page"),
+                                        (3, 2, "page"), (4, 3, "mlx"),
+                                        (2, 2, "mlx")])
+def test_gate_up_exact_integer_brute_force(oracle_mod, kg, ku, tail):
     """Integer activations in [-2, 2]: G and U are exact integers (int64
     matmul of the decoded code values), gate32 = RN32(G * scale) with the
     factored scale formed in numpy float32, and the output is the exact
-    tail; gate and up of different widths are decoded each with its own."""
+    tail (page 52's, or MLX's in bf16 arithmetic); gate and up of different
+    widths are decoded each with its own."""
     E, I, H, T, L, Tb = 2, 8, 512, 3, 12, 256
     rng = np.random.default_rng(kg * 10 + ku)
     gc = syn.words_u32(kg, 5, E * I * (H * kg // 32)).reshape(E, I, -1)
@@ -107,7 +110,8 @@ def test_gate_up_exact_integer_brute_force(oracle_mod, kg, ku):
     offs, tok, _ = oracle_mod.group_rows(topk, E)
     d = oracle_mod.trellis_gate_up_swiglu(x, gc, uc, gsv.view(np.uint16),
                                           usv.view(np.uint16), kg, ku, L, Tb,
-                                          offs, tok)
+                                          offs, tok, tail=tail)
+    exact_out = X.exact_mlx_out_bits if tail == "mlx" else X.exact_out_bits
     yg = _decode_rows(oracle_mod, gc, H, Tb, kg, L)
     yu = _decode_rows(oracle_mod, uc, H, Tb, ku, L)
     rcp = np.float32(1.0 / 147.800537109375)
@@ -122,8 +126,8 @@ def test_gate_up_exact_integer_brute_force(oracle_mod, kg, ku):
         assert np.array_equal(d["gate32"][p], g32)
         assert np.array_equal(d["up32"][p], u32)
         for i in range(I):
-            assert d["out"][p, i] == X.exact_out_bits(float(g32[i]),
-                                                      float(u32[i])), (p, i)
+            assert d["out"][p, i] == exact_out(float(g32[i]),
+                                               float(u32[i])), (p, i)
 
 
 def test_trellis_sampled_equals_full_and_rejects_bad_geometry(oracle_mod):
