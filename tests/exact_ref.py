@@ -113,19 +113,51 @@ def exact_sigmoid_f32_chain(g: float) -> float:
 
 
 @functools.lru_cache(maxsize=1)
+def exact_sigmoid_f32_table():
+    """exact_sigmoid_f32_chain of every finite bf16 gateT pattern b (NaN for
+    the non-finite patterns), as f32 values held in Python floats."""
+    s32 = [math.nan] * 65536
+    for b in range(65536):
+        if (b >> 7) & 0xFF == 0xFF:
+            continue
+        s32[b] = exact_sigmoid_f32_chain(bf16_value(b))
+    return s32
+
+
+@functools.lru_cache(maxsize=1)
 def exact_tail_tables():
     """For every finite bf16 gateT pattern b: (sigmoidT bits, siluT bits),
     from the exact chain above.  Non-finite patterns hold -1."""
     sig = np.full(65536, -1, dtype=np.int64)
     silu = np.full(65536, -1, dtype=np.int64)
+    s32 = exact_sigmoid_f32_table()
     for b in range(65536):
         if (b >> 7) & 0xFF == 0xFF:
             continue
         g = bf16_value(b)
-        sT = round_bf16(exact_sigmoid_f32_chain(g))
+        sT = round_bf16(s32[b])
         siluT = round_bf16(mul_f32(g, sT))
         sig[b] = bf16_bits(sT)
         silu[b] = bf16_bits(siluT)
+    return sig, silu
+
+
+@functools.lru_cache(maxsize=1)
+def exact_tail_tables_f32_sigmoid():
+    """The 'sigmoid kept in f32' reading of the tail: for every finite bf16
+    gateT pattern b, (sigmoidT bits, siluT bits) with
+    siluT = bf16(RN32(gateT * s32)), s32 the exact f32 chain itself (not
+    rounded to bf16 first); sigmoidT is still bf16(s32).  Non-finite
+    patterns hold -1."""
+    sig = np.full(65536, -1, dtype=np.int64)
+    silu = np.full(65536, -1, dtype=np.int64)
+    s32 = exact_sigmoid_f32_table()
+    for b in range(65536):
+        if (b >> 7) & 0xFF == 0xFF:
+            continue
+        g = bf16_value(b)
+        sig[b] = bf16_bits(round_bf16(s32[b]))
+        silu[b] = bf16_bits(round_bf16(mul_f32(g, s32[b])))
     return sig, silu
 
 

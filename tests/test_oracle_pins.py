@@ -112,6 +112,27 @@ def test_tail_sigmoid_rounding_matters(oracle_mod):
     assert diff > 0
 
 
+def test_tail_f32_sigmoid_reading_exhaustive(oracle_mod):
+    """The oracle's alternative reading (silu_mode 1: the sigmoid kept in
+    f32 for the silu product) on all 65,536 bf16 gate values against the
+    exact chain: 300-bit exp, every step rounded by rational arithmetic,
+    siluT = bf16(RN32(gateT * s32)); and out = bf16(siluT * upT) for two
+    up values, one of them negative."""
+    sig, silu = X.exact_tail_tables_f32_sigmoid()
+    keep = np.nonzero(sig >= 0)[0]
+    g = np.array([X.bf16_value(int(b)) for b in keep], np.float32)
+    for up in (1.0, -2.75):
+        r = oracle_mod.tail_array(g, np.full_like(g, up), silu_mode=1)
+        assert np.array_equal(r[:, 0], keep.astype(np.uint16))
+        assert np.array_equal(r[:, 2], sig[keep].astype(np.uint16))
+        bad = np.nonzero(r[:, 3] != silu[keep].astype(np.uint16))[0]
+        assert bad.size == 0, [hex(int(keep[i])) for i in bad[:10]]
+        uT = X.round_bf16(up)
+        want = np.array([X.bf16_bits(X.round_bf16(X.mul_f32(
+            X.bf16_value(int(s)), uT))) for s in silu[keep]], np.uint16)
+        assert np.array_equal(r[:, 4], want)
+
+
 # -------------------------------------------------- worked example (golden) --
 
 def test_worked_example(oracle_mod):
