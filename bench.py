@@ -11,10 +11,15 @@ One step = one pass of the whole path over one batch of synthetic input:
     different expert slab from a pool larger than 4x L2, captured once in a
     CUDA graph and replayed.
 Inputs stay resident in HBM; every step streams its weights from HBM (the
-weight pool of every workload is larger than L2).  Prints one JSON line.
+weight pool of every workload is larger than L2).  Prints one JSON line for
+the headline workload (by default the prefill, 160 experts, top-8, 4096
+tokens, H=5120, I=1536: the largest one that fits one GPU) with a
+"per_config" object holding the other workloads of the same operation and
+format, timed in the same process (and the single-expert decode once more
+with one slab reused, its weights L2-resident).
 
   python bench.py [--workload NAME] [--op gate_up|down|mlp] [--steps K]
-                  [--warmup W] [--gpus N]
+                  [--warmup W] [--gpus N] [--no-per-config]
   python bench.py --impl reference ...   (the CPU oracle, timed alone)
 """
 from __future__ import annotations
@@ -67,13 +72,15 @@ def op_metric(op: str, fmt: str) -> str:
 
 OP_ENTRY = {"gate_up": "q4moe_gate_up_swiglu", "down": "q4moe_down_proj",
             "mlp": "q4moe_expert_mlp"}
-DEFAULT_WORKLOAD = "expert1_h4096_i1536_m1_x1000"
+DEFAULT_WORKLOAD = "moe160_top8_t4096_h5120_i1536"
+# seconds of untimed steps, sampled for clocks, before the timed region
+SUSTAIN_S = 1.0
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -101,7 +108,12 @@ def parse_args():
     ap.add_argument("--matvec-tile", type=int, default=0,
                     choices=[0, 16, 32, 64, 128],
                     help="unit height of the TMA matvec (0: per call)")
-    return ap.parse_args()
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the headline workload only")
+    ap.add_argument("--l2-hot", action="store_true",
+                    help="single-expert decode: every call on the same slab "
+                         "(weights L2-resident)")
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------ workload math --
@@ -171,19 +183,36 @@ def load_traffic(workload: str, kernel_file: str):
 
 # ---------------------------------------------------------------- clocks --
 
+def device_smi_id(device_index: int) -> str:
+    """The GPU's id for nvidia-smi --id: its UUID (unique under
+    CUDA_VISIBLE_DEVICES, where the torch ordinal is not the physical
+    index), else the ordinal."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        if u:
+            return u if u.startswith(("GPU-", "MIG-")) else "GPU-" + u
+    except Exception:           # noqa: BLE001 - any failure: the ordinal
+        pass
+    return str(device_index)
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms.  mark()
+    starts a new segment (e.g. the timed region after a sustain loop);
+    summary() reports the whole run and each segment."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, device_index: int):
-        self.dev = device_index
+        self.dev = device_smi_id(device_index)
         self.proc = None
         self.file = None
+        self.marks = []
 
     def __enter__(self):
         try:
@@ -197,6 +226,23 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _rows(self):
+        rows = []
+        if self.file is None:
+            return rows
+        with open(self.file.name) as f:
+            for line in f:
+                if not line.endswith("\n"):
+                    break                    # a row still being written
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        return rows
+
+    def mark(self):
+        """Start a new segment: the rows sampled from now on."""
+        self.marks.append(len(self._rows()))
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -205,37 +251,43 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if self.proc is None or self.file is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
-                    "samples": 0}
-        self.file.flush()
-        rows = []
-        with open(self.file.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append(parts)
-                except ValueError:
-                    pass
-        os.unlink(self.file.name)
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+    @staticmethod
+    def _stats(rows):
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[9]) or 0.0) > 0.0]
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         reasons = set()
-        for r in rows:
+        for r in load:
             for n, v in zip(names, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
-        power = [float(r[3]) for r in rows
-                 if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(rows),
+                "samples_under_load": len(load),
                 "power_w_max": max(power) if power else None}
+
+    def summary(self):
+        """Clock statistics of the samples taken while the GPU was busy
+        (utilization above 0), over the whole run, and per segment."""
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "segments": []}
+        rows = self._rows()
+        os.unlink(self.file.name)
+        out = self._stats(rows)
+        bounds = [0] + self.marks + [len(rows)]
+        out["segments"] = [self._stats(rows[a:b])
+                           for a, b in zip(bounds[:-1], bounds[1:])]
+        return out
 
 
 # ------------------------------------------------------------- GPU set-up --
@@ -245,7 +297,8 @@ class GpuWorkload:
 
     def __init__(self, w: syn.Workload, kernel: str, device: int,
                  use_workspace: bool = True, matvec_tile: int = 0,
-                 op: str = "gate_up", fmt: str = "q4"):
+                 op: str = "gate_up", fmt: str = "q4",
+                 l2_hot: bool = False):
         import torch
         from up_swiglu_gb300 import q4moe as q
         self.torch, self.q, self.w, self.op = torch, q, w, op
@@ -262,7 +315,9 @@ class GpuWorkload:
             L = q.q4moe_canonical_layout_format(
                 w.H, w.I, q.FORMAT_Q8 if fmt == "q8" else q.FORMAT_Q4)
         self.layout = L
-        if w.repeats > 1:
+        if w.repeats > 1 and l2_hot:
+            pool_experts = 1                  # one slab, L2-resident
+        elif w.repeats > 1:
             # distinct expert slabs, more than 4x L2 in total
             pool_experts = max(8, math.ceil(4 * L2_BYTES / L.slab_bytes) + 1)
             pool_experts = min(pool_experts, w.repeats)
@@ -544,92 +599,11 @@ def run_reference(args, w, rank, world):
     return 0
 
 
-def main():
-    args = parse_args()
-    w = syn.WORKLOADS[args.workload]
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
-        return run_reference(args, w, rank, world)
-
-    import torch
-    from up_swiglu_gb300 import q4moe as q
-    if not torch.cuda.is_available():
-        print(json.dumps({"error": "no CUDA device"}))
-        return 1
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    q.load()
-
-    op, fmt = args.op, args.format
-    if fmt == "trellis":
-        if op != "gate_up":
-            print(json.dumps({"error": "the trellis format has gate/up only"}))
-            return 1
-        fmt = f"trellis:{args.trellis_bits}"
-    gw = GpuWorkload(w, args.kernel, local,
-                     use_workspace=not args.no_workspace,
-                     matvec_tile=args.matvec_tile, op=op, fmt=fmt)
-    units = workload_units(w, gw.topk_host, gw.pool_experts, op, fmt)
-    dev = gw.dev
-    stream = gw.stream
-
-    # CPU baseline (host threads only, before the timed GPU work)
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        spr, n, threads = oracle_sample(w, gw.host, args.cpu_seconds,
-                                        op=op, fmt=fmt)
-        v, _ = cpu_value(w, units, spr)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
-               "kind": "oracle",
-               "sample": f"{n} routed rows x all their outputs "
-                         f"(~{args.cpu_seconds:.0f} s), scaled to the step's "
-                         f"{w.routed_rows * w.repeats} rows"}
-
-    # warm-up
-    for _ in range(max(args.warmup, 3)):
-        gw.enqueue_step()
-    torch.cuda.synchronize(dev)
-    assert q.q4moe_device_status(stream, clear=True) == 0
-
-    # timed region: K steps, barrier + synchronize on both sides
-    ev = [(torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ev_end = [torch.cuda.Event(enable_timing=True)
-              for _ in range(args.steps)]
-    n0 = q.q4moe_launch_count()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_stop = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for k in range(args.steps):
-            gw.enqueue_step(ev[k])
-            ev_end[k].record(stream)
-        t_stop.record(stream)
-        torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
-    launches = q.q4moe_launch_count() - n0
-    if gw.graph is not None:
-        launches = gw.launches_per_step * args.steps
-    total_ms = t_start.elapsed_time(t_stop)
-    gate_up_ms = [ev[k][1].elapsed_time(ev_end[k]) for k in range(args.steps)]
-    total_ms = max_over_ranks(total_ms, dist, dev)
-    ms_per_step = total_ms / args.steps
-    value, tflops = job_rates(units, args.steps, world, total_ms)
-    clocks = clk.summary()
-
-    # roofline of the dominant kernel: the fused call(s) of the operation
-    peaks, peak_src = load_peaks()
-    gu_ms = statistics.mean(gate_up_ms)
-    per_launch_ms = gu_ms / gw.calls
+def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
+                timed_s):
+    """Roofline of the fused call(s) of the operation: HBM for the decode
+    kernels, the tensor core for the GEMM (burst peak unless the timed
+    region lasts seconds)."""
     rows_per_expert = (w.routed_rows if w.repeats > 1 else
                        w.routed_rows / units["touched_experts"])
     # (the trellis kernel decodes every weight once per 8 rows at any size:
@@ -642,7 +616,7 @@ def main():
         bytes_per_launch = units["bytes"] / gw.calls
         achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 2),
+        return {"bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": load_traffic(
@@ -651,17 +625,113 @@ def main():
                 "kernel": ("q4moe_trellis_gate_up_swiglu (integer-bound "
                            "decode)" if gw.trellis
                            else f"{OP_ENTRY[op]} matvec"),
+                "algorithmic_bytes_per_launch": int(bytes_per_launch),
                 "peak_source": f"hbm_gbs of {peak_src}"}
-    else:
-        flops_per_launch = units["flops"] / gw.calls
-        achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 2),
-                "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(traffic_key, "q4moe_gemm.cu"),
-                "kernel": f"{OP_ENTRY[op]} gemm",
-                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+    flops_per_launch = units["flops"] / gw.calls
+    achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
+    sustained = timed_s >= 2.0
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = peaks[key]
+    return {"bound": "tensor", "achieved": round(achieved, 2),
+            "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": load_traffic(traffic_key, "q4moe_gemm.cu"),
+            "kernel": f"{OP_ENTRY[op]} gemm (the call's launches: row copy "
+                      "and tensor-core GEMM)",
+            "algorithmic_flops_per_launch": int(flops_per_launch),
+            "peak_source": f"{key} of {peak_src}"}
+
+
+def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
+            headline=False, l2_hot=False):
+    """Set up one workload, time it (warm-up, then exactly args.steps steps
+    between barriers and synchronisations), time it end to end with host
+    buffers, and time the oracle on a bounded sample of it.  Returns the
+    measured fields; the headline workload also samples clocks over an
+    untimed sustain loop before its timed region."""
+    import torch
+    q = __import__("up_swiglu_gb300.q4moe", fromlist=["q4moe"])
+    gw = GpuWorkload(w, args.kernel, local,
+                     use_workspace=not args.no_workspace,
+                     matvec_tile=args.matvec_tile, op=op, fmt=fmt,
+                     l2_hot=l2_hot)
+    units = workload_units(w, gw.topk_host, gw.pool_experts, op, fmt)
+    dev = gw.dev
+    stream = gw.stream
+
+    # CPU baseline (host threads only, before the timed GPU work)
+    cpu = None
+    if rank == 0 and cpu_seconds > 0:
+        spr, n, threads = oracle_sample(w, gw.host, cpu_seconds,
+                                        op=op, fmt=fmt)
+        v, _ = cpu_value(w, units, spr)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} routed rows x all their outputs "
+                         f"(~{cpu_seconds:.0f} s), scaled to the step's "
+                         f"{w.routed_rows * w.repeats} rows"}
+
+    # warm-up
+    for _ in range(max(args.warmup, 3)):
+        gw.enqueue_step()
+    torch.cuda.synchronize(dev)
+    assert q.q4moe_device_status(stream, clear=True) == 0
+
+    clk = ClockSampler(local) if headline else None
+    if clk is not None:
+        clk.__enter__()
+    sustain = None
+    try:
+        if clk is not None:
+            # untimed sustain loop (sampled): at least SUSTAIN_S seconds
+            t0 = time.time()
+            n_sus = 0
+            while time.time() - t0 < SUSTAIN_S:
+                for _ in range(8):
+                    gw.enqueue_step()
+                torch.cuda.synchronize(dev)
+                n_sus += 8
+            sustain = {"seconds": round(time.time() - t0, 3),
+                       "steps": n_sus}
+            clk.mark()
+        # timed region: K steps, barrier + synchronize on both sides
+        ev = [(torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        ev_end = [torch.cuda.Event(enable_timing=True)
+                  for _ in range(args.steps)]
+        n0 = q.q4moe_launch_count()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_stop = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            gw.enqueue_step(ev[k])
+            ev_end[k].record(stream)
+        t_stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        if clk is not None:
+            clk.mark()
+    finally:
+        if clk is not None:
+            clk.__exit__(None, None, None)
+    launches = q.q4moe_launch_count() - n0
+    if gw.graph is not None:
+        launches = gw.launches_per_step * args.steps
+    total_ms = t_start.elapsed_time(t_stop)
+    call_ms = [ev[k][1].elapsed_time(ev_end[k]) for k in range(args.steps)]
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    ms_per_step = total_ms / args.steps
+    value, tflops = job_rates(units, args.steps, world, total_ms)
+
+    peaks, peak_src = load_peaks()
+    per_launch_ms = statistics.mean(call_ms) / gw.calls
+    roof = roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks,
+                       peak_src, total_ms * 1e-3)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (activations + routing) from pinned memory, D2H of the outputs
@@ -689,12 +759,108 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_value = units["weight_bytes"] * world / (e2e_ms * 1e-3) / 1e9
     status = q.q4moe_device_status(stream, clear=True)
+    res = {
+        "gw": gw, "units": units, "ms_per_step": ms_per_step,
+        "value": value, "tflops": tflops, "roofline": roof, "cpu": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "launches": int(launches), "status": status,
+        "call_ms": statistics.mean(call_ms),
+        "clocks": clk.summary() if clk is not None else None,
+        "sustain": sustain,
+    }
+    return res
+
+
+def release(res):
+    """Free a measured workload's device memory before the next one."""
+    import torch
+    res.pop("gw", None)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def per_config_entry(w, res, l2_hot=False):
+    gw_pool = res["units"]["touched_experts"]
+    return {
+        "workload": w.name + (" (one slab reused: L2-resident weights)"
+                              if l2_hot else ""),
+        "routed_rows": w.routed_rows, "repeats": w.repeats,
+        "touched_experts": gw_pool,
+        "ms_per_step": round(res["ms_per_step"], 5),
+        "value": round(res["value"], 3), "unit": "GB/s",
+        "tflops": round(res["tflops"], 3),
+        "roofline": res["roofline"],
+        "cpu_baseline": res["cpu"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+        "device_status": res["status"],
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = syn.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    from up_swiglu_gb300 import q4moe as q
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    q.load()
+
+    op, fmt = args.op, args.format
+    if fmt == "trellis":
+        if op != "gate_up":
+            print(json.dumps({"error": "the trellis format has gate/up only"}))
+            return 1
+        fmt = f"trellis:{args.trellis_bits}"
+    cpu_s = 0.0 if args.no_cpu_baseline else args.cpu_seconds
+
+    # the other workloads of this operation and format first (each freed
+    # before the next), then the headline one
+    per_config = {}
+    if not args.no_per_config:
+        for name in sorted(syn.WORKLOADS,
+                           key=lambda n: syn.WORKLOADS[n].routed_rows *
+                           syn.WORKLOADS[n].E):
+            if name == w.name:
+                continue
+            wc = syn.WORKLOADS[name]
+            variants = [False] + ([True] if wc.repeats > 1 else [])
+            for hot in variants:
+                r = measure(args, wc, local, dist, world, rank, op, fmt,
+                            0.0 if hot else max(1.0, cpu_s / 4),
+                            l2_hot=hot)
+                per_config[name + (":l2hot" if hot else "")] = \
+                    per_config_entry(wc, r, hot)
+                release(r)
+
+    res = measure(args, w, local, dist, world, rank, op, fmt, cpu_s,
+                  headline=True, l2_hot=args.l2_hot)
+    gw, units = res["gw"], res["units"]
+    clocks = res["clocks"]
+    timed = clocks["segments"][1] if len(clocks["segments"]) > 1 else clocks
+    sus = clocks["segments"][0] if len(clocks["segments"]) > 1 else None
 
     if rank == 0:
         line = {
-            "metric": op_metric(op, fmt), "value": round(value, 3), "unit": "GB/s",
+            "metric": op_metric(op, fmt), "value": round(res["value"], 3),
+            "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "ms_per_step": round(res["ms_per_step"], 4),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generator; no dataset)",
             "config": {"workload": w.name, "op": op, "format": fmt,
@@ -704,27 +870,38 @@ def main():
                        "routed_rows": w.routed_rows, "repeats": w.repeats,
                        "touched_experts": units["touched_experts"],
                        "weight_bytes_per_step": units["weight_bytes"],
-                       "l2": "weights larger than L2 every step "
-                             f"({gw.pool_experts} distinct expert slabs)",
+                       "flops_per_step": units["flops"],
+                       "l2": ("one slab reused every call (L2-resident "
+                              "weights)" if args.l2_hot else
+                              "weights larger than L2 every step "
+                              f"({gw.pool_experts} distinct expert slabs)"),
                        "kernel_choice": args.kernel,
                        "workspace": not args.no_workspace,
                        "matvec_tile": args.matvec_tile or "per call",
                        "parallelism": f"replicas x{world}" if world > 1
                        else "single GPU"},
-            "tflops": round(tflops, 3),
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s",
-                    "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": int(launches),
-            "clocks": {"sm_mhz": clocks["sm_mhz"],
+            "tflops": round(res["tflops"], 3),
+            "roofline": res["roofline"],
+            "cpu_baseline": res["cpu"],
+            "e2e": res["e2e"],
+            "gpu_launches": res["launches"],
+            "clocks": {"sm_mhz": timed["sm_mhz"],
                        "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"],
-                       "samples": clocks["samples"]},
-            "device_status": status,
+                       "samples": timed["samples_under_load"],
+                       "sustain": None if sus is None else {
+                           "seconds": res["sustain"]["seconds"],
+                           "sm_mhz": sus["sm_mhz"],
+                           "samples": sus["samples_under_load"],
+                           "reasons": sus["reasons"],
+                           "power_w_max": sus["power_w_max"]},
+                       "samples_total": clocks["samples_under_load"]},
+            "device_status": res["status"],
         }
+        if per_config:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
+    release(res)
     if dist is not None:
         dist.destroy_process_group()
     return 0

@@ -99,3 +99,66 @@ def test_tail_reported_for_each_format():
     assert bench.swiglu_tail("trellis:4,4") == "page"
     assert bench.swiglu_tail("trellis:4,3") == "mlx"
     assert bench.swiglu_tail("trellis:2,4") == "mlx"
+
+
+def test_clock_summary_keeps_busy_samples_and_segments(tmp_path):
+    """Clock statistics come from the samples taken while the GPU was busy;
+    mark() splits the run into a sustain segment and the timed region."""
+    import bench
+    rows = [
+        # idx, sm, max, power, active, hw, hw_th, sw_th, sw_cap, util
+        "0, 1995, 2070, 180.0, 0x0, Not Active, Not Active, Not Active, "
+        "Not Active, 0",
+        "0, 1800, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, "
+        "Active, 100",
+        "0, 1850, 2070, 1350.0, 0x0, Not Active, Not Active, Not Active, "
+        "Not Active, 100",
+        "0, 2000, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, "
+        "Not Active, 97",
+    ]
+    clk = bench.ClockSampler.__new__(bench.ClockSampler)
+    clk.proc = object()
+    clk.file = open(tmp_path / "clk.csv", "w+")
+    clk.marks = []
+    clk.file.write("\n".join(rows[:3]) + "\n")
+    clk.file.flush()
+    clk.mark()
+    clk.file.write(rows[3] + "\n" + "0, 17")   # last row still being written
+    clk.file.flush()
+    s = clk.summary()
+    assert s["samples"] == 4 and s["samples_under_load"] == 3
+    assert s["sm_mhz"] == 1850.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    sus, timed = s["segments"]
+    assert sus["samples_under_load"] == 2 and sus["sm_mhz"] == 1825.0
+    assert timed["samples_under_load"] == 1 and timed["sm_mhz"] == 2000.0
+    assert timed["reasons"] == []
+
+
+def test_gemm_roofline_takes_the_burst_peak_for_short_regions():
+    """A tensor-bound line is compared with the burst bf16 peak unless the
+    timed region lasts seconds; a decode line with the copy bandwidth."""
+    import types
+    import bench
+    from up_swiglu_gb300 import synthetic as syn
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0,
+             "bf16_tflops_sustained": 1700.0}
+    gw = types.SimpleNamespace(calls=1, trellis=False)
+    w = syn.WORKLOADS["moe160_top8_t4096_h5120_i1536"]
+    units = {"touched_experts": 160, "bytes": 1.4e9, "flops": 1.0e12,
+             "weight_bytes": 1.26e9}
+    r = bench.roofline_of(gw, w, units, "gate_up", "q4", 1.0, peaks,
+                          "measured", 0.1)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0
+    assert r["achieved"] == pytest.approx(1000.0)
+    assert r["frac"] == pytest.approx(0.5)
+    r = bench.roofline_of(gw, w, units, "gate_up", "q4", 1.0, peaks,
+                          "measured", 5.0)
+    assert r["peak"] == 1700.0
+    w3 = syn.WORKLOADS["moe128_top8_t32_h5120_i1536"]
+    units3 = {"touched_experts": 117, "bytes": 6.0e8, "flops": 8e9,
+              "weight_bytes": 5.9e8}
+    r = bench.roofline_of(gw, w3, units3, "gate_up", "q4", 0.2, peaks,
+                          "measured", 0.1)
+    assert r["bound"] == "hbm" and r["peak"] == 6000.0
+    assert r["achieved"] == pytest.approx(3000.0)

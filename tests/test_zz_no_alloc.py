@@ -43,8 +43,49 @@ def _outputs(d, offs, tok, noalloc):
     return out.cpu().numpy().view(np.uint16)
 
 
+def _gemm_reference(d, offs, tok):
+    """The regular entry point with the GEMM forced and a torch-allocated
+    workspace: the path the no-alloc call takes with its own scratch."""
+    import torch
+    M = int(tok.shape[0])
+    out = torch.full((M, d.p.I), -1, dtype=torch.int16, device="cuda")
+    ws = torch.empty(q.q4moe_workspace_bytes(M, d.p.H) + 256,
+                     dtype=torch.uint8, device="cuda")
+    o = q.q4moe_options_t()
+    o.kernel = q.KERNEL_GEMM
+    off = (-ws.data_ptr()) % 256
+    o.workspace = ws.data_ptr() + off
+    o.workspace_bytes = q.q4moe_workspace_bytes(M, d.p.H)
+    q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, offs, tok, M, d.p.H, d.p.I, out,
+                              o)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint16)
+
+
+def test_noalloc_gemm_path_uses_its_scratch_twice():
+    """One expert with 1280 rows at I = 4096: 5 x 32 GEMM tiles fill every
+    SM, so the automatic choice sends the call to the tensor-core GEMM, whose
+    row copy writes the library's scratch (1280 x 512 x 2 bytes) and whose
+    TMA loads read it back.  A different problem fills the scratch first;
+    then two calls in a row must match the regular entry point with its own
+    workspace bit for bit, each launching the row copy and the GEMM."""
+    p0 = hz.problem_with_counts(77, [1280], 4096, 512)
+    d0 = hz.upload(p0)
+    offs0, tok0, _ = hz.group(d0)
+    _outputs(d0, offs0, tok0, noalloc=True)      # other contents first
+    p = hz.problem_with_counts(78, [1280], 4096, 512)
+    d = hz.upload(p)
+    offs, tok, _ = hz.group(d)
+    want = _gemm_reference(d, offs, tok)
+    for _ in range(2):
+        n0 = q.q4moe_launch_count()
+        got = _outputs(d, offs, tok, noalloc=True)
+        assert q.q4moe_launch_count() - n0 == 2  # row copy + GEMM
+        assert np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("counts,I,H", [
-    ([0, 60, 130, 7, 257, 1, 90], 256, 512),      # tensor-core GEMM experts
+    ([0, 60, 130, 7, 257, 1, 90], 256, 512),      # matvec (automatic choice)
     ([3, 1, 8, 0, 2], 384, 1024),                 # matvec-only experts
 ])
 def test_noalloc_matches_regular_entry_point_twice(counts, I, H):

@@ -12,6 +12,7 @@
 // __device__ array, which exists once on every GPU that loads the library
 // and stays there until the process exits.  Nothing here calls cudaMalloc,
 // cudaFree or any allocating routine.
+#include <climits>
 #include <cstdio>
 #include <mutex>
 
@@ -66,6 +67,14 @@ extern "C" int q4moe_gate_up_swiglu_noalloc(
     if (M < 0 || H < 0)
         return q4moe::report_error(Q4MOE_ERR_INVALID_ARG,
                                    "M and H must be non-negative");
+    // bound M and H before forming M * H * 2 (no int64 overflow): beyond
+    // these the scratch could never hold the rows anyway
+    if (M > INT32_MAX || H > (INT64_C(1) << 24) ||
+        (M > 0 && M * H > (INT64_C(1) << 40)))
+        return q4moe::report_error(
+            Q4MOE_ERR_INVALID_ARG,
+            "q4moe_gate_up_swiglu_noalloc: M * H exceeds the library's "
+            "fixed scratch");
     const int64_t need = q4moe_workspace_bytes(M, H);
     if (need > (int64_t)Q4MOE_NOALLOC_SCRATCH_BYTES) {
         char msg[200];
