@@ -885,17 +885,25 @@ def main(argv=None):
             "cpu_baseline": res["cpu"],
             "e2e": res["e2e"],
             "gpu_launches": res["launches"],
-            "clocks": {"sm_mhz": timed["sm_mhz"],
+            # the timed region is too short for many samples (nvidia-smi
+            # samples every 50 ms): the clock record covers the untimed
+            # sustain loop of the same steps right before it as well
+            "clocks": {"sm_mhz": clocks["sm_mhz"],
                        "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"],
-                       "samples": timed["samples_under_load"],
+                       "samples": clocks["samples_under_load"],
+                       "power_w_max": clocks["power_w_max"],
+                       "window": "sustain loop of "
+                                 f"{res['sustain']['seconds']} s + timed "
+                                 "region",
+                       "timed_region": {
+                           "sm_mhz": timed["sm_mhz"],
+                           "samples": timed["samples_under_load"],
+                           "reasons": timed["reasons"]},
                        "sustain": None if sus is None else {
-                           "seconds": res["sustain"]["seconds"],
                            "sm_mhz": sus["sm_mhz"],
                            "samples": sus["samples_under_load"],
-                           "reasons": sus["reasons"],
-                           "power_w_max": sus["power_w_max"]},
-                       "samples_total": clocks["samples_under_load"]},
+                           "reasons": sus["reasons"]}},
             "device_status": res["status"],
         }
         if per_config:

@@ -42,7 +42,7 @@ int cuda_fail(cudaError_t err, const char *what) {
 __device__ unsigned int g_status_word;
 // bf16 sigmoid of every bf16 gate value for each tail (page 52's, then
 // MLX's), built at the first call on a device
-__device__ uint16_t g_sigmoid_table[2 * q4moe::kSigmoidTable];
+__device__ __align__(16) uint16_t g_sigmoid_table[2 * q4moe::kSigmoidTable];
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {

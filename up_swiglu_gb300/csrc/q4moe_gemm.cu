@@ -750,6 +750,9 @@ cudaError_t launch_gemm_kernel(const GateUpArgs &a, const XgMaps &maps,
 }  // namespace
 
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
+    const bool ts = gemm_tma_supported(a) && (a.down || a.xg != nullptr);
+    if (ts && a.down)                // mid is grouped already: no copy
+        return launch_gemm_tma(a, a.x, s);
     XgMaps maps;
     memset(&maps, 0, sizeof maps);
     if (a.down) {                    // mid is grouped already: no copy
@@ -771,6 +774,8 @@ cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
                           sizeof(int32_t) * (size_t)(a.E + 1), s, a)) !=
         cudaSuccess)
         return err;
+    if (ts)
+        return launch_gemm_tma(a, a.xg, s);
     return launch_gemm_kernel<true, false>(a, maps, s);
 }
 

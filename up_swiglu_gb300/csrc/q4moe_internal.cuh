@@ -105,6 +105,12 @@ cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
 bool matvec_tma_supported(const GateUpArgs &a);
 cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
+// The tcgen05 GEMM whose weights, dequantised tiles and token rows all move
+// through TMA-fed rings (q4moe_gemm_tma.cu), on token rows already in
+// grouped order (the workspace copy of x, or mid for the down projection).
+bool gemm_tma_supported(const GateUpArgs &a);
+cudaError_t launch_gemm_tma(const GateUpArgs &a, const uint16_t *rows,
+                           cudaStream_t s);
 cudaError_t launch_trellis_gate_up(const GateUpArgs &a, cudaStream_t s);
 // GEMM tiles over the output rows of one expert's 256 grouped rows: 128
 // intermediate rows (gate and up) per tile, or 256 output rows (two halves

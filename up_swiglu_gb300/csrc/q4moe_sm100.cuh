@@ -84,6 +84,45 @@ static __device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Non-blocking test of an mbarrier phase (no suspend: cheaper than
+// try_wait when the phase is usually complete already).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait by spinning on test_wait, for the one thread whose issue
+// rate sets the pace (the MMA issuer): returns false (and, the first time,
+// raises Q4MOE_DEV_WAIT_TIMEOUT) once the CTA has aborted or the wait ran
+// out (4 s).
+__device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort,
+                                          unsigned int *status) {
+    if (mbar_test_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity))
+            return true;
+        if ((it & 255u) == 0) {
+            if (*abort)
+                return false;
+            if (globaltimer_ns() - t0 > 4000000000ull) {
+                if (atomicExch((int *)abort, 1) == 0)
+                    atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag, used while draining copies
 // before exit (they land within microseconds; 0.2 s is ample).
 __device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity) {
@@ -255,6 +294,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// The same for 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+          "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for this thread's TMEM loads, naming the two 8-column destination
+// arrays as operands so that no read of them is moved above the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[8],
+                                                  uint32_t (&b)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]),
+                   "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(b[0]), "+r"(b[1]),
+                   "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),
+                   "+r"(b[7])
+                 :
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
