@@ -42,11 +42,12 @@
  *    device; "host" pointers are ordinary host memory.  Every buffer is
  *    borrowed: the caller owns it and keeps it alive until the work queued
  *    on `stream` has completed.
- *  - GPU entry points are asynchronous on `stream` and allocate no memory.
- *    They never synchronise the host, except once per device: the first
- *    call on a device fills a 128 KB table in the library's own device
- *    memory (the bf16 sigmoid of every bf16 value) and waits for it, so
- *    that first call must not be made while a stream is being captured.
+ *  - GPU entry points are asynchronous on `stream`, allocate no memory and
+ *    never synchronise the host (q4moe_device_status excepted).  The bf16
+ *    sigmoid of every bf16 value (128 KB per tail) is constant data of the
+ *    library image, so no call launches set-up work; the first call on a
+ *    device only looks up the device addresses of that table and of the
+ *    status word (host queries).
  *    Argument errors the host can see are returned before anything is
  *    launched.  Inconsistent data that only the
  *    GPU can see (row offsets, token indices, expert ids, slab pointers) sets
@@ -64,7 +65,7 @@
 extern "C" {
 #endif
 
-#define Q4MOE_ABI_VERSION 7
+#define Q4MOE_ABI_VERSION 8
 
 /* Slab base addresses and strides must be multiples of this (the pages use
  * 16 KiB, a multiple, for zero-copy residency slots; page 51 layout.ts). */
@@ -471,16 +472,30 @@ int64_t q4moe_launch_count(void);
 /*
  * Diagnostic: evaluate the device's SwiGLU tail alone.  For n elements,
  * from bf16 gate and up values (device uint16 [n] each) write the device
- * uint16 [n][4] results sigT, siluT, out, and gateT re-rounded (a check
- * that it is already bf16).  Used to test the tail exhaustively.
+ * uint16 [n][4] results sigT, siluT, out (as the tensor-core GEMM forms
+ * them, from the sigmoid table) and sigT as the decode kernels form it (in
+ * registers when their fast form is conclusive, else from the table).
+ * Used to test both forms of the tail exhaustively.
  */
 int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
                      int64_t n, uint16_t *res, cudaStream_t stream);
 
 /* The same for the MLX tail (Q4MOE_TAIL_MLX), with the same arguments and
- * result layout. */
+ * result layout (column 3 repeats sigT: every kernel takes the MLX sigmoid
+ * from its table). */
 int q4moe_debug_tail_mlx(const uint16_t *gate_bf16, const uint16_t *up_bf16,
                          int64_t n, uint16_t *res, cudaStream_t stream);
+
+/*
+ * Diagnostic: run the kernels' bounded on-chip waits (the try_wait form of
+ * the producers and consumers and the spin of the MMA issuer) on an
+ * mbarrier that nothing arrives on, with a limit of limit_ns (1e3 .. 1e9,
+ * i.e. 1 us .. 1 s; the kernels themselves wait at most 4 s).  The kernel
+ * gives up after the limit, raises Q4MOE_DEV_WAIT_TIMEOUT in the device
+ * status word and returns; the device stays usable.  For testing the
+ * time-out path.  No passage of the pages corresponds to it.
+ */
+int q4moe_debug_wait_timeout(int64_t limit_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -233,6 +233,9 @@ def test_host_argument_errors():
         q.ERR_INVALID_ARG
     assert lib.q4moe_debug_tail_mlx(None, None, 4, None, None) == \
         q.ERR_INVALID_ARG
+    # the wait diagnostic takes limits of 1 us .. 1 s only
+    for ns in (0, 999, 1000000001, -5):
+        assert lib.q4moe_debug_wait_timeout(ns, None) == q.ERR_INVALID_ARG
     # the tail option: MLX's is for trellis codes only, values outside the
     # three and a nonzero reserved field are refused
     for tail, reserved in ((q.TAIL_MLX, 0), (3, 0), (-1, 0),

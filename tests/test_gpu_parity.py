@@ -135,7 +135,9 @@ def test_group_rows_many_blocks_bad_ids():
 
 def test_tail_exhaustive_bf16():
     """All 65,536 bf16 gate values (finite), several up values: the device
-    tail equals the oracle's bit for bit (sigmoid, silu and out)."""
+    tail equals the oracle's bit for bit (sigmoid, silu and out), and so
+    does the sigmoid as the decode kernels form it (in registers when the
+    fast form is conclusive, else from the table)."""
     import torch
     g = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     g = g[((g >> 7) & 0xFF) != 0xFF]
@@ -150,7 +152,8 @@ def test_tail_exhaustive_bf16():
         gf = syn.bf16_bits_to_f32(g)
         uf = syn.bf16_bits_to_f32(u)
         t = oracle.tail_array(gf, uf)
-        assert np.array_equal(r[:, 3], g)
+        bad = np.flatnonzero(r[:, 3] != t[:, 2])
+        assert bad.size == 0, f"decode-form sigmoid: {bad.size} differ"
         for col, name in ((0, "sigmoid"), (1, "silu"), (2, "out")):
             bad = np.flatnonzero(r[:, col] != t[:, col + 2])
             assert bad.size == 0, f"{name}: {bad.size} differ, e.g. gate " \

@@ -41,8 +41,13 @@ int cuda_fail(cudaError_t err, const char *what) {
 // exists once in every device context that loads the library).
 __device__ unsigned int g_status_word;
 // bf16 sigmoid of every bf16 gate value for each tail (page 52's, then
-// MLX's), built at the first call on a device
-__device__ __align__(16) uint16_t g_sigmoid_table[2 * q4moe::kSigmoidTable];
+// MLX's): constant data of the library image, written at build time by the
+// package's table generator (up_swiglu_gb300/build.py), so no call has to
+// fill it
+__device__ __align__(16) const uint16_t
+    g_sigmoid_table[2 * q4moe::kSigmoidTable] = {
+#include "q4moe_sigmoid_table.inc"
+};
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -57,7 +62,9 @@ DeviceInfo g_devices[kMaxDevices];
 std::mutex g_devices_mutex;
 
 // Per-device set-up, done on the first call that needs it with that device
-// current: the compute capability check and the status word's address.
+// current: the compute capability check and the device addresses of the
+// status word and the sigmoid tables (host queries only: nothing is
+// launched and no stream is synchronised).
 int device_info(DeviceInfo **out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -90,21 +97,9 @@ int device_info(DeviceInfo **out) {
             if (err != cudaSuccess)
                 return cuda_fail(err, "cudaGetSymbolAddress(status word)");
             d.status = static_cast<unsigned int *>(p);
-            // the sigmoid table, built once on a private stream
             if ((err = cudaGetSymbolAddress(&p, g_sigmoid_table)) !=
                 cudaSuccess)
                 return cuda_fail(err, "cudaGetSymbolAddress(sigmoid table)");
-            cudaStream_t s = nullptr;
-            if ((err = cudaStreamCreateWithFlags(
-                     &s, cudaStreamNonBlocking)) != cudaSuccess)
-                return cuda_fail(err, "cudaStreamCreateWithFlags");
-            err = q4moe::launch_build_sigmoid_table(
-                static_cast<uint16_t *>(p), s);
-            if (err == cudaSuccess)
-                err = cudaStreamSynchronize(s);
-            cudaStreamDestroy(s);
-            if (err != cudaSuccess)
-                return cuda_fail(err, "sigmoid table");
             d.sigmoid = static_cast<const uint16_t *>(p);
         }
         d.ready = true;
@@ -831,6 +826,21 @@ int q4moe_debug_tail(const uint16_t *gate_bf16, const uint16_t *up_bf16,
                                                d->sigmoid, false, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, "debug tail launch");
+    return ok();
+}
+
+int q4moe_debug_wait_timeout(int64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000)
+        return fail(Q4MOE_ERR_INVALID_ARG,
+                    "limit_ns must be in 1e3 .. 1e9 (1 us .. 1 s)");
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc)
+        return rc;
+    cudaError_t err =
+        q4moe::launch_debug_wait(d->status, (uint64_t)limit_ns, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "debug wait launch");
     return ok();
 }
 

@@ -124,12 +124,12 @@ cudaError_t launch_group_rows(const int32_t *topk, int64_t pairs, int32_t k,
                               int32_t *token_of_row, int32_t *row_of_pair,
                               unsigned int *status, int num_sms,
                               cudaStream_t s);
+cudaError_t launch_debug_wait(unsigned int *status, uint64_t limit_ns,
+                              cudaStream_t s);
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u,
                               int64_t n, uint16_t *res,
                               const uint16_t *sigmoid, bool mlx,
                               cudaStream_t s);
-// Fills both sigmoid tables (2 x 65,536 entries).
-cudaError_t launch_build_sigmoid_table(uint16_t *table, cudaStream_t s);
 // Entries of one sigmoid table; the MLX tail's table follows the page's.
 constexpr int kSigmoidTable = 65536;
 
@@ -161,23 +161,6 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
     return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
 }
 
-// The page's f32 sigmoid chain 1 / (1 + exp(-g)) (page 52, GATE_UP_SOURCE
-// tail) with IEEE add and divide and no flush to zero.  expf is within 2 ulp
-// of exp; the result can only round to a different bf16 than the correctly
-// rounded chain when it lies within a few f32 ulp of a bf16 rounding
-// midpoint, and there the chain is recomputed from the double-precision
-// exponential.
-__device__ __forceinline__ float sigmoid_chain(float g) {
-    float e = expf(-g);
-    float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
-    const int lo = (int)(__float_as_uint(s) & 0xFFFFu);
-    if (abs(lo - 0x8000) <= 32) {
-        e = __double2float_rn(exp(-(double)g));
-        s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
-    }
-    return s;
-}
-
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -199,9 +182,10 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // square is below 2^-40).  Then sigmoid = rcp(1 + e).  For g > -16 its error
 // against the page's f32 chain is a few f32 ulp (ex2 and rcp about 2 ulp
 // each), so when it lies more than 16 ulp from a bf16 rounding midpoint both
-// round to the same bf16 and *ok is set; otherwise sigmoid_bf16_exact runs
-// the chain itself.  (sigmoidT depends on the 16-bit g only; all 65,536
-// cases are tested against the oracle.)
+// round to the same bf16 and *ok is set; otherwise the caller takes the
+// table entry.  (sigmoidT depends on the 16-bit g only; the fast form's
+// conclusive results and the table are tested against the oracle on all
+// 65,536 inputs.)
 __device__ __forceinline__ float sigmoid_bf16_fast_f(float g, bool *ok) {
     const float kHead = 1.44269502162933349609375f;  // float(log2 e)
     const float kTail = 1.925963033500011e-08f;      // log2 e - kHead
@@ -221,39 +205,13 @@ __device__ __forceinline__ uint16_t sigmoid_bf16_fast(float g, bool *ok) {
     return (uint16_t)(__float_as_uint(sigmoid_bf16_fast_f(g, ok)) >> 16);
 }
 
-static __device__ __noinline__ uint16_t sigmoid_bf16_exact(float g) {
-    return bf16_rne(sigmoid_chain(g));
-}
-
-__device__ __forceinline__ uint16_t sigmoid_bf16(float g) {
-    bool ok;
-    const uint16_t s = sigmoid_bf16_fast(g, &ok);
-    return ok ? s : sigmoid_bf16_exact(g);
-}
-
 // sigmoidT depends on the 16 bits of gateT only: the kernels read it from a
-// table of all 65,536 values, built once per device from sigmoid_bf16 (so
-// the table and the direct computation agree bit for bit; both are tested
-// against the oracle on every input).  The table is 128 KB and stays in L2.
+// table of all 65,536 values, constant data of the library image computed
+// at build time from the page's f32 chain (tested against the oracle on
+// every input).  The table is 128 KB and stays in L2.
 __device__ __forceinline__ uint16_t sigmoid_bf16_table(const uint16_t *table,
                                                        uint16_t gT) {
     return __ldg(table + gT);
-}
-
-// The sigmoid of MLX's compiled SwiGLU in bf16 arithmetic, the tail of the
-// pages' mixed-width trellis kernel (page 57, mixed-gate-up-factored.ts):
-// every step evaluated in f32, correctly rounded, and rounded to bf16:
-// e = bf16(exp(|g|)), d = bf16(1 + e), y = bf16(1 / d), and the sigmoid is
-// y for negative g (not -0), else bf16(1 - y).  exp is taken in double and
-// rounded once to f32 (correctly rounded but for results within a double
-// ulp of an f32 rounding midpoint; all 65,536 inputs are tested against
-// the oracle).  Used only to fill the table, once per device.
-__device__ __forceinline__ uint16_t sigmoid_bf16_mlx(float g) {
-    const float e32 = __double2float_rn(exp((double)fabsf(g)));
-    const float e = bf16_f32(bf16_rne(e32));
-    const float d = bf16_f32(bf16_rne(__fadd_rn(1.0f, e)));
-    const uint16_t y = bf16_rne(__fdiv_rn(1.0f, d));
-    return g < 0.0f ? y : bf16_rne(__fsub_rn(1.0f, bf16_f32(y)));
 }
 
 // gateT, upT -> out (bf16 bits).  sig and silu are also returned.  Both
@@ -272,8 +230,8 @@ __device__ __forceinline__ uint16_t swiglu_tail_bits(const uint16_t *table,
 
 // The same for one element whose latency matters more than its count (the
 // matvec's few outputs per thread): the sigmoid computed in registers when
-// the fast form is conclusive (it then equals the table entry, which was
-// built by the same function), the table only otherwise.
+// the fast form is conclusive (it then equals the table entry: both are the
+// correctly rounded chain), the table only otherwise.
 __device__ __forceinline__ uint16_t swiglu_out(const uint16_t *table,
                                                float gate32, float up32) {
     const uint16_t gT = bf16_rne(gate32), uT = bf16_rne(up32);

@@ -23,6 +23,7 @@
 // 0, slabs at base + e * stride), else the generic down kernel below (any
 // K % 8 == 0): one warp per output row, one matrix, no tail.
 #include "q4moe_internal.cuh"
+#include "q4moe_sm100.cuh"
 
 namespace q4moe {
 namespace {
@@ -213,18 +214,27 @@ down_generic_kernel(GateUpArgs a) {
 
 __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
                                   int64_t n, uint16_t *res,
-                                  const uint16_t *table) {
+                                  const uint16_t *table, int mlx) {
     // (table: the page 52 tail's or the MLX tail's)
     grid_dependency_wait();
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
-        const uint16_t gT = bf16_rne(bf16_f32(g[j]));
+        const uint16_t gT = g[j];
         uint16_t s, si;
         const uint16_t o = swiglu_tail_bits(table, gT, u[j], &s, &si);
         res[4 * j + 0] = s;
         res[4 * j + 1] = si;
         res[4 * j + 2] = o;
-        res[4 * j + 3] = gT;
+        // the sigmoid as the decode kernels form it for the page's tail:
+        // in registers when the fast form is conclusive, else the table
+        uint16_t sd = s;
+        if (!mlx) {
+            bool ok;
+            sd = sigmoid_bf16_fast(bf16_f32(gT), &ok);
+            if (!ok)
+                sd = sigmoid_bf16_table(table, gT);
+        }
+        res[4 * j + 3] = sd;
     }
 }
 
@@ -250,6 +260,36 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
                              a);
 }
 
+namespace {
+// The bounded waits of the kernels on an mbarrier that nothing arrives on:
+// thread 0 waits as the producers and consumers do (try_wait), thread 32 as
+// the MMA issuer does (test_wait spin).  The first to run out raises
+// Q4MOE_DEV_WAIT_TIMEOUT and the abort flag, which ends the other's wait.
+__global__ void debug_wait_kernel(unsigned int *status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&bar, 1);
+        abort_flag = 0;
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int *abort = &abort_flag;
+    if (threadIdx.x == 0)
+        sm100::wait_phase(&bar, 0, abort, status, limit_ns);
+    else if (threadIdx.x == 32)
+        sm100::wait_spin(&bar, 0, abort, status, limit_ns);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_debug_wait(unsigned int *status, uint64_t limit_ns,
+                              cudaStream_t s) {
+    return launch_pdl(debug_wait_kernel, dim3(1), dim3(64), 0, s, status,
+                      limit_ns);
+}
+
 cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
                               uint16_t *res, const uint16_t *sigmoid,
                               bool mlx, cudaStream_t s) {
@@ -258,26 +298,7 @@ cudaError_t launch_debug_tail(const uint16_t *g, const uint16_t *u, int64_t n,
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
     return launch_pdl(debug_tail_kernel, dim3((unsigned)blocks), dim3(256), 0,
                       s, g, u, n, res,
-                      mlx ? sigmoid + kSigmoidTable : sigmoid);
-}
-
-namespace {
-// The kernels' tables: sigmoid_bf16 (page 52 tail) and sigmoid_bf16_mlx
-// (MLX tail) of every bf16 value
-__global__ void build_sigmoid_table_kernel(uint16_t *table) {
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < kSigmoidTable;
-         j += gridDim.x * blockDim.x) {
-        const float g = bf16_f32((uint16_t)j);
-        table[j] = sigmoid_bf16(g);
-        table[kSigmoidTable + j] = sigmoid_bf16_mlx(g);
-    }
-}
-}  // namespace
-
-cudaError_t launch_build_sigmoid_table(uint16_t *table, cudaStream_t s) {
-    build_sigmoid_table_kernel<<<256, 256, 0, s>>>(table);
-    count_launches(1);
-    return cudaGetLastError();
+                      mlx ? sigmoid + kSigmoidTable : sigmoid, mlx ? 1 : 0);
 }
 
 }  // namespace q4moe

@@ -60,12 +60,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Limit of every on-chip wait of the library's kernels.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s
+
 // Bounded wait on an mbarrier phase.  Returns false (and, the first time,
 // raises Q4MOE_DEV_WAIT_TIMEOUT) once the CTA has aborted or the wait ran
-// out (4 s).
+// out (limit_ns).
 static __device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
                                                volatile int *abort,
-                                               unsigned int *status) {
+                                               unsigned int *status,
+                                               uint64_t limit_ns =
+                                                   kWaitLimitNs) {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = globaltimer_ns();
@@ -75,7 +80,7 @@ static __device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity,
         if ((it & 63u) == 0) {
             if (*abort)
                 return false;
-            if (globaltimer_ns() - t0 > 4000000000ull) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (atomicExch((int *)abort, 1) == 0)
                     atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
                 return false;
@@ -101,10 +106,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // Bounded wait by spinning on test_wait, for the one thread whose issue
 // rate sets the pace (the MMA issuer): returns false (and, the first time,
 // raises Q4MOE_DEV_WAIT_TIMEOUT) once the CTA has aborted or the wait ran
-// out (4 s).
+// out (limit_ns).
 __device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity,
                                           volatile int *abort,
-                                          unsigned int *status) {
+                                          unsigned int *status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_test_wait(bar, parity))
         return true;
     const uint64_t t0 = globaltimer_ns();
@@ -114,7 +120,7 @@ __device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity,
         if ((it & 255u) == 0) {
             if (*abort)
                 return false;
-            if (globaltimer_ns() - t0 > 4000000000ull) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (atomicExch((int *)abort, 1) == 0)
                     atomicOr(status, Q4MOE_DEV_WAIT_TIMEOUT);
                 return false;

@@ -13,7 +13,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 7
+ABI_VERSION = 8
 SLAB_ALIGNMENT = 4096
 MAX_EXPERTS = 1024
 
@@ -56,6 +56,7 @@ EXPORTS = (
     "q4moe_down_proj", "q4moe_expert_mlp", "q4moe_canonical_layout_format",
     "q4moe_trellis_canonical_layout", "q4moe_trellis_pack_slab",
     "q4moe_trellis_gate_up_swiglu", "q4moe_debug_tail_mlx",
+    "q4moe_debug_wait_timeout",
 )
 
 # Size of the library's fixed scratch used by q4moe_gate_up_swiglu_noalloc.
@@ -171,6 +172,7 @@ def load(build_if_missing: bool = True):
                                      ctypes.c_int]),
             "q4moe_debug_tail": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
             "q4moe_debug_tail_mlx": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+            "q4moe_debug_wait_timeout": (ctypes.c_int, [_I64, _P]),
             "q4moe_launch_count": (ctypes.c_int64, []),
             "q4moe_workspace_bytes": (ctypes.c_int64, [_I64, _I64]),
             "q4moe_gate_up_swiglu_noalloc": (ctypes.c_int,
@@ -367,6 +369,10 @@ def q4moe_launch_count() -> int:
 def q4moe_debug_tail(gate_bf16, up_bf16, n, res, stream=None) -> None:
     _check(load().q4moe_debug_tail(_ptr(gate_bf16), _ptr(up_bf16), n,
                                    _ptr(res), _stream(stream)))
+
+
+def q4moe_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load().q4moe_debug_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def q4moe_debug_tail_mlx(gate_bf16, up_bf16, n, res, stream=None) -> None:
