@@ -317,13 +317,13 @@ int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
  *   H, I                    must equal the layout's.
  *   out                     device bf16 [M][I], grouped-row order, fully
  *                           written on success.
- * Kernel choice (Q4MOE_KERNEL_AUTO): experts with at most 48 rows run on
- * the HBM-streaming matvec; the experts above go to the tcgen05 tensor-core
- * GEMM when between them they make at least one GEMM tile (128 intermediate
- * rows x up to 256 grouped rows) per SM, else the matvec takes every
- * expert.  Decided on the host for one expert and on the device for
- * several; a call with fewer than 49 * ceil(SMs / (I / 128)) rows never
- * launches the GEMM.
+ * Kernel choice (Q4MOE_KERNEL_AUTO): with several experts and at least 4
+ * grouped rows per expert on average (M >= 4 E), experts with more than 16
+ * rows run on the tcgen05 tensor-core GEMM (tiles of 128 intermediate rows
+ * x up to 256 grouped rows) and the others on the HBM-streaming matvec;
+ * with fewer rows the matvec takes every expert and the GEMM is not
+ * launched.  One expert goes to the GEMM when it has more than 48 rows and
+ * makes at least one tile per SM, else to the matvec.
  */
 int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *expert_slabs,
                          const int32_t *row_offsets_per_expert,

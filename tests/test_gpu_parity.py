@@ -210,10 +210,10 @@ def test_parity_reduced_workloads(kernel, E, T, k, routing, x_std):
 
 @pytest.mark.parametrize("big", [13, 12])
 def test_auto_mixes_matvec_and_gemm(big):
-    """Automatic choice with I = 1536 (12 GEMM tiles per expert chunk):
-    13 experts above 48 rows make 156 tiles, enough for one per SM, and go
-    to the GEMM while the small ones stay on the matvec; 12 make 144 and the
-    matvec takes every expert.  Either way the oracle's results."""
+    """Automatic choice with I = 1536 (12 GEMM tiles per expert chunk): the
+    experts above 16 rows (60, 48 and 17 rows) go to the GEMM while the
+    small ones (1, 8, 9 rows, and an empty one) stay on the matvec.  The
+    oracle's results, bit for bit on exact inputs."""
     counts = [60] * big + [1, 8, 9, 48, 0, 17]
     p = hz.problem_with_counts(80 + big, counts, 1536, 512, exact=True)
     _run_and_compare(p, exact=True)
@@ -221,14 +221,16 @@ def test_auto_mixes_matvec_and_gemm(big):
     _run_and_compare(p)
 
 
-@pytest.mark.parametrize("counts,launches", [([60] * 10, 1),
-                                             ([60] * 11 + [40], 2)])
+@pytest.mark.parametrize("counts,launches", [([3] * 20, 1),
+                                             ([60] + [1] * 39, 1),
+                                             ([8] * 10, 2),
+                                             ([60] * 2 + [1] * 6, 2)])
 def test_auto_skips_a_gemm_that_cannot_get_work(counts, launches):
-    """Under the automatic choice the GEMM needs ceil(152 / 12) = 13
-    experts above 48 rows: with fewer than 13 * 49 = 637 rows in the call
-    only the matvec is launched (600 rows here), with more the GEMM is
-    launched and finds too few tiles (700 rows: 11 experts of 60).  Same
-    results either way."""
+    """Under the automatic choice the GEMM is launched only when the call
+    has at least 4 rows per expert: 60 rows over 20 experts, or 99 over 40
+    with one expert of 60, take the matvec alone (one launch); 80 rows over
+    10 experts launch the GEMM as well, which finds no expert above 16 rows;
+    126 over 8 give it the two experts of 60.  Same results either way."""
     import torch
     p = hz.problem_with_counts(77, counts, 1536, 512, exact=True)
     d = hz.upload(p)

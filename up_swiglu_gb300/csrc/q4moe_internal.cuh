@@ -39,7 +39,6 @@ struct GateUpArgs {
     int32_t num_sms;
     int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
     int32_t matvec_last;         // no GEMM launch follows the matvec's
-    int32_t gemm_min_tiles;      // > 0: the automatic choice (matvec_limit)
     const uint16_t *sigmoid;     // sigmoid tables: [2][65536] bf16, indexed
                                  // by the bf16 bits of gateT: the page 52
                                  // tail's, then the MLX tail's
@@ -285,34 +284,12 @@ __device__ __forceinline__ bool stage_row_offsets(const GateUpArgs &a,
     return ok;
 }
 
-// Experts with more rows than this go to the GEMM.  Under the automatic
-// choice (a.gemm_min_tiles > 0) the experts above a.matvec_max_rows go to
-// the GEMM only when they make at least a.gemm_min_tiles GEMM tiles
-// (gemm_row_tiles x up to 256 grouped rows): fewer would leave most SMs
-// idle while the GEMM runs, and the matvec takes every expert instead.
-// Every kernel of the call evaluates the same rule on the staged offsets;
-// all threads of the block must call it.
+// Experts with more rows than this go to the GEMM (the host's kernel
+// choice; every kernel of the call reads the same value).  The staged row
+// offsets are not needed: the choice is a row threshold.
 __device__ __forceinline__ int32_t matvec_limit(const GateUpArgs &a,
-                                                const int32_t *s_off) {
-    if (a.gemm_min_tiles <= 0)
-        return a.matvec_max_rows;
-    __shared__ int s_tiles;
-    if (threadIdx.x == 0)
-        s_tiles = 0;
-    __syncthreads();
-    int t = 0;
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-        const int n = s_off[e + 1] - s_off[e];
-        if (n > a.matvec_max_rows)
-            t += (n + 255) / 256 * gemm_row_tiles(a);
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1)
-        t += __shfl_xor_sync(0xffffffffu, t, d);
-    if ((threadIdx.x & 31) == 0 && t != 0)
-        atomicAdd(&s_tiles, t);
-    __syncthreads();
-    return s_tiles >= a.gemm_min_tiles ? a.matvec_max_rows : INT32_MAX;
+                                                const int32_t *) {
+    return a.matvec_max_rows;
 }
 
 // Token of grouped row p, or -1 (and a status bit) when out of range.
