@@ -110,6 +110,15 @@ def parse_args(argv=None):
                     help="unit height of the TMA matvec (0: per call)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time the headline workload only")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="a reduced copy of the workload with this many "
+                         "experts (profiling; 0: the workload's own)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="a reduced copy of the workload with this many "
+                         "tokens (profiling; 0: the workload's own)")
+    ap.add_argument("--sustain-seconds", type=float, default=SUSTAIN_S,
+                    help="untimed steps sampled for clocks before the timed "
+                         "region (0: none, e.g. under a profiler)")
     ap.add_argument("--l2-hot", action="store_true",
                     help="single-expert decode: every call on the same slab "
                          "(weights L2-resident)")
@@ -162,23 +171,28 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str, kernel_file: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken
-    on the current source of the kernel (sha256 of the .cu file)."""
+def load_traffic(key: str):
+    """DRAM bytes per call (the sum over the call's kernels) from the
+    committed ncu summaries (profiles/ncu_traffic.txt), if every kernel's
+    row was taken on its current source (sha256 prefix of the .cu file);
+    else None."""
     import hashlib
-    src = os.path.join(ROOT, "up_swiglu_gb300", "csrc", kernel_file)
     table = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    total, found = 0.0, False
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         for line in open(table):
             parts = line.split()
-            if len(parts) >= 4 and not line.startswith("#") and \
-                    parts[0] == workload and parts[1] == kernel_file and \
-                    parts[2] == sha:
-                return float(parts[3])
+            if len(parts) < 4 or line.startswith("#") or parts[0] != key:
+                continue
+            src = os.path.join(ROOT, "up_swiglu_gb300", "csrc", parts[1])
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            if sha != parts[2]:
+                return None                  # a kernel changed since
+            total += float(parts[3])
+            found = True
     except OSError:
-        pass
-    return None
+        return None
+    return total if found else None
 
 
 # ---------------------------------------------------------------- clocks --
@@ -619,9 +633,7 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
         return {"bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": load_traffic(
-                    traffic_key, "q4moe_trellis.cu" if gw.trellis
-                    else "q4moe_matvec_tma.cu"),
+                "traffic": load_traffic(traffic_key),
                 "kernel": ("q4moe_trellis_gate_up_swiglu (integer-bound "
                            "decode)" if gw.trellis
                            else f"{OP_ENTRY[op]} matvec"),
@@ -635,7 +647,7 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
     return {"bound": "tensor", "achieved": round(achieved, 2),
             "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
-            "traffic": load_traffic(traffic_key, "q4moe_gemm.cu"),
+            "traffic": load_traffic(traffic_key),
             "kernel": f"{OP_ENTRY[op]} gemm (the call's launches: row copy "
                       "and tensor-core GEMM)",
             "algorithmic_flops_per_launch": int(flops_per_launch),
@@ -680,19 +692,20 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
     clk = ClockSampler(local) if headline else None
     if clk is not None:
         clk.__enter__()
-    sustain = None
+    sustain = {"seconds": 0.0, "steps": 0}
     try:
-        if clk is not None:
-            # untimed sustain loop (sampled): at least SUSTAIN_S seconds
+        if clk is not None and args.sustain_seconds > 0:
+            # untimed sustain loop (sampled)
             t0 = time.time()
             n_sus = 0
-            while time.time() - t0 < SUSTAIN_S:
+            while time.time() - t0 < args.sustain_seconds:
                 for _ in range(8):
                     gw.enqueue_step()
                 torch.cuda.synchronize(dev)
                 n_sus += 8
             sustain = {"seconds": round(time.time() - t0, 3),
                        "steps": n_sus}
+        if clk is not None:
             clk.mark()
         # timed region: K steps, barrier + synchronize on both sides
         ev = [(torch.cuda.Event(enable_timing=True),
@@ -802,6 +815,14 @@ def per_config_entry(w, res, l2_hot=False):
 def main(argv=None):
     args = parse_args(argv)
     w = syn.WORKLOADS[args.workload]
+    if args.experts or args.tokens:
+        # a reduced copy for profiling: same shapes, routing and recipe
+        import dataclasses
+        E = args.experts or w.E
+        T = args.tokens or w.T
+        w = dataclasses.replace(w, name=f"{w.name}:E{E}:T{T}", E=E, T=T,
+                                topk=min(w.topk, E))
+        args.no_per_config = True
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
