@@ -31,6 +31,8 @@ def _gpu():
 
 
 def _outputs(d, offs, tok, noalloc):
+    """The no-alloc call, or the regular one given a workspace of its own
+    (the same kernels and the same summation order)."""
     import torch
     M = int(tok.shape[0])
     out = torch.full((M, d.p.I), -1, dtype=torch.int16, device="cuda")
@@ -38,7 +40,13 @@ def _outputs(d, offs, tok, noalloc):
         q.q4moe_gate_up_swiglu_noalloc(d.x, d.slabs, offs, tok, M, d.p.H,
                                        d.p.I, out)
     else:
-        q.q4moe_gate_up_swiglu(d.x, d.slabs, offs, tok, M, d.p.H, d.p.I, out)
+        ws = torch.empty(q.q4moe_workspace_bytes(M, d.p.H) + 256,
+                         dtype=torch.uint8, device="cuda")
+        o = q.q4moe_options_t()
+        o.workspace = ws.data_ptr() + (-ws.data_ptr()) % 256
+        o.workspace_bytes = q.q4moe_workspace_bytes(M, d.p.H)
+        q.q4moe_gate_up_swiglu_ex(d.x, d.slabs, offs, tok, M, d.p.H, d.p.I,
+                                  out, o)
     torch.cuda.synchronize()
     return out.cpu().numpy().view(np.uint16)
 

@@ -102,6 +102,9 @@ cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s);
 bool matvec_mma_supported(const GateUpArgs &a);
 cudaError_t launch_matvec_mma(const GateUpArgs &a, cudaStream_t s);
 bool matvec_tma_supported(const GateUpArgs &a);
+// One expert, at most 8 grouped rows (q4moe_matvec_lat.cu).
+bool matvec_latency_supported(const GateUpArgs &a);
+cudaError_t launch_matvec_latency(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_matvec_tma(const GateUpArgs &a, cudaStream_t s);
 cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s);
 // The tcgen05 GEMM whose weights, dequantised tiles and token rows all move

@@ -241,6 +241,8 @@ __global__ void debug_tail_kernel(const uint16_t *g, const uint16_t *u,
 }  // namespace
 
 cudaError_t launch_matvec(const GateUpArgs &a, cudaStream_t s) {
+    if (matvec_latency_supported(a))
+        return launch_matvec_latency(a, s);
     if (matvec_tma_supported(a))
         return launch_matvec_tma(a, s);
     const dim3 grid((unsigned)((a.I + kRowsPerBlock - 1) / kRowsPerBlock),

@@ -1,0 +1,390 @@
+// q4moe_matvec_lat.cu -- the fused gate/up + SwiGLU for one expert and at
+// most 8 grouped rows (single-sequence decode), laid out for latency.
+//
+// Same arithmetic as the page's matvec (page 52, streamed-experts.ts,
+// GATE_UP_SOURCE): per row i, gate and up sums over k of (nibble - 8, or
+// the signed byte) * x in f32, row scale, bf16 gate/up, SwiGLU tail.
+//
+// A call this small is bound by its chain of latencies, not by bandwidth:
+// 6.3 MB of weights (H=4096, I=1536) stream in under 1 us at the measured
+// copy bandwidth.  Each CTA takes R = ceil(I / SMs) consecutive
+// intermediate rows.  Before the dependency wait the CTA asks L2 to
+// prefetch its weight rows (a prefetch only warms L2, the point of
+// coherence, so it is safe whatever the previous kernel writes); the
+// previous call releases this one as soon as its own CTAs hold their
+// operands, so that prefetch overlaps the previous call's arithmetic.
+// Right after the dependency wait one thread issues a
+// bulk copy (cp.async.bulk) per weight row of both matrices while a thread
+// of another warp checks the row offsets, reads the token indices and
+// issues one copy per activation row, and the threads that finish the
+// rows load their row scales.  The products then go to the tensor core:
+// the CTA's 2R weight rows (gate rows, then up rows) form n8 tiles of the
+// B operand of mma.sync m16n8k16 (bf16 in, f32 accumulate), the grouped
+// rows are the first M rows of A, and every warp takes every 16th 32-wide
+// K slice.  A thread's 32-bit (Q4) or 64-bit (Q8) weight load holds the 8
+// consecutive K of its slot group; the slots of A and B are filled in the
+// same K order (for Q4 the pairs {k, k+4}, which one mask-and-or per pair
+// builds: a nibble n under the bf16 exponent of 128.0 reads 128 + n, and
+// one bf16x2 subtraction of 136 gives n - 8, exactly), so every product is
+// exact.  The 16 warps' partial sums meet in shared memory and are added
+// in warp order, so a row's result depends on its own activations only and
+// is the same on every run.
+//
+// The arithmetic is bound by the issue port of each SM sub-partition:
+// the integer steps issue at half rate and an mma.sync m16n8k16 takes 8
+// cycles, about 134 issue cycles per warp and K slice, 2.3 us per call at
+// H=4096, I=1536 on 140 SMs.
+//
+// Every wait is bounded; on time-out the CTA raises Q4MOE_DEV_WAIT_TIMEOUT
+// and stores nothing.  Row offsets other than {0, M} raise
+// Q4MOE_DEV_BAD_ROW_OFFSETS and nothing is stored; a token index out of
+// range raises Q4MOE_DEV_BAD_TOKEN and its row is computed from zeros.
+#include <algorithm>
+
+#include "q4moe_internal.cuh"
+#include "q4moe_sm100.cuh"
+
+namespace q4moe {
+namespace {
+
+using namespace sm100;
+
+constexpr int kLatWarps = 16;
+constexpr int kLatThreads = kLatWarps * 32;
+constexpr int kLatMaxRows = 8;               // grouped rows per call
+constexpr int kLatMaxTiles = 4;              // n8 tiles: 2R <= 32 rows
+
+// Shared-memory row pitches.  A weight row starts 16 (Q4) or 32 (Q8) bytes
+// past a 128-byte multiple of the previous one, so the 8 rows of a tile
+// that a warp reads at once fall in different banks; an activation row
+// starts 64 bytes past one, for the same reason across grouped rows.
+__host__ __device__ __forceinline__ int64_t lat_row_pitch(int64_t rb,
+                                                          bool q8) {
+    return (rb + 127) / 128 * 128 + (q8 ? 32 : 16);
+}
+__host__ __device__ __forceinline__ int64_t lat_x_pitch(int64_t H) {
+    return (H * 2 + 127) / 128 * 128 + 64;
+}
+__host__ __device__ __forceinline__ int lat_tile_rows(int R) {
+    return (2 * R + 7) & ~7;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completion reported to *bar as bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src,
+                                         uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Q4: the pairs {n_j - 8, n_{j+4} - 8} (j = 0..3) of one packed word.
+__device__ __forceinline__ void nibble_pairs(uint32_t w, uint32_t (&b)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t v;
+        asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;"
+            : "=r"(v)
+            : "r"(w >> (4 * j)));
+        b[j] = sub_bf16x2(v, 0x43084308u);
+    }
+}
+
+// Q8: the pairs {b0, b1}, {b2, b3} of a word of four signed bytes.  Under
+// the bf16 exponent byte 0x43 the low seven bits m of a byte read 128 + m
+// and its sign bit turns that into 256 + 2m; subtracting 128 + 128 * sign
+// leaves the byte's value, exactly (8 significant bits at most).
+__device__ __forceinline__ void byte_pairs(uint32_t w, uint32_t &lo,
+                                           uint32_t &hi) {
+    const uint32_t t0 = __byte_perm(w, 0x43434343u, 0x4140);
+    const uint32_t t1 = __byte_perm(w, 0x43434343u, 0x4342);
+    lo = sub_bf16x2(t0 & 0x437F437Fu, t0 & 0x43804380u);
+    hi = sub_bf16x2(t1 & 0x437F437Fu, t1 & 0x43804380u);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0,
+                                         uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+    // rows 8..15 of A (grouped rows 8..15) are zero
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%6,%5,%6}, {%7,%8}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+template <bool kQ8, int kM>
+__global__ void __launch_bounds__(kLatThreads, 1)
+matvec_latency_kernel(GateUpArgs a, int R) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    // weights [2R][row pitch] (gate rows, then up rows), activations
+    // bf16 [kM][x pitch], partial sums f32 [warps][tile rows][kM], barriers
+    const int64_t rb = weight_row_bytes(a, a.H);
+    const int64_t rp = lat_row_pitch(rb, kQ8), xp = lat_x_pitch(a.H);
+    const int H = (int)a.H, M = (int)a.M;
+    const int i0 = blockIdx.x * R;
+    const int nr = min(R, (int)a.I - i0);
+    const int V = lat_tile_rows(R), T8 = V / 8;
+    uint8_t *w_sm = smem;
+    uint8_t *x_sm = smem + (size_t)2 * R * rp;
+    float *part = reinterpret_cast<float *>(x_sm + (size_t)kM * xp);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(
+        part + (size_t)kLatWarps * V * kM);
+    __shared__ int s_tok[kLatMaxRows];
+    __shared__ int s_bad, s_bad_tok;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid < 2 * nr) {
+        // L2 prefetch of the CTA's weight rows, gate row tid / 2 or up row
+        const int64_t row = i0 + (tid >> 1);
+        prefetch_l2(a.base + ((tid & 1) ? a.up_w_off : a.gate_w_off) +
+                        row * rb,
+                    (uint32_t)rb);
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_dependency_wait();
+
+    if (tid == 0) {
+        // the weight rows of both matrices (they need nothing else)
+        mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * 2 * rb));
+        const uint8_t *slab = a.base;
+        for (int r = 0; r < nr; ++r) {
+            const int64_t row = i0 + r;
+            bulk_g2s(smem_u32(w_sm + (size_t)r * rp),
+                     slab + a.gate_w_off + row * rb, (uint32_t)rb, &bars[0]);
+            bulk_g2s(smem_u32(w_sm + (size_t)(R + r) * rp),
+                     slab + a.up_w_off + row * rb, (uint32_t)rb, &bars[0]);
+        }
+    } else if (tid == 32) {
+        // the row offsets of the one expert must be {0, M}; the token of
+        // each grouped row, then its activations
+        const int32_t off0 = __ldg(a.row_offsets), off1 = __ldg(a.row_offsets + 1);
+        const bool bad = off0 != 0 || off1 != M;
+        s_bad = bad;
+        if (bad && blockIdx.x == 0)
+            atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
+        uint32_t xbytes = 0;
+        int tok[kLatMaxRows], bad_tok = 0;
+#pragma unroll
+        for (int p = 0; p < kM; ++p) {
+            tok[p] = p < M ? (int)row_token(a, p) : -1;
+            s_tok[p] = tok[p];
+            if (tok[p] >= 0)
+                xbytes += (uint32_t)H * 2;
+            else if (p < M)
+                bad_tok = 1;
+        }
+        s_bad_tok = bad_tok;
+        mbar_arrive_expect_tx(&bars[1], xbytes);
+#pragma unroll
+        for (int p = 0; p < kM; ++p)
+            if (tok[p] >= 0)
+                bulk_g2s(smem_u32(x_sm + (size_t)p * xp),
+                         a.x + (int64_t)tok[p] * H, (uint32_t)H * 2,
+                         &bars[1]);
+    }
+    // the thread that finishes (row r, grouped row p) loads r's scales
+    const bool fin = tid < nr * M;
+    const int fr = fin ? tid % nr : 0, fp = fin ? tid / nr : 0;
+    float sg = 0.0f, su = 0.0f;
+    if (fin) {
+        sg = __ldg(reinterpret_cast<const float *>(a.base + a.gate_s_off) +
+                   i0 + fr);
+        su = __ldg(reinterpret_cast<const float *>(a.base + a.up_s_off) +
+                   i0 + fr);
+    }
+    __syncthreads();                         // s_tok, s_bad, s_bad_tok
+    if (s_bad_tok) {
+        // a grouped row whose token index is out of range (status raised)
+        // is computed from zeros, as in the other kernels
+        for (int p = 0; p < M; ++p)
+            if (s_tok[p] < 0)
+                for (int k = tid; k < H; k += kLatThreads)
+                    reinterpret_cast<uint16_t *>(x_sm + (size_t)p * xp)[k] = 0;
+        __syncthreads();
+    }
+    if (!wait_phase(&bars[0], 0, &s_abort, a.status) ||
+        !wait_phase(&bars[1], 0, &s_abort, a.status)) {
+        // (a time-out: the copies in flight land before the CTA exits)
+        if (tid == 0) {
+            drain_phase(&bars[0], 0);
+            drain_phase(&bars[1], 0);
+        }
+        return;
+    }
+    // The next launch may start now (its CTAs only prefetch before their
+    // own dependency wait).  Released at the start of the kernel instead,
+    // the next call's CTAs crowded these SMs and a chain of calls ran 2.3x
+    // slower; released after the arithmetic, 14% slower than never.
+    if (a.matvec_last)
+        grid_launch_dependents();
+
+    // thread (g, t) of the warp: grouped row g of A, weight row 8j + g of
+    // tile j, slot pairs 2t and 2t + 8 of each 16-wide K step
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t *wrow[kLatMaxTiles];
+    bool wok[kLatMaxTiles];
+#pragma unroll
+    for (int j = 0; j < kLatMaxTiles; ++j) {
+        const int v = 8 * j + g;
+        wok[j] = j < T8 && (v < R ? v < nr : v - R < nr);
+        wrow[j] = w_sm + (size_t)(wok[j] ? v : 0) * rp;
+    }
+    float acc[kLatMaxTiles][4];
+#pragma unroll
+    for (int j = 0; j < kLatMaxTiles; ++j)
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    const uint8_t *xrow = x_sm + (size_t)g * xp + (size_t)t * 16;
+    const int slices = H / 32;
+#pragma unroll 2
+    for (int c = warp; c < slices; c += kLatWarps) {
+        // A: activations K = 32c + 8t .. + 7 of grouped row g
+        uint32_t ae0 = 0, ae2 = 0, ao0 = 0, ao2 = 0;
+        if (g < M) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(xrow + (size_t)c * 64);
+            if (kQ8) {
+                ae0 = v.x; ae2 = v.y; ao0 = v.z; ao2 = v.w;
+            } else {
+                ae0 = __byte_perm(v.x, v.z, 0x5410);     // {x0, x4}
+                ae2 = __byte_perm(v.x, v.z, 0x7632);     // {x1, x5}
+                ao0 = __byte_perm(v.y, v.w, 0x5410);     // {x2, x6}
+                ao2 = __byte_perm(v.y, v.w, 0x7632);     // {x3, x7}
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kLatMaxTiles; ++j) {
+            if (j >= T8)
+                break;
+            uint32_t b[4];
+            if (kQ8) {
+                uint2 w = make_uint2(0u, 0u);
+                if (wok[j])
+                    w = *reinterpret_cast<const uint2 *>(
+                        wrow[j] + (size_t)c * 32 + t * 8);
+                byte_pairs(w.x, b[0], b[1]);
+                byte_pairs(w.y, b[2], b[3]);
+            } else {
+                uint32_t w = 0x88888888u;            // zero weights
+                if (wok[j])
+                    w = *reinterpret_cast<const uint32_t *>(
+                        wrow[j] + (size_t)c * 16 + t * 4);
+                nibble_pairs(w, b);
+            }
+            mma_bf16(acc[j], ae0, ae2, b[0], b[1]);
+            mma_bf16(acc[j], ao0, ao2, b[2], b[3]);
+        }
+    }
+    // accumulator (grouped row g, tile row 2t and 2t + 1) -> partials
+    if (g < M) {
+#pragma unroll
+        for (int j = 0; j < kLatMaxTiles; ++j) {
+            if (j >= T8)
+                break;
+            float *d = part + ((size_t)warp * V + 8 * j + 2 * t) * kM + g;
+            d[0] = acc[j][0];
+            d[kM] = acc[j][1];
+        }
+    }
+    __syncthreads();
+    if (!fin || s_bad)
+        return;
+    float gs = part[(size_t)fr * kM + fp];
+    float us = part[(size_t)(R + fr) * kM + fp];
+#pragma unroll
+    for (int w = 1; w < kLatWarps; ++w) {
+        gs = __fadd_rn(gs, part[((size_t)w * V + fr) * kM + fp]);
+        us = __fadd_rn(us, part[((size_t)w * V + R + fr) * kM + fp]);
+    }
+    const float g32 = __fmul_rn(gs, sg), u32 = __fmul_rn(us, su);
+    const int64_t o = (int64_t)fp * a.I + i0 + fr;
+    a.out[o] = swiglu_out(a.sigmoid, g32, u32);
+    if (a.gate_f32)
+        a.gate_f32[o] = g32;
+    if (a.up_f32)
+        a.up_f32[o] = u32;
+}
+
+size_t lat_smem(const GateUpArgs &a, int R, int kM) {
+    const int64_t rb = weight_row_bytes(a, a.H);
+    return (size_t)2 * R * lat_row_pitch(rb, a.q8) +
+           (size_t)kM * lat_x_pitch(a.H) +
+           (size_t)kLatWarps * lat_tile_rows(R) * kM * sizeof(float) +
+           2 * sizeof(uint64_t);
+}
+
+int lat_bucket(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+int lat_rows(const GateUpArgs &a) {
+    return (int)((a.I + a.num_sms - 1) / a.num_sms);
+}
+
+template <bool kQ8, int kM>
+cudaError_t launch_m(const GateUpArgs &a, cudaStream_t s) {
+    const int R = lat_rows(a);
+    const size_t smem = lat_smem(a, R, kM);
+    cudaError_t err = cudaFuncSetAttribute(
+        matvec_latency_kernel<kQ8, kM>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    const unsigned grid = (unsigned)((a.I + R - 1) / R);
+    return launch_pdl(matvec_latency_kernel<kQ8, kM>, dim3(grid),
+                      dim3(kLatThreads), smem, s, a, R);
+}
+
+template <bool kQ8>
+cudaError_t launch_q(const GateUpArgs &a, cudaStream_t s) {
+    switch (lat_bucket(a.M)) {
+    case 1: return launch_m<kQ8, 1>(a, s);
+    case 2: return launch_m<kQ8, 2>(a, s);
+    case 4: return launch_m<kQ8, 4>(a, s);
+    default: return launch_m<kQ8, 8>(a, s);
+    }
+}
+
+}  // namespace
+
+// One expert, 1..8 grouped rows, gate/up, slabs at base (no pointer table),
+// whole 16-byte weight rows and activation rows (16-byte aligned), H a
+// multiple of 32, at most 16 intermediate rows per CTA, all of them in
+// shared memory.
+bool matvec_latency_supported(const GateUpArgs &a) {
+    const int64_t rb = weight_row_bytes(a, a.H);
+    if (a.E != 1 || a.M < 1 || a.M > kLatMaxRows || a.down || a.invariant ||
+        a.slab_ptrs != nullptr || a.H % 32 != 0 || rb % 16 != 0 ||
+        a.gate_w_off % 16 != 0 || a.up_w_off % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(a.base) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(a.x) & 15) != 0)
+        return false;
+    const int R = lat_rows(a);
+    return 2 * R <= 8 * kLatMaxTiles &&
+           lat_smem(a, R, lat_bucket(a.M)) <= 200 * 1024;
+}
+
+cudaError_t launch_matvec_latency(const GateUpArgs &a, cudaStream_t s) {
+    return a.q8 ? launch_q<true>(a, s) : launch_q<false>(a, s);
+}
+
+}  // namespace q4moe
