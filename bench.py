@@ -613,11 +613,24 @@ def run_reference(args, w, rank, world):
     return 0
 
 
+def l2_residency(gw):
+    """How the step's weights sit against L2: more distinct slab bytes
+    than L2 holds, or all of them resident after the first step."""
+    total = gw.pool_experts * gw.layout.slab_bytes
+    if total > L2_BYTES:
+        return ("weights larger than L2 every step "
+                f"({gw.pool_experts} distinct expert slabs, "
+                f"{total / 2**20:.0f} MiB)")
+    return (f"weights L2-resident ({gw.pool_experts} expert slab(s), "
+            f"{total / 2**20:.1f} MiB, reused every step)")
+
+
 def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
-                timed_s):
+                timed_s, l2_hot=False):
     """Roofline of the fused call(s) of the operation: HBM for the decode
     kernels, the tensor core for the GEMM (burst peak unless the timed
-    region lasts seconds)."""
+    region lasts seconds).  The traffic of an L2-hot run has its own key
+    (taken without cache flushes)."""
     rows_per_expert = (w.routed_rows if w.repeats > 1 else
                        w.routed_rows / units["touched_experts"])
     # (the trellis kernel decodes every weight once per 8 rows at any size:
@@ -626,6 +639,8 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
     traffic_key = w.name if op == "gate_up" else f"{w.name}:{op}"
     if fmt != "q4":
         traffic_key += ":" + fmt.split(":")[0]
+    if l2_hot:
+        traffic_key += ":l2hot"
     if decode:
         bytes_per_launch = units["bytes"] / gw.calls
         achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
@@ -744,7 +759,7 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
     peaks, peak_src = load_peaks()
     per_launch_ms = statistics.mean(call_ms) / gw.calls
     roof = roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks,
-                       peak_src, total_ms * 1e-3)
+                       peak_src, total_ms * 1e-3, l2_hot=l2_hot)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (activations + routing) from pinned memory, D2H of the outputs
@@ -782,6 +797,7 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
         "call_ms": statistics.mean(call_ms),
         "clocks": clk.summary() if clk is not None else None,
         "sustain": sustain,
+        "l2": l2_residency(gw),
     }
     return res
 
@@ -801,6 +817,7 @@ def per_config_entry(w, res, l2_hot=False):
                               if l2_hot else ""),
         "routed_rows": w.routed_rows, "repeats": w.repeats,
         "touched_experts": gw_pool,
+        "l2": res["l2"],
         "ms_per_step": round(res["ms_per_step"], 5),
         "value": round(res["value"], 3), "unit": "GB/s",
         "tflops": round(res["tflops"], 3),
@@ -892,10 +909,7 @@ def main(argv=None):
                        "touched_experts": units["touched_experts"],
                        "weight_bytes_per_step": units["weight_bytes"],
                        "flops_per_step": units["flops"],
-                       "l2": ("one slab reused every call (L2-resident "
-                              "weights)" if args.l2_hot else
-                              "weights larger than L2 every step "
-                              f"({gw.pool_experts} distinct expert slabs)"),
+                       "l2": res["l2"],
                        "kernel_choice": args.kernel,
                        "workspace": not args.no_workspace,
                        "matvec_tile": args.matvec_tile or "per call",

@@ -162,3 +162,33 @@ def test_gemm_roofline_takes_the_burst_peak_for_short_regions():
                           "measured", 0.1)
     assert r["bound"] == "hbm" and r["peak"] == 6000.0
     assert r["achieved"] == pytest.approx(3000.0)
+
+
+def test_l2_residency_and_hot_traffic_key(monkeypatch):
+    """The line says whether the step's distinct slab bytes exceed L2, and
+    an L2-hot run looks its DRAM traffic up under its own key."""
+    import types
+    import bench
+    from up_swiglu_gb300 import synthetic as syn
+    small = types.SimpleNamespace(pool_experts=1,
+                                  layout=types.SimpleNamespace(
+                                      slab_bytes=133_120))
+    big = types.SimpleNamespace(pool_experts=83,
+                                layout=types.SimpleNamespace(
+                                    slab_bytes=6_316_032))
+    assert bench.l2_residency(small).startswith("weights L2-resident")
+    assert bench.l2_residency(big).startswith("weights larger than L2")
+    keys = []
+    monkeypatch.setattr(bench, "load_traffic",
+                        lambda k: keys.append(k) or None)
+    gw = types.SimpleNamespace(calls=1000, trellis=False)
+    w = syn.WORKLOADS["expert1_h4096_i1536_m1_x1000"]
+    units = {"touched_experts": 1000, "bytes": 6.3e9, "flops": 2.5e10,
+             "weight_bytes": 6.3e9}
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0,
+             "bf16_tflops_sustained": 1700.0}
+    bench.roofline_of(gw, w, units, "gate_up", "q4", 0.005, peaks,
+                      "measured", 0.1)
+    bench.roofline_of(gw, w, units, "gate_up", "q4", 0.005, peaks,
+                      "measured", 0.1, l2_hot=True)
+    assert keys == [w.name, w.name + ":l2hot"]
