@@ -13,27 +13,31 @@
 // coherence, so it is safe whatever the previous kernel writes); the
 // previous call releases this one as soon as its own CTAs hold their
 // operands, so that prefetch overlaps the previous call's arithmetic.
-// Right after the dependency wait one thread issues a
-// bulk copy (cp.async.bulk) per weight row of both matrices while a thread
-// of another warp checks the row offsets, reads the token indices and
-// issues one copy per activation row, and the threads that finish the
-// rows load their row scales.  The products then go to the tensor core:
-// the CTA's 2R weight rows (gate rows, then up rows) form n8 tiles of the
-// B operand of mma.sync m16n8k16 (bf16 in, f32 accumulate), the grouped
-// rows are the first M rows of A, and every warp takes every 16th 32-wide
-// K slice.  A thread's 32-bit (Q4) or 64-bit (Q8) weight load holds the 8
-// consecutive K of its slot group; the slots of A and B are filled in the
-// same K order (for Q4 the pairs {k, k+4}, which one mask-and-or per pair
-// builds: a nibble n under the bf16 exponent of 128.0 reads 128 + n, and
-// one bf16x2 subtraction of 136 gives n - 8, exactly), so every product is
-// exact.  The 16 warps' partial sums meet in shared memory and are added
-// in warp order, so a row's result depends on its own activations only and
-// is the same on every run.
+// Right after the dependency wait one thread of each of 15 warps issues
+// the bulk copies (cp.async.bulk) of a gate row and the matching up row
+// (one thread issuing them all took 0.26 us longer per call) while a
+// thread of the other warp checks the row offsets, reads the token indices
+// and issues one copy per activation row, and the threads that finish the
+// rows load their row scales.
 //
-// The arithmetic is bound by the issue port of each SM sub-partition:
-// the integer steps issue at half rate and an mma.sync m16n8k16 takes 8
-// cycles, about 134 issue cycles per warp and K slice, 2.3 us per call at
-// H=4096, I=1536 on 140 SMs.
+// The products go to the tensor core, mma.sync m16n8k16 (bf16 in, f32
+// accumulate).  The CTA's 2R weight rows (gate rows, then up rows) form m16
+// tiles of the A operand, the grouped rows being the first M columns of B,
+// and the last 2R mod 16 rows n8 tiles of the B operand, the grouped rows
+// being the first M rows of A; both forms take the activations in the same
+// registers.  Every warp takes every 16th 32-wide K slice.  A thread's
+// 32-bit (Q4) or 64-bit (Q8) weight load holds the 8 consecutive K of its
+// slot group; the slots of A and B are filled in the same K order (for Q4
+// the pairs {k, k+4}, which one mask-and-or per pair builds: a nibble n
+// under the bf16 exponent of 128.0 reads 128 + n, and one bf16x2
+// subtraction of 136 gives n - 8, exactly), so every product is exact.
+// The 16 warps' partial sums meet in shared memory and are added in warp
+// order, so a row's result depends on its own activations only and is the
+// same on every run.
+//
+// The arithmetic is bound by the issue port of each SM sub-partition: the
+// integer steps issue at half rate and an mma.sync m16n8k16 takes 8 issue
+// cycles.
 //
 // Every wait is bounded; on time-out the CTA raises Q4MOE_DEV_WAIT_TIMEOUT
 // and stores nothing.  Row offsets other than {0, M} raise
@@ -52,7 +56,9 @@ using namespace sm100;
 constexpr int kLatWarps = 16;
 constexpr int kLatThreads = kLatWarps * 32;
 constexpr int kLatMaxRows = 8;               // grouped rows per call
-constexpr int kLatMaxTiles = 4;              // n8 tiles: 2R <= 32 rows
+constexpr int kLatMaxRowsPerCta = 16;        // R
+constexpr int kLatMaxM16 = 2;                // m16 tiles: 2R <= 32 rows
+constexpr int kLatMaxN8 = 2;                 // n8 tiles: 2R mod 16 < 16
 
 // Shared-memory row pitches.  A weight row starts 16 (Q4) or 32 (Q8) bytes
 // past a 128-byte multiple of the previous one, so the 8 rows of a tile
@@ -117,15 +123,47 @@ __device__ __forceinline__ void byte_pairs(uint32_t w, uint32_t &lo,
     hi = sub_bf16x2(t1 & 0x437F437Fu, t1 & 0x43804380u);
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0,
-                                         uint32_t a2, uint32_t b0,
-                                         uint32_t b1) {
-    // rows 8..15 of A (grouped rows 8..15) are zero
+// n8 form: A = grouped rows (rows 8..15 zero), B = 8 weight rows.
+__device__ __forceinline__ void mma_n8(float (&c)[4], uint32_t a0,
+                                       uint32_t a2, uint32_t b0,
+                                       uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%6,%5,%6}, {%7,%8}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// m16 form: A = 16 weight rows, B = grouped rows as columns.
+__device__ __forceinline__ void mma_m16(float (&c)[4], uint32_t a0,
+                                        uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The four bf16 pairs of one weight row's word(s) for K slice c: pairs 0,
+// 1 for the slice's first 16-wide step, 2, 3 for its second.
+template <bool kQ8>
+__device__ __forceinline__ void weight_pairs(const uint8_t *row, bool ok,
+                                             int c, int t, uint32_t (&b)[4]) {
+    if (kQ8) {
+        uint2 w = make_uint2(0u, 0u);
+        if (ok)
+            w = *reinterpret_cast<const uint2 *>(row + (size_t)c * 32 + t * 8);
+        byte_pairs(w.x, b[0], b[1]);
+        byte_pairs(w.y, b[2], b[3]);
+    } else {
+        uint32_t w = 0x88888888u;                // zero weights
+        if (ok)
+            w = *reinterpret_cast<const uint32_t *>(row + (size_t)c * 16 +
+                                                    t * 4);
+        nibble_pairs(w, b);
+    }
 }
 
 template <bool kQ8, int kM>
@@ -139,7 +177,7 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     const int H = (int)a.H, M = (int)a.M;
     const int i0 = blockIdx.x * R;
     const int nr = min(R, (int)a.I - i0);
-    const int V = lat_tile_rows(R), T8 = V / 8;
+    const int V = lat_tile_rows(R);
     uint8_t *w_sm = smem;
     uint8_t *x_sm = smem + (size_t)2 * R * rp;
     float *part = reinterpret_cast<float *>(x_sm + (size_t)kM * xp);
@@ -166,16 +204,21 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     __syncthreads();
     grid_dependency_wait();
 
-    if (tid == 0) {
-        // the weight rows of both matrices (they need nothing else)
-        mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * 2 * rb));
-        const uint8_t *slab = a.base;
-        for (int r = 0; r < nr; ++r) {
+    if (lane == 0 && warp != 1) {
+        // the weight rows of both matrices (they need nothing else): lane 0
+        // of each warp but warp 1 issues the rows r = k mod 15 (k = 0 for
+        // warp 0, warp - 1 for the others), the first one expecting all
+        // the bytes (the barrier's count of bytes may run ahead of it)
+        const int k = warp == 0 ? 0 : warp - 1;
+        if (k == 0)
+            mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * 2 * rb));
+        for (int r = k; r < nr; r += kLatWarps - 1) {
             const int64_t row = i0 + r;
             bulk_g2s(smem_u32(w_sm + (size_t)r * rp),
-                     slab + a.gate_w_off + row * rb, (uint32_t)rb, &bars[0]);
+                     a.base + a.gate_w_off + row * rb, (uint32_t)rb,
+                     &bars[0]);
             bulk_g2s(smem_u32(w_sm + (size_t)(R + r) * rp),
-                     slab + a.up_w_off + row * rb, (uint32_t)rb, &bars[0]);
+                     a.base + a.up_w_off + row * rb, (uint32_t)rb, &bars[0]);
         }
     } else if (tid == 32) {
         // the row offsets of the one expert must be {0, M}; the token of
@@ -241,70 +284,95 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     if (a.matvec_last)
         grid_launch_dependents();
 
-    // thread (g, t) of the warp: grouped row g of A, weight row 8j + g of
-    // tile j, slot pairs 2t and 2t + 8 of each 16-wide K step
+    // thread (g, t) of the warp: in an m16 tile weight rows g and g + 8
+    // (A) and grouped rows 2t, 2t + 1 (columns of the result); in an n8
+    // tile grouped row g (A) and weight rows 2t, 2t + 1 of the result.  The
+    // activations of grouped row g, slots 2t and 2t + 8 of each 16-wide K
+    // step, serve both forms.
     const int g = lane >> 2, t = lane & 3;
-    const uint8_t *wrow[kLatMaxTiles];
-    bool wok[kLatMaxTiles];
+    const int T16 = 2 * R / 16, T8 = (V - 16 * T16) / 8;
+    const uint8_t *mrow[kLatMaxM16][2], *nrow[kLatMaxN8];
+    bool mok[kLatMaxM16][2], nok[kLatMaxN8];
 #pragma unroll
-    for (int j = 0; j < kLatMaxTiles; ++j) {
-        const int v = 8 * j + g;
-        wok[j] = j < T8 && (v < R ? v < nr : v - R < nr);
-        wrow[j] = w_sm + (size_t)(wok[j] ? v : 0) * rp;
+    for (int q = 0; q < kLatMaxM16; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int v = 16 * q + 8 * h + g;
+            mok[q][h] = q < T16 && (v < R ? v < nr : v - R < nr);
+            mrow[q][h] = w_sm + (size_t)(mok[q][h] ? v : 0) * rp;
+        }
+#pragma unroll
+    for (int j = 0; j < kLatMaxN8; ++j) {
+        const int v = 16 * T16 + 8 * j + g;
+        nok[j] = j < T8 && v < 2 * R && (v < R ? v < nr : v - R < nr);
+        nrow[j] = w_sm + (size_t)(nok[j] ? v : 0) * rp;
     }
-    float acc[kLatMaxTiles][4];
+    float am[kLatMaxM16][4], an[kLatMaxN8][4];
 #pragma unroll
-    for (int j = 0; j < kLatMaxTiles; ++j)
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    for (int q = 0; q < kLatMaxM16; ++q)
+        am[q][0] = am[q][1] = am[q][2] = am[q][3] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kLatMaxN8; ++j)
+        an[j][0] = an[j][1] = an[j][2] = an[j][3] = 0.0f;
     const uint8_t *xrow = x_sm + (size_t)g * xp + (size_t)t * 16;
     const int slices = H / 32;
 #pragma unroll 2
     for (int c = warp; c < slices; c += kLatWarps) {
-        // A: activations K = 32c + 8t .. + 7 of grouped row g
-        uint32_t ae0 = 0, ae2 = 0, ao0 = 0, ao2 = 0;
+        // activations K = 32c + 8t .. + 7 of grouped row g
+        uint32_t xe0 = 0, xe2 = 0, xo0 = 0, xo2 = 0;
         if (g < M) {
             const uint4 v = *reinterpret_cast<const uint4 *>(xrow + (size_t)c * 64);
             if (kQ8) {
-                ae0 = v.x; ae2 = v.y; ao0 = v.z; ao2 = v.w;
+                xe0 = v.x; xe2 = v.y; xo0 = v.z; xo2 = v.w;
             } else {
-                ae0 = __byte_perm(v.x, v.z, 0x5410);     // {x0, x4}
-                ae2 = __byte_perm(v.x, v.z, 0x7632);     // {x1, x5}
-                ao0 = __byte_perm(v.y, v.w, 0x5410);     // {x2, x6}
-                ao2 = __byte_perm(v.y, v.w, 0x7632);     // {x3, x7}
+                xe0 = __byte_perm(v.x, v.z, 0x5410);     // {x0, x4}
+                xe2 = __byte_perm(v.x, v.z, 0x7632);     // {x1, x5}
+                xo0 = __byte_perm(v.y, v.w, 0x5410);     // {x2, x6}
+                xo2 = __byte_perm(v.y, v.w, 0x7632);     // {x3, x7}
             }
         }
 #pragma unroll
-        for (int j = 0; j < kLatMaxTiles; ++j) {
+        for (int q = 0; q < kLatMaxM16; ++q) {
+            if (q >= T16)
+                break;
+            uint32_t lo[4], hi[4];
+            weight_pairs<kQ8>(mrow[q][0], mok[q][0], c, t, lo);
+            weight_pairs<kQ8>(mrow[q][1], mok[q][1], c, t, hi);
+            mma_m16(am[q], lo[0], hi[0], lo[1], hi[1], xe0, xe2);
+            mma_m16(am[q], lo[2], hi[2], lo[3], hi[3], xo0, xo2);
+        }
+#pragma unroll
+        for (int j = 0; j < kLatMaxN8; ++j) {
             if (j >= T8)
                 break;
             uint32_t b[4];
-            if (kQ8) {
-                uint2 w = make_uint2(0u, 0u);
-                if (wok[j])
-                    w = *reinterpret_cast<const uint2 *>(
-                        wrow[j] + (size_t)c * 32 + t * 8);
-                byte_pairs(w.x, b[0], b[1]);
-                byte_pairs(w.y, b[2], b[3]);
-            } else {
-                uint32_t w = 0x88888888u;            // zero weights
-                if (wok[j])
-                    w = *reinterpret_cast<const uint32_t *>(
-                        wrow[j] + (size_t)c * 16 + t * 4);
-                nibble_pairs(w, b);
-            }
-            mma_bf16(acc[j], ae0, ae2, b[0], b[1]);
-            mma_bf16(acc[j], ao0, ao2, b[2], b[3]);
+            weight_pairs<kQ8>(nrow[j], nok[j], c, t, b);
+            mma_n8(an[j], xe0, xe2, b[0], b[1]);
+            mma_n8(an[j], xo0, xo2, b[2], b[3]);
         }
     }
-    // accumulator (grouped row g, tile row 2t and 2t + 1) -> partials
+    // accumulators -> partials [warp][tile row][grouped row]
+    float *pw = part + (size_t)warp * V * kM;
+#pragma unroll
+    for (int q = 0; q < kLatMaxM16; ++q) {
+        if (q >= T16)
+            break;
+        const int v = 16 * q + g;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (2 * t + u < M) {
+                pw[(size_t)v * kM + 2 * t + u] = am[q][u];
+                pw[(size_t)(v + 8) * kM + 2 * t + u] = am[q][2 + u];
+            }
+    }
     if (g < M) {
 #pragma unroll
-        for (int j = 0; j < kLatMaxTiles; ++j) {
+        for (int j = 0; j < kLatMaxN8; ++j) {
             if (j >= T8)
                 break;
-            float *d = part + ((size_t)warp * V + 8 * j + 2 * t) * kM + g;
-            d[0] = acc[j][0];
-            d[kM] = acc[j][1];
+            const int v = 16 * T16 + 8 * j + 2 * t;
+            pw[(size_t)v * kM + g] = an[j][0];
+            pw[(size_t)(v + 1) * kM + g] = an[j][1];
         }
     }
     __syncthreads();
@@ -379,7 +447,7 @@ bool matvec_latency_supported(const GateUpArgs &a) {
         (reinterpret_cast<uintptr_t>(a.x) & 15) != 0)
         return false;
     const int R = lat_rows(a);
-    return 2 * R <= 8 * kLatMaxTiles &&
+    return R <= kLatMaxRowsPerCta &&
            lat_smem(a, R, lat_bucket(a.M)) <= 200 * 1024;
 }
 
