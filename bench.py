@@ -626,11 +626,12 @@ def l2_residency(gw):
 
 
 def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
-                timed_s, l2_hot=False):
+                timed_s, l2_hot=False, kernel="auto"):
     """Roofline of the fused call(s) of the operation: HBM for the decode
     kernels, the tensor core for the GEMM (burst peak unless the timed
     region lasts seconds).  The traffic of an L2-hot run has its own key
-    (taken without cache flushes)."""
+    (taken without cache flushes), and so have trellis widths other than
+    4/4 and a forced kernel choice (other kernels, other bytes)."""
     rows_per_expert = (w.routed_rows if w.repeats > 1 else
                        w.routed_rows / units["touched_experts"])
     # (the trellis kernel decodes every weight once per 8 rows at any size:
@@ -638,7 +639,10 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
     decode = rows_per_expert < 64 or fmt.startswith("trellis")
     traffic_key = w.name if op == "gate_up" else f"{w.name}:{op}"
     if fmt != "q4":
-        traffic_key += ":" + fmt.split(":")[0]
+        traffic_key += ":" + (fmt if fmt.startswith("trellis:") and
+                              fmt != "trellis:4,4" else fmt.split(":")[0])
+    if kernel != "auto":
+        traffic_key += ":" + kernel
     if l2_hot:
         traffic_key += ":l2hot"
     if decode:
@@ -759,7 +763,8 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
     peaks, peak_src = load_peaks()
     per_launch_ms = statistics.mean(call_ms) / gw.calls
     roof = roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks,
-                       peak_src, total_ms * 1e-3, l2_hot=l2_hot)
+                       peak_src, total_ms * 1e-3, l2_hot=l2_hot,
+                       kernel=args.kernel)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (activations + routing) from pinned memory, D2H of the outputs

@@ -192,3 +192,26 @@ def test_l2_residency_and_hot_traffic_key(monkeypatch):
     bench.roofline_of(gw, w, units, "gate_up", "q4", 0.005, peaks,
                       "measured", 0.1, l2_hot=True)
     assert keys == [w.name, w.name + ":l2hot"]
+
+
+def test_traffic_key_names_width_and_forced_kernel(monkeypatch):
+    """Traffic rows are per kernel set: trellis widths other than 4/4 and a
+    forced kernel choice look up keys of their own."""
+    import types
+    import bench
+    from up_swiglu_gb300 import synthetic as syn
+    keys = []
+    monkeypatch.setattr(bench, "load_traffic",
+                        lambda k: keys.append(k) or None)
+    gw = types.SimpleNamespace(calls=1, trellis=False)
+    w = syn.WORKLOADS["moe128_top8_t32_h5120_i1536"]
+    units = {"touched_experts": 117, "bytes": 6.0e8, "flops": 8e9,
+             "weight_bytes": 5.9e8}
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0,
+             "bf16_tflops_sustained": 1700.0}
+    for fmt, kernel in [("trellis:4,4", "auto"), ("trellis:4,3", "auto"),
+                        ("q8", "auto"), ("q4", "matvec")]:
+        bench.roofline_of(gw, w, units, "gate_up", fmt, 0.2, peaks,
+                          "measured", 0.1, kernel=kernel)
+    assert keys == [w.name + ":trellis", w.name + ":trellis:4,3",
+                    w.name + ":q8", w.name + ":matvec"]
