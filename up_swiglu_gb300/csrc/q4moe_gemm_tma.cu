@@ -20,7 +20,7 @@
 //  D      = two f32 accumulators in tensor memory (gate: columns 0..N-1,
 //           up: columns 256..256+N-1), lane = weight row;
 //  tail   = row scales, bf16 rounding and the SwiGLU chain per element (the
-//           bf16 sigmoid from the per-device table), or the down
+//           bf16 sigmoid from the library's constant table), or the down
 //           projection's scale and rounding.
 //
 // Measured choices (prefill workload, traces of one CTA):

@@ -4,6 +4,8 @@
 // launch_matvec picks the first version the call allows (the TMA version
 // with a fixed unit height and the generic version are batch-invariant: a
 // row's result does not depend on the other rows of the call):
+//   q4moe_matvec_lat.cu  one expert, 1 to 8 grouped rows, gate/up, not in
+//                        batch-invariant calls (laid out for latency);
 //   q4moe_matvec_tma.cu  slabs at base + e * stride, H % 256 == 0,
 //                        I % 16 == 0, 16-byte aligned weight sections
 //                        (weights moved by TMA);
