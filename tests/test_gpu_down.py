@@ -135,6 +135,33 @@ def test_down_bad_offsets_raise_status(kernel):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("counts,K,N,exact", [([1], 1536, 4096, False),
+                                              ([5], 1536, 4096, True),
+                                              ([8], 512, 4864, True),
+                                              ([3], 256, 4600, True),
+                                              ([2], 5120, 1024, False)])
+def test_down_single_expert_latency_kernel(counts, K, N, exact):
+    """One expert with at most 8 rows (the single-sequence decode): the
+    kernel laid out for latency (each CTA a few output rows, K split over
+    its warps).  N = 4864 gives every CTA 32 rows (two m16 tiles), N = 4600
+    a last CTA of 12 rows; the matvec choice runs the same kernel."""
+    _check_down(counts, K, N, exact=exact, seed=K + N)
+    _check_down(counts, K, N, kernel=q.KERNEL_MATVEC, exact=exact,
+                seed=K + N)
+
+
+def test_down_single_expert_bad_offsets():
+    """The latency kernel checks the one expert's offsets {0, M}: a wrong
+    pair raises the status bit and nothing is written."""
+    p, mid, offs = hz.down_only_problem(9, [4], 512, 1024)
+    d = hz.upload(p)
+    bad = offs.copy()
+    bad[1] = 3
+    gpu = hz.down(d, bad, mid, debug=False)
+    assert q.q4moe_device_status(clear=True) & q.DEV_BAD_ROW_OFFSETS
+    assert np.all(gpu["out"] == 0xFFFF)
+
+
 # ------------------------------------------------------------ expert MLP --
 
 def _mlp_problem(seed, E, I, H, T, k, exact):

@@ -134,7 +134,7 @@ def _check_down(counts, K, N, kernel=q.KERNEL_AUTO, exact=False, tile=0,
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("counts,K,N", [([1], 256, 128), ([3, 0, 70, 1], 512, 384),
-                                        ([9, 2], 1536, 272)])
+                                        ([9, 2], 1536, 272), ([5], 1536, 4600)])
 def test_q8_down(kernel, counts, K, N):
     if kernel == q.KERNEL_GEMM and N % 128:
         pytest.skip("the GEMM needs N % 128 == 0")

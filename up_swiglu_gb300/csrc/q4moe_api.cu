@@ -721,10 +721,18 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *slabs,
     return dispatch(a, o, d, stream);
 }
 
-int q4moe_down_proj(const void *mid, const q4moe_slabs_t *slabs,
-                    const int32_t *row_offsets, int64_t M, int64_t H,
-                    int64_t I, void *out, const q4moe_options_t *opts,
-                    cudaStream_t stream) {
+namespace {
+
+// The down projection; hold_next keeps the single-expert latency kernel
+// from releasing the next launch early.  Measured on the single-expert
+// decode (H=4096, I=1536, one row, graphs of 1000 calls): released early,
+// a chain of down projections takes 3.59 us per call instead of 4.25, but
+// an expert MLP (gate/up, then down, then the next gate/up) 10.24 instead
+// of 9.24 us, the gate/up that follows losing more than the down gains.
+int down_proj(const void *mid, const q4moe_slabs_t *slabs,
+              const int32_t *row_offsets, int64_t M, int64_t H, int64_t I,
+              void *out, const q4moe_options_t *opts, cudaStream_t stream,
+              bool hold_next) {
     int rc = check_slabs(slabs, H, I, M);
     if (rc)
         return rc;
@@ -752,7 +760,18 @@ int q4moe_down_proj(const void *mid, const q4moe_slabs_t *slabs,
     a.I = H;                                 // its output rows
     a.out = static_cast<uint16_t *>(out);
     a.gate_f32 = o.gate_f32;
+    a.hold_next = hold_next;
     return dispatch(a, o, d, stream);
+}
+
+}  // namespace
+
+int q4moe_down_proj(const void *mid, const q4moe_slabs_t *slabs,
+                    const int32_t *row_offsets, int64_t M, int64_t H,
+                    int64_t I, void *out, const q4moe_options_t *opts,
+                    cudaStream_t stream) {
+    return down_proj(mid, slabs, row_offsets, M, H, I, out, opts, stream,
+                     false);
 }
 
 int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *slabs,
@@ -777,8 +796,8 @@ int q4moe_expert_mlp(const void *x, const q4moe_slabs_t *slabs,
     q4moe_options_t od{};
     od.kernel = o.kernel;
     od.matvec_tile = o.matvec_tile;
-    return q4moe_down_proj(mid, slabs, row_offsets, M, H, I, out, &od,
-                           stream);
+    return down_proj(mid, slabs, row_offsets, M, H, I, out, &od, stream,
+                     true);
 }
 
 int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *slabs,

@@ -39,6 +39,9 @@ struct GateUpArgs {
     int32_t num_sms;
     int32_t matvec_tile;         // TMA matvec unit height (0: automatic)
     int32_t matvec_last;         // no GEMM launch follows the matvec's
+    int32_t hold_next;           // 1: the single-expert latency kernel does
+                                 // not release the next launch early (the
+                                 // down stage of the expert MLP)
     const uint16_t *sigmoid;     // sigmoid tables: [2][65536] bf16, indexed
                                  // by the bf16 bits of gateT: the page 52
                                  // tail's, then the MLX tail's

@@ -56,7 +56,7 @@ using namespace sm100;
 constexpr int kLatWarps = 16;
 constexpr int kLatThreads = kLatWarps * 32;
 constexpr int kLatMaxRows = 8;               // grouped rows per call
-constexpr int kLatMaxRowsPerCta = 16;        // R
+constexpr int kLatMaxTileRows = 32;          // weight rows per CTA
 constexpr int kLatMaxM16 = 2;                // m16 tiles: 2R <= 32 rows
 constexpr int kLatMaxN8 = 2;                 // n8 tiles: 2R mod 16 < 16
 
@@ -71,8 +71,8 @@ __host__ __device__ __forceinline__ int64_t lat_row_pitch(int64_t rb,
 __host__ __device__ __forceinline__ int64_t lat_x_pitch(int64_t H) {
     return (H * 2 + 127) / 128 * 128 + 64;
 }
-__host__ __device__ __forceinline__ int lat_tile_rows(int R) {
-    return (2 * R + 7) & ~7;
+__host__ __device__ __forceinline__ int lat_tile_rows(int NR) {
+    return (NR + 7) & ~7;
 }
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
@@ -166,20 +166,23 @@ __device__ __forceinline__ void weight_pairs(const uint8_t *row, bool ok,
     }
 }
 
-template <bool kQ8, int kM>
+template <bool kQ8, bool kDown, int kM>
 __global__ void __launch_bounds__(kLatThreads, 1)
 matvec_latency_kernel(GateUpArgs a, int R) {
     extern __shared__ __align__(128) uint8_t smem[];
-    // weights [2R][row pitch] (gate rows, then up rows), activations
-    // bf16 [kM][x pitch], partial sums f32 [warps][tile rows][kM], barriers
+    // weights [kMats R][row pitch] (gate rows, then up rows; the down
+    // projection's rows), activations bf16 [kM][x pitch] (rows of x, or of
+    // mid), partial sums f32 [warps][tile rows][kM], barriers.  For the
+    // down projection H is its K and I its output rows.
+    constexpr int kMats = kDown ? 1 : 2;
     const int64_t rb = weight_row_bytes(a, a.H);
     const int64_t rp = lat_row_pitch(rb, kQ8), xp = lat_x_pitch(a.H);
     const int H = (int)a.H, M = (int)a.M;
     const int i0 = blockIdx.x * R;
     const int nr = min(R, (int)a.I - i0);
-    const int V = lat_tile_rows(R);
+    const int NR = kMats * R, V = lat_tile_rows(NR);
     uint8_t *w_sm = smem;
-    uint8_t *x_sm = smem + (size_t)2 * R * rp;
+    uint8_t *x_sm = smem + (size_t)NR * rp;
     float *part = reinterpret_cast<float *>(x_sm + (size_t)kM * xp);
     uint64_t *bars = reinterpret_cast<uint64_t *>(
         part + (size_t)kLatWarps * V * kM);
@@ -188,10 +191,10 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid < 2 * nr) {
-        // L2 prefetch of the CTA's weight rows, gate row tid / 2 or up row
-        const int64_t row = i0 + (tid >> 1);
-        prefetch_l2(a.base + ((tid & 1) ? a.up_w_off : a.gate_w_off) +
+    if (tid < kMats * nr) {
+        // L2 prefetch of the CTA's weight rows (gate row tid / 2 or up row)
+        const int64_t row = i0 + tid / kMats;
+        prefetch_l2(a.base + (tid % kMats ? a.up_w_off : a.gate_w_off) +
                         row * rb,
                     (uint32_t)rb);
     }
@@ -205,24 +208,28 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     grid_dependency_wait();
 
     if (lane == 0 && warp != 1) {
-        // the weight rows of both matrices (they need nothing else): lane 0
-        // of each warp but warp 1 issues the rows r = k mod 15 (k = 0 for
-        // warp 0, warp - 1 for the others), the first one expecting all
-        // the bytes (the barrier's count of bytes may run ahead of it)
+        // the weight rows (they need nothing else): lane 0 of each warp
+        // but warp 1 issues the rows r = k mod 15 (k = 0 for warp 0,
+        // warp - 1 for the others; a gate row and its up row together),
+        // the first one expecting all the bytes (the barrier's count of
+        // bytes may run ahead of it)
         const int k = warp == 0 ? 0 : warp - 1;
         if (k == 0)
-            mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * 2 * rb));
+            mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * kMats * rb));
         for (int r = k; r < nr; r += kLatWarps - 1) {
             const int64_t row = i0 + r;
             bulk_g2s(smem_u32(w_sm + (size_t)r * rp),
                      a.base + a.gate_w_off + row * rb, (uint32_t)rb,
                      &bars[0]);
-            bulk_g2s(smem_u32(w_sm + (size_t)(R + r) * rp),
-                     a.base + a.up_w_off + row * rb, (uint32_t)rb, &bars[0]);
+            if (!kDown)
+                bulk_g2s(smem_u32(w_sm + (size_t)(R + r) * rp),
+                         a.base + a.up_w_off + row * rb, (uint32_t)rb,
+                         &bars[0]);
         }
     } else if (tid == 32) {
         // the row offsets of the one expert must be {0, M}; the token of
-        // each grouped row, then its activations
+        // each grouped row (the down projection reads mid row p), then its
+        // activations
         const int32_t off0 = __ldg(a.row_offsets), off1 = __ldg(a.row_offsets + 1);
         const bool bad = off0 != 0 || off1 != M;
         s_bad = bad;
@@ -232,7 +239,7 @@ matvec_latency_kernel(GateUpArgs a, int R) {
         int tok[kLatMaxRows], bad_tok = 0;
 #pragma unroll
         for (int p = 0; p < kM; ++p) {
-            tok[p] = p < M ? (int)row_token(a, p) : -1;
+            tok[p] = p >= M ? -1 : kDown ? p : (int)row_token(a, p);
             s_tok[p] = tok[p];
             if (tok[p] >= 0)
                 xbytes += (uint32_t)H * 2;
@@ -255,8 +262,9 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     if (fin) {
         sg = __ldg(reinterpret_cast<const float *>(a.base + a.gate_s_off) +
                    i0 + fr);
-        su = __ldg(reinterpret_cast<const float *>(a.base + a.up_s_off) +
-                   i0 + fr);
+        if (!kDown)
+            su = __ldg(reinterpret_cast<const float *>(a.base + a.up_s_off) +
+                       i0 + fr);
     }
     __syncthreads();                         // s_tok, s_bad, s_bad_tok
     if (s_bad_tok) {
@@ -280,8 +288,9 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     // The next launch may start now (its CTAs only prefetch before their
     // own dependency wait).  Released at the start of the kernel instead,
     // the next call's CTAs crowded these SMs and a chain of calls ran 2.3x
-    // slower; released after the arithmetic, 14% slower than never.
-    if (a.matvec_last)
+    // slower; released after the arithmetic, 14% slower than never.  The
+    // expert MLP's down stage holds it (hold_next: measured faster there).
+    if (a.matvec_last && !a.hold_next)
         grid_launch_dependents();
 
     // thread (g, t) of the warp: in an m16 tile weight rows g and g + 8
@@ -290,7 +299,11 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     // activations of grouped row g, slots 2t and 2t + 8 of each 16-wide K
     // step, serve both forms.
     const int g = lane >> 2, t = lane & 3;
-    const int T16 = 2 * R / 16, T8 = (V - 16 * T16) / 8;
+    const int T16 = NR / 16, T8 = (V - 16 * T16) / 8;
+    // weight row v of the tiles holds data (the last CTA has nr < R)
+    auto row_ok = [&](int v) {
+        return v < NR && (kDown || v < R ? v < nr : v - R < nr);
+    };
     const uint8_t *mrow[kLatMaxM16][2], *nrow[kLatMaxN8];
     bool mok[kLatMaxM16][2], nok[kLatMaxN8];
 #pragma unroll
@@ -298,13 +311,13 @@ matvec_latency_kernel(GateUpArgs a, int R) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int v = 16 * q + 8 * h + g;
-            mok[q][h] = q < T16 && (v < R ? v < nr : v - R < nr);
+            mok[q][h] = q < T16 && row_ok(v);
             mrow[q][h] = w_sm + (size_t)(mok[q][h] ? v : 0) * rp;
         }
 #pragma unroll
     for (int j = 0; j < kLatMaxN8; ++j) {
         const int v = 16 * T16 + 8 * j + g;
-        nok[j] = j < T8 && v < 2 * R && (v < R ? v < nr : v - R < nr);
+        nok[j] = j < T8 && row_ok(v);
         nrow[j] = w_sm + (size_t)(nok[j] ? v : 0) * rp;
     }
     float am[kLatMaxM16][4], an[kLatMaxN8][4];
@@ -378,15 +391,24 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     __syncthreads();
     if (!fin || s_bad)
         return;
+    const int64_t o = (int64_t)fp * a.I + i0 + fr;
     float gs = part[(size_t)fr * kM + fp];
+#pragma unroll
+    for (int w = 1; w < kLatWarps; ++w)
+        gs = __fadd_rn(gs, part[((size_t)w * V + fr) * kM + fp]);
+    const float g32 = __fmul_rn(gs, sg);
+    if (kDown) {
+        // the down projection: scale, one rounding
+        a.out[o] = bf16_rne(g32);
+        if (a.gate_f32)
+            a.gate_f32[o] = g32;
+        return;
+    }
     float us = part[(size_t)(R + fr) * kM + fp];
 #pragma unroll
-    for (int w = 1; w < kLatWarps; ++w) {
-        gs = __fadd_rn(gs, part[((size_t)w * V + fr) * kM + fp]);
+    for (int w = 1; w < kLatWarps; ++w)
         us = __fadd_rn(us, part[((size_t)w * V + R + fr) * kM + fp]);
-    }
-    const float g32 = __fmul_rn(gs, sg), u32 = __fmul_rn(us, su);
-    const int64_t o = (int64_t)fp * a.I + i0 + fr;
+    const float u32 = __fmul_rn(us, su);
     a.out[o] = swiglu_out(a.sigmoid, g32, u32);
     if (a.gate_f32)
         a.gate_f32[o] = g32;
@@ -396,9 +418,10 @@ matvec_latency_kernel(GateUpArgs a, int R) {
 
 size_t lat_smem(const GateUpArgs &a, int R, int kM) {
     const int64_t rb = weight_row_bytes(a, a.H);
-    return (size_t)2 * R * lat_row_pitch(rb, a.q8) +
+    const int NR = (a.down ? 1 : 2) * R;
+    return (size_t)NR * lat_row_pitch(rb, a.q8) +
            (size_t)kM * lat_x_pitch(a.H) +
-           (size_t)kLatWarps * lat_tile_rows(R) * kM * sizeof(float) +
+           (size_t)kLatWarps * lat_tile_rows(NR) * kM * sizeof(float) +
            2 * sizeof(uint64_t);
 }
 
@@ -408,51 +431,53 @@ int lat_rows(const GateUpArgs &a) {
     return (int)((a.I + a.num_sms - 1) / a.num_sms);
 }
 
-template <bool kQ8, int kM>
+template <bool kQ8, bool kDown, int kM>
 cudaError_t launch_m(const GateUpArgs &a, cudaStream_t s) {
     const int R = lat_rows(a);
     const size_t smem = lat_smem(a, R, kM);
     cudaError_t err = cudaFuncSetAttribute(
-        matvec_latency_kernel<kQ8, kM>,
+        matvec_latency_kernel<kQ8, kDown, kM>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
     const unsigned grid = (unsigned)((a.I + R - 1) / R);
-    return launch_pdl(matvec_latency_kernel<kQ8, kM>, dim3(grid),
+    return launch_pdl(matvec_latency_kernel<kQ8, kDown, kM>, dim3(grid),
                       dim3(kLatThreads), smem, s, a, R);
 }
 
-template <bool kQ8>
+template <bool kQ8, bool kDown>
 cudaError_t launch_q(const GateUpArgs &a, cudaStream_t s) {
     switch (lat_bucket(a.M)) {
-    case 1: return launch_m<kQ8, 1>(a, s);
-    case 2: return launch_m<kQ8, 2>(a, s);
-    case 4: return launch_m<kQ8, 4>(a, s);
-    default: return launch_m<kQ8, 8>(a, s);
+    case 1: return launch_m<kQ8, kDown, 1>(a, s);
+    case 2: return launch_m<kQ8, kDown, 2>(a, s);
+    case 4: return launch_m<kQ8, kDown, 4>(a, s);
+    default: return launch_m<kQ8, kDown, 8>(a, s);
     }
 }
 
 }  // namespace
 
-// One expert, 1..8 grouped rows, gate/up, slabs at base (no pointer table),
-// whole 16-byte weight rows and activation rows (16-byte aligned), H a
-// multiple of 32, at most 16 intermediate rows per CTA, all of them in
-// shared memory.
+// One expert, 1..8 grouped rows, gate/up or down, slabs at base (no
+// pointer table), whole 16-byte weight rows and activation rows (16-byte
+// aligned), K a multiple of 32, at most 32 weight rows per CTA (16 of each
+// gate/up matrix), all of them in shared memory.
 bool matvec_latency_supported(const GateUpArgs &a) {
     const int64_t rb = weight_row_bytes(a, a.H);
-    if (a.E != 1 || a.M < 1 || a.M > kLatMaxRows || a.down || a.invariant ||
+    if (a.E != 1 || a.M < 1 || a.M > kLatMaxRows || a.invariant ||
         a.slab_ptrs != nullptr || a.H % 32 != 0 || rb % 16 != 0 ||
         a.gate_w_off % 16 != 0 || a.up_w_off % 16 != 0 ||
         (reinterpret_cast<uintptr_t>(a.base) & 15) != 0 ||
         (reinterpret_cast<uintptr_t>(a.x) & 15) != 0)
         return false;
     const int R = lat_rows(a);
-    return R <= kLatMaxRowsPerCta &&
+    return (a.down ? 1 : 2) * R <= kLatMaxTileRows &&
            lat_smem(a, R, lat_bucket(a.M)) <= 200 * 1024;
 }
 
 cudaError_t launch_matvec_latency(const GateUpArgs &a, cudaStream_t s) {
-    return a.q8 ? launch_q<true>(a, s) : launch_q<false>(a, s);
+    if (a.down)
+        return a.q8 ? launch_q<true, true>(a, s) : launch_q<false, true>(a, s);
+    return a.q8 ? launch_q<true, false>(a, s) : launch_q<false, false>(a, s);
 }
 
 }  // namespace q4moe
