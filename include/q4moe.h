@@ -323,7 +323,10 @@ int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
  * x up to 256 grouped rows) and the others on the HBM-streaming matvec;
  * with fewer rows the matvec takes every expert and the GEMM is not
  * launched.  One expert goes to the GEMM when it has more than 48 rows and
- * makes at least one tile per SM, else to the matvec.
+ * makes at least one tile per SM, else to the matvec: with at most 8 rows
+ * to a version laid out for latency (each SM a few rows, the K range split
+ * over its warps; also for the down projection), which the batch-invariant
+ * choice never uses.
  */
 int q4moe_gate_up_swiglu(const void *x, const q4moe_slabs_t *expert_slabs,
                          const int32_t *row_offsets_per_expert,
