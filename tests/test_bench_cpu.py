@@ -215,3 +215,16 @@ def test_traffic_key_names_width_and_forced_kernel(monkeypatch):
                           "measured", 0.1, kernel=kernel)
     assert keys == [w.name + ":trellis", w.name + ":trellis:4,3",
                     w.name + ":q8", w.name + ":matvec"]
+
+
+def test_bracket_stride_samples_at_least_four_steps():
+    """The fused call is timed on every stride-th step: 8 for long runs,
+    at least 4 samples when there are 4 steps or more, every step below."""
+    import bench
+    assert bench.bracket_stride(100) == 8
+    assert bench.bracket_stride(20) == 5
+    assert bench.bracket_stride(3) == 1 and bench.bracket_stride(1) == 1
+    for k in range(1, 200):
+        s = bench.bracket_stride(k)
+        n = sum(1 for i in range(k) if i % s == s - 1)
+        assert n >= min(k, 4)

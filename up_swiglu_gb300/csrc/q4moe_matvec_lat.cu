@@ -86,13 +86,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src,
         : "memory");
 }
 
-// Ask L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p),
-                 "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -21,6 +21,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16 bytes).
+// A prefetch only warms L2, the point of coherence, so it never makes data
+// stale: it may be issued before a dependency wait.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
