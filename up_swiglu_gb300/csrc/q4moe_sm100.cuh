@@ -30,6 +30,12 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
                  : "memory");
 }
 
+// Ask L2 for the 128-byte line holding p (an ordinary per-thread prefetch,
+// through the load path rather than the TMA unit).
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
