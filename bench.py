@@ -679,6 +679,84 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
             "peak_source": f"{key} of {peak_src}"}
 
 
+# Copies per step from which the end-to-end loop double-buffers (below, the
+# streams' and events' host work costs more than the overlap gains: the
+# small single expert measured 1.4 against 3.7 GB/s).
+PIPELINE_MIN_BYTES = 256 * 1024
+
+
+def e2e_time(gw, op, x_h, t_h, steps, copy_routing, pipeline=True):
+    """Milliseconds per step end to end: every step copies its inputs from
+    pinned host memory to the device and reads its outputs back.  A step of
+    one call with enough bytes to copy double-buffers them (the copies of
+    steps k + 1 and k - 1 run on two copy streams while step k computes); a
+    graph of calls, whose buffers the graph fixes, and a small step copy in
+    their stream's order.  Returns (ms, pipelined)."""
+    import torch
+    dev, stream = gw.dev, gw.stream
+    in_name = "mid" if op == "down" else "x"
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if gw.graph is not None or not pipeline:
+        o_h = torch.empty(gw.out.shape, dtype=torch.int16).pin_memory()
+        x_dev = getattr(gw, in_name)
+        e0.record(stream)
+        for _ in range(steps):
+            x_dev.copy_(x_h, non_blocking=True)
+            if copy_routing:
+                gw.topk.copy_(t_h, non_blocking=True)
+            gw.enqueue_step()
+            o_h.copy_(gw.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps, False
+    # two slots of the buffers the copies touch (inputs, routing, outputs);
+    # the grouping, workspace and scratch are used by the compute stream only
+    slots = [(getattr(gw, in_name), gw.topk, gw.out),
+             (torch.empty_like(getattr(gw, in_name)),
+              torch.empty_like(gw.topk), torch.empty_like(gw.out))]
+    o_h = [torch.empty(gw.out.shape, dtype=torch.int16).pin_memory()
+           for _ in range(2)]
+    h2d_s = torch.cuda.Stream(dev)
+    d2h_s = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    saved = slots[0]
+    e0.record(stream)
+    h2d_s.wait_event(e0)
+    d2h_s.wait_event(e0)
+    for k in range(steps):
+        sl = k % 2
+        x_d, t_d, out_d = slots[sl]
+        with torch.cuda.stream(h2d_s):
+            if k >= 2:                       # step k - 2 done with the slot
+                h2d_s.wait_event(ev_done[sl])
+            x_d.copy_(x_h, non_blocking=True)
+            if copy_routing:
+                t_d.copy_(t_h, non_blocking=True)
+            ev_in[sl].record(h2d_s)
+        stream.wait_event(ev_in[sl])
+        if k >= 2:                           # step k - 2's outputs read
+            stream.wait_event(ev_read[sl])
+        setattr(gw, in_name, x_d)
+        gw.topk, gw.out = t_d, out_d
+        gw.enqueue_step()
+        ev_done[sl].record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev_done[sl])
+            o_h[sl].copy_(out_d, non_blocking=True)
+            ev_read[sl].record(d2h_s)
+    stream.wait_stream(d2h_s)
+    stream.wait_stream(h2d_s)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    setattr(gw, in_name, saved[0])
+    gw.topk, gw.out = saved[1], saved[2]
+    return e0.elapsed_time(e1) / steps, True
+
+
 def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
             headline=False, l2_hot=False):
     """Set up one workload, time it (warm-up, then exactly args.steps steps
@@ -782,30 +860,18 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
                        peak_src, total_ms * 1e-3, l2_hot=l2_hot,
                        kernel=args.kernel)
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs (activations + routing) from pinned memory, D2H of the outputs
-    # (the down projection's input is mid instead of x)
-    x_dev = gw.mid if op == "down" else gw.x
+    # end to end through the public API with host buffers: H2D of every
+    # step's inputs (activations + routing) from pinned memory, D2H of its
+    # outputs (the down projection's input is mid instead of x)
     x_src = gw.host["mid"] if op == "down" else gw.host["x"]
     x_h = torch.from_numpy(x_src.view(np.int16)).pin_memory()
     t_h = torch.from_numpy(gw.topk_host).pin_memory()
-    o_h = torch.empty(gw.out.shape, dtype=torch.int16).pin_memory()
     h2d = x_h.numel() * 2 + (t_h.numel() * 4 if w.repeats == 1 else 0)
-    d2h = o_h.numel() * 2
+    d2h = gw.out.numel() * 2
     e2e_steps = max(3, min(args.steps, 10))
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        x_dev.copy_(x_h, non_blocking=True)
-        if w.repeats == 1:
-            gw.topk.copy_(t_h, non_blocking=True)
-        gw.enqueue_step()
-        o_h.copy_(gw.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms, pipelined = e2e_time(gw, op, x_h, t_h, e2e_steps,
+                                 copy_routing=w.repeats == 1,
+                                 pipeline=h2d + d2h >= PIPELINE_MIN_BYTES)
     e2e_value = units["weight_bytes"] * world / (e2e_ms * 1e-3) / 1e9
     status = q.q4moe_device_status(stream, clear=True)
     res = {
@@ -813,7 +879,10 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
         "value": value, "tflops": tflops, "roofline": roof, "cpu": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "copies": ("overlapping the neighbouring steps' compute "
+                           "(two buffer sets, two copy streams)"
+                           if pipelined else "in the step's stream order")},
         "launches": int(launches), "status": status,
         "call_ms": statistics.mean(call_ms),
         "clocks": clk.summary() if clk is not None else None,
