@@ -632,7 +632,7 @@ def bracket_stride(steps: int) -> int:
 
 
 def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
-                timed_s, l2_hot=False, kernel="auto"):
+                timed_s, l2_hot=False, kernel="auto", workspace=True):
     """Roofline of the fused call(s) of the operation: HBM for the decode
     kernels, the tensor core for the GEMM (burst peak unless the timed
     region lasts seconds).  The traffic of an L2-hot run has its own key
@@ -649,6 +649,8 @@ def roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks, peak_src,
                               fmt != "trellis:4,4" else fmt.split(":")[0])
     if kernel != "auto":
         traffic_key += ":" + kernel
+    if not workspace and op != "down":
+        traffic_key += ":no_workspace"
     if l2_hot:
         traffic_key += ":l2hot"
     if decode:
@@ -858,7 +860,7 @@ def measure(args, w, local, dist, world, rank, op, fmt, cpu_seconds,
     per_launch_ms = statistics.mean(call_ms) / gw.calls
     roof = roofline_of(gw, w, units, op, fmt, per_launch_ms, peaks,
                        peak_src, total_ms * 1e-3, l2_hot=l2_hot,
-                       kernel=args.kernel)
+                       kernel=args.kernel, workspace=not args.no_workspace)
 
     # end to end through the public API with host buffers: H2D of every
     # step's inputs (activations + routing) from pinned memory, D2H of its

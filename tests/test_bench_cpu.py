@@ -213,8 +213,11 @@ def test_traffic_key_names_width_and_forced_kernel(monkeypatch):
                         ("q8", "auto"), ("q4", "matvec")]:
         bench.roofline_of(gw, w, units, "gate_up", fmt, 0.2, peaks,
                           "measured", 0.1, kernel=kernel)
+    bench.roofline_of(gw, w, units, "gate_up", "q4", 0.2, peaks, "measured",
+                      0.1, workspace=False)
     assert keys == [w.name + ":trellis", w.name + ":trellis:4,3",
-                    w.name + ":q8", w.name + ":matvec"]
+                    w.name + ":q8", w.name + ":matvec",
+                    w.name + ":no_workspace"]
 
 
 def test_bracket_stride_samples_at_least_four_steps():
