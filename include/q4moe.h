@@ -358,7 +358,8 @@ int q4moe_gate_up_swiglu_ex(const void *x, const q4moe_slabs_t *expert_slabs,
  *                           scale before rounding.  num_tokens, up_f32 and
  *                           workspace must be 0 / NULL (the rows of mid are
  *                           already grouped).
- * Kernel choice per expert as for gate/up; the GEMM's tiles are 256 output
+ * Kernel choice per expert as for gate/up, with experts above 32 rows (not
+ * 16) on the GEMM when it is launched; the GEMM's tiles are 256 output
  * rows.  Summation order: as for gate/up (exact inputs give exact bits).
  */
 int q4moe_down_proj(const void *mid, const q4moe_slabs_t *expert_slabs,

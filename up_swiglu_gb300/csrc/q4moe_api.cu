@@ -371,19 +371,21 @@ int dispatch(q4moe::GateUpArgs &a, const q4moe_options_t &o,
         matvec_max = 0;
     } else if (o.kernel == Q4MOE_KERNEL_AUTO && gemm_ok) {
         // Several experts: when the call has at least 4 rows per expert on
-        // average, experts above 16 rows go to the GEMM and the rest to the
-        // matvec (both launched; an expert's count is known on the device
-        // only); with fewer rows the matvec takes every expert (no GEMM
-        // launch).  Measured on the verify workload (1024 rows over 160
-        // experts, Zipf): 0.344 ms on the matvec alone, 0.298 ms with the
-        // experts above 16 rows on the GEMM (8: 0.326, 32: 0.324, 48:
-        // 0.341); a GEMM launch that finds no expert costs ~3 % of the
+        // average, experts above 16 rows (32 for the down projection) go
+        // to the GEMM and the rest to the matvec (both launched; an
+        // expert's count is known on the device only); with fewer rows the
+        // matvec takes every expert (no GEMM launch).  Measured on the
+        // verify workload (1024 rows over 160 experts, Zipf): gate/up 0.344
+        // ms on the matvec alone, 0.294 ms with the experts above 16 rows
+        // on the GEMM (12: 0.334, 24: 0.293, 32: 0.321); the down
+        // projection 0.170 ms above 16, 0.162 above 32 (48: 0.179, 64:
+        // 0.184); a GEMM launch that finds no expert costs ~3 % of the
         // grouped decode (256 rows over 128 experts).  One expert: the
         // GEMM when its rows fill every SM with tiles.
         const int64_t row_tiles = q4moe::gemm_row_tiles(a);
         const int64_t tiles = (a.M + 255) / 256 * row_tiles;
         if (a.E > 1 && a.M >= 4 * (int64_t)a.E) {
-            matvec_max = 16;
+            matvec_max = a.down ? 32 : 16;
         } else if (a.E == 1 && a.M > 48 && tiles >= d->num_sms) {
             matvec_max = 0;
         }
