@@ -13,12 +13,12 @@
 // coherence, so it is safe whatever the previous kernel writes); the
 // previous call releases this one as soon as its own CTAs hold their
 // operands, so that prefetch overlaps the previous call's arithmetic.
-// Right after the dependency wait one thread of each of 15 warps issues
-// the bulk copies (cp.async.bulk) of a gate row and the matching up row
-// (one thread issuing them all took 0.26 us longer per call) while a
-// thread of the other warp checks the row offsets, reads the token indices
-// and issues one copy per activation row, and the threads that finish the
-// rows load their row scales.
+// Right after the dependency wait one thread of each of 14 warps (15 for
+// the down projection) issues the bulk copies (cp.async.bulk) of a gate
+// row and the matching up row (one thread issuing them all took 0.26 us
+// longer per call) while a thread of another warp reads the token indices
+// and issues one copy per activation row, the row offsets are checked
+// beside them, and the threads that finish the rows load their scales.
 //
 // The products go to the tensor core, mma.sync m16n8k16 (bf16 in, f32
 // accumulate).  The CTA's 2R weight rows (gate rows, then up rows) form m16
@@ -84,6 +84,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src,
         "[%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// The row offsets of a call's one expert must be {0, M}: *bad = whether
+// they are not (block 0 raises the status bit).
+__device__ __forceinline__ void check_single_offsets(const GateUpArgs &a,
+                                                     int M, int *bad) {
+    const int32_t off0 = __ldg(a.row_offsets), off1 = __ldg(a.row_offsets + 1);
+    const bool b = off0 != 0 || off1 != M;
+    *bad = b;
+    if (b && blockIdx.x == 0)
+        atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
 }
 
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
@@ -200,16 +211,21 @@ matvec_latency_kernel(GateUpArgs a, int R) {
     __syncthreads();
     grid_dependency_wait();
 
-    if (lane == 0 && warp != 1) {
-        // the weight rows (they need nothing else): lane 0 of each warp
-        // but warp 1 issues the rows r = k mod 15 (k = 0 for warp 0,
-        // warp - 1 for the others; a gate row and its up row together),
-        // the first one expecting all the bytes (the barrier's count of
-        // bytes may run ahead of it)
+    // gate/up: warp 15 checks the offsets beside the activation copies
+    // (measured 0.7 % faster); the down projection, whose activation rows
+    // need no token lookup, checks them after issuing those copies and
+    // keeps warp 15 issuing weight rows (0.9 % faster)
+    constexpr int kIssuers = kDown ? kLatWarps - 1 : kLatWarps - 2;
+    if (lane == 0 && warp != 1 && warp <= kIssuers) {
+        // the weight rows (they need nothing else): lane 0 of warp 0 and
+        // of warps 2..kIssuers issues the rows r = k mod kIssuers (k = 0
+        // for warp 0, warp - 1 for the others; a gate row and its up row
+        // together), the first one expecting all the bytes (the barrier's
+        // count of bytes may run ahead of it)
         const int k = warp == 0 ? 0 : warp - 1;
         if (k == 0)
             mbar_arrive_expect_tx(&bars[0], (uint32_t)(nr * kMats * rb));
-        for (int r = k; r < nr; r += kLatWarps - 1) {
+        for (int r = k; r < nr; r += kIssuers) {
             const int64_t row = i0 + r;
             bulk_g2s(smem_u32(w_sm + (size_t)r * rp),
                      a.base + a.gate_w_off + row * rb, (uint32_t)rb,
@@ -219,15 +235,13 @@ matvec_latency_kernel(GateUpArgs a, int R) {
                          a.base + a.up_w_off + row * rb, (uint32_t)rb,
                          &bars[0]);
         }
+    } else if (!kDown && tid == (kLatWarps - 1) * 32) {
+        // the row offsets of the one expert must be {0, M} (checked beside
+        // the copies: only the stores wait for the answer)
+        check_single_offsets(a, M, &s_bad);
     } else if (tid == 32) {
-        // the row offsets of the one expert must be {0, M}; the token of
-        // each grouped row (the down projection reads mid row p), then its
-        // activations
-        const int32_t off0 = __ldg(a.row_offsets), off1 = __ldg(a.row_offsets + 1);
-        const bool bad = off0 != 0 || off1 != M;
-        s_bad = bad;
-        if (bad && blockIdx.x == 0)
-            atomicOr(a.status, Q4MOE_DEV_BAD_ROW_OFFSETS);
+        // the token of each grouped row (the down projection reads mid row
+        // p), then its activations
         uint32_t xbytes = 0;
         int tok[kLatMaxRows], bad_tok = 0;
 #pragma unroll
@@ -247,6 +261,8 @@ matvec_latency_kernel(GateUpArgs a, int R) {
                 bulk_g2s(smem_u32(x_sm + (size_t)p * xp),
                          a.x + (int64_t)tok[p] * H, (uint32_t)H * 2,
                          &bars[1]);
+        if (kDown)
+            check_single_offsets(a, M, &s_bad);
     }
     // the thread that finishes (row r, grouped row p) loads r's scales
     const bool fin = tid < nr * M;
