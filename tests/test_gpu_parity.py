@@ -443,6 +443,29 @@ def test_single_expert_several_chunks(exact):
     _run_and_compare(p, exact=exact)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("I,H", [(100, 96), (1536, 4128), (256, 512)])
+def test_single_expert_latency_kernel_shapes(M, I, H):
+    """One expert with 1 to 8 rows runs on the kernel laid out for latency
+    (each CTA ceil(I / SMs) intermediate rows, the K range split over its
+    warps): K = 96 and 4128 (not multiples of 256, which the ring matvec
+    needs), I = 100 (one row per CTA), row counts of each of its template
+    sizes and between; exact and real-valued against the oracle."""
+    for exact in (True, False):
+        p = hz.problem_with_counts(40 + M + I, [M], I, H, exact=exact)
+        _run_and_compare(p, exact=exact)
+
+
+@pytest.mark.parametrize("shift", [40, -60, -90])
+def test_single_expert_latency_kernel_scaled_activations(shift):
+    """The latency kernel multiplies bf16 activations as they are (no f16
+    staging): exact-integer activations times 2^shift still give exact
+    sums, so the bits must match the oracle's."""
+    p = hz.problem_with_counts(81, [3], 1536, 1024, exact=True)
+    p.x = _scale_bf16(p.x, shift)
+    _run_and_compare(p, exact=True)
+
+
 @pytest.mark.parametrize("kernel", [q.KERNEL_AUTO, q.KERNEL_MATVEC])
 def test_single_chunk_bad_token_reads_zeros(kernel):
     """One expert, 6 rows (a single chunk, whose rows of x move as bulk

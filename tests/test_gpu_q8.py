@@ -156,6 +156,16 @@ def test_q8_mlp_exact_mid_then_down(kernel):
     parity.compare_down_bits(gpu["out"], orc, hz.down_scales(p, offs), p.I)
 
 
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_q8_single_expert_latency_kernel(M):
+    """Q8, one expert with 1 to 8 rows (the kernel laid out for latency):
+    K = 160 (rows of 160 bytes), I = 100 (one row per CTA); exact and
+    real-valued against the Q8 oracle."""
+    for exact in (True, False):
+        p = hz.q8_counts_problem(50 + M, [M], 100, 160, exact=exact)
+        _check(p, exact=exact)
+
+
 def test_q8_full_size_decode_sampled():
     """Q8 at the grouped-decode size (128 experts, top-8, 32 tokens,
     H = 5120, I = 1536): sampled outputs and whole rows against the
