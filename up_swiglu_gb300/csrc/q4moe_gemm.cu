@@ -199,8 +199,11 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
 // experts above the matvec's row limit) into the workspace, bf16 [M][H].
 // The offsets are staged in shared memory (the expert of a row is a binary
 // search there); one warp copies one row, each lane keeping four 16-byte
-// loads in flight.
+// loads in flight.  kPairs writes each chunk of 8 activations in the order
+// {0,4,1,5,2,6,3,7} (the Q4 gate/up form of q4moe_gemm_tma.cu, whose
+// dequantised weights come in that order).
 constexpr int kGatherThreads = 256;
+template <bool kPairs>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_rows_kernel(GateUpArgs a) {
     extern __shared__ int32_t s_goff[];
@@ -242,6 +245,13 @@ gather_rows_kernel(GateUpArgs a) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t c = c0 + 32 * u;
+                if (kPairs) {           // {x0x1,x2x3,x4x5,x6x7} -> {x0x4,..}
+                    const uint4 w = v[u];
+                    v[u] = make_uint4(__byte_perm(w.x, w.z, 0x5410),
+                                      __byte_perm(w.x, w.z, 0x7632),
+                                      __byte_perm(w.y, w.w, 0x5410),
+                                      __byte_perm(w.y, w.w, 0x7632));
+                }
                 if (c < chunks)
                     dst[c] = v[u];
             }
@@ -769,8 +779,11 @@ cudaError_t launch_gemm(const GateUpArgs &a, cudaStream_t s) {
     const int blocks = (int)std::min<int64_t>(
         (a.M + kGatherThreads / 32 - 1) / (kGatherThreads / 32),
         (int64_t)a.num_sms * 8);
-    if ((err = launch_pdl(gather_rows_kernel, dim3((unsigned)blocks),
-                          dim3(kGatherThreads),
+    // the tensor-core GEMM's Q4 form reads its activations in paired order
+    const bool pairs = ts && !a.q8;
+    if ((err = launch_pdl(pairs ? gather_rows_kernel<true>
+                                : gather_rows_kernel<false>,
+                          dim3((unsigned)blocks), dim3(kGatherThreads),
                           sizeof(int32_t) * (size_t)(a.E + 1), s, a)) !=
         cudaSuccess)
         return err;
