@@ -21,9 +21,11 @@
 //           in which A's cheapest dequantisation yields the weights;
 //  D      = two f32 accumulators in tensor memory (gate: columns 0..N-1,
 //           up: columns 256..256+N-1), lane = weight row;
-//  tail   = row scales, bf16 rounding and the SwiGLU chain per element (the
-//           bf16 sigmoid from the library's constant table), or the down
-//           projection's scale and rounding.
+//  tail   = row scales, bf16 rounding and the SwiGLU chain on packed pairs
+//           of columns (one conversion rounds two values, two packed bf16
+//           multiplies give two outputs; the bf16 sigmoid from the
+//           library's constant table), or the down projection's scale and
+//           rounding.
 //
 // Measured choices (prefill workload, traces of one CTA, steps in ms):
 //  * each dequantisation thread prefetches its row's line 4 blocks past
@@ -544,37 +546,51 @@ gemm_tma_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                 }
                 const int64_t o0 = (int64_t)(ti.row0 + c0) * a.I + i;
                 if (kDown) {
-                    // out = bf16(sum * scale) for both halves
+                    // out = bf16(sum * scale) for both halves, rounded in
+                    // packed pairs of columns
+                    uint32_t lo[kC / 2], hi[kC / 2];
+#pragma unroll
+                    for (int jj = 0; jj < kC; jj += 2) {
+                        lo[jj / 2] = bf16x2_rn(g32[jj], g32[jj + 1]);
+                        hi[jj / 2] = bf16x2_rn(u32[jj], u32[jj + 1]);
+                    }
 #pragma unroll
                     for (int jj = 0; jj < kC; ++jj) {
                         if (c0 + jj < ti.nvalid) {
+                            const int sh = (jj & 1) * 16;
                             const int64_t oi = o0 + (int64_t)jj * a.I;
-                            a.out[oi] = bf16_bits(g32[jj]);
+                            a.out[oi] = (uint16_t)(lo[jj / 2] >> sh);
                             if (a.gate_f32)
                                 a.gate_f32[oi] = g32[jj];
                             if (hi_ok) {
-                                a.out[oi + hi_row] = bf16_bits(u32[jj]);
+                                a.out[oi + hi_row] =
+                                    (uint16_t)(hi[jj / 2] >> sh);
                                 if (a.gate_f32)
                                     a.gate_f32[oi + hi_row] = u32[jj];
                             }
                         }
                     }
                 } else {
-                    // independent chains the scheduler can interleave;
-                    // sigmoids from the table
-                    float sT[kC];
+                    // packed pairs of columns: gateT and upT by one
+                    // conversion each, the sigmoids from the table, the
+                    // two products by packed bf16 multiplies
+                    uint32_t ob[kC / 2];
 #pragma unroll
-                    for (int jj = 0; jj < kC; ++jj)
-                        sT[jj] = bf16_f32(sigmoid_bf16_table(
-                            a.sigmoid,
-                            (uint16_t)(__float_as_uint(bf16_round(g32[jj])) >>
-                                       16)));
+                    for (int jj = 0; jj < kC; jj += 2) {
+                        const uint32_t g2 = bf16x2_rn(g32[jj], g32[jj + 1]);
+                        const uint32_t s2 =
+                            (uint32_t)sigmoid_bf16_table(a.sigmoid,
+                                                         (uint16_t)g2) |
+                            ((uint32_t)sigmoid_bf16_table(
+                                 a.sigmoid, (uint16_t)(g2 >> 16))
+                             << 16);
+                        ob[jj / 2] = swiglu_tail_pair(
+                            g2, s2, bf16x2_rn(u32[jj], u32[jj + 1]));
+                    }
 #pragma unroll
                     for (int jj = 0; jj < kC; ++jj) {
-                        const float si = bf16_round(
-                            __fmul_rn(bf16_round(g32[jj]), sT[jj]));
                         const uint16_t o =
-                            bf16_bits(__fmul_rn(si, bf16_round(u32[jj])));
+                            (uint16_t)(ob[jj / 2] >> ((jj & 1) * 16));
                         if (c0 + jj < ti.nvalid) {
                             const int64_t oi = o0 + (int64_t)jj * a.I;
                             a.out[oi] = o;

@@ -166,6 +166,30 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
     return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
 }
 
+// Two f32 values rounded to bf16 (to nearest even) by one packed
+// conversion: lo in the low half, hi in the high half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// The tail's two products, sil = bf16(gateT * sigT) and out =
+// bf16(sil * upT), on packed pairs of bf16 (bit patterns).  Both operands
+// of each product are bf16, so its exact value has at most 16 significant
+// bits: from 2^-134 up it is an f32, and below 2^-134 it rounds to zero in
+// bf16 whatever comes first.  The page's f32 multiply followed by rounding
+// to bf16 is therefore a single rounding, the one the packed bf16 multiply
+// (round to nearest even, subnormals kept) makes.
+__device__ __forceinline__ uint32_t swiglu_tail_pair(uint32_t g2, uint32_t s2,
+                                                     uint32_t u2) {
+    const __nv_bfloat162 si =
+        __hmul2_rn(*reinterpret_cast<const __nv_bfloat162 *>(&g2),
+                   *reinterpret_cast<const __nv_bfloat162 *>(&s2));
+    const __nv_bfloat162 o =
+        __hmul2_rn(si, *reinterpret_cast<const __nv_bfloat162 *>(&u2));
+    return *reinterpret_cast<const uint32_t *>(&o);
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
