@@ -322,7 +322,9 @@ int q4moe_group_rows(const int32_t *topk_ids, int64_t T, int32_t k,
  * rows run on the tcgen05 tensor-core GEMM (tiles of 128 intermediate rows
  * x up to 256 grouped rows) and the others on the HBM-streaming matvec;
  * with fewer rows the matvec takes every expert and the GEMM is not
- * launched.  One expert goes to the GEMM when it has more than 48 rows and
+ * launched; from 128 rows per expert on average (M >= 128 E) the GEMM
+ * takes every expert and the matvec is not launched.  One expert goes to
+ * the GEMM when it has more than 48 rows and
  * makes at least one tile per SM, else to the matvec: with at most 8 rows
  * to a version laid out for latency (each SM a few rows, the K range split
  * over its warps; also for the down projection), which the batch-invariant

@@ -224,13 +224,17 @@ def test_auto_mixes_matvec_and_gemm(big):
 @pytest.mark.parametrize("counts,launches", [([3] * 20, 1),
                                              ([60] + [1] * 39, 1),
                                              ([8] * 10, 2),
-                                             ([60] * 2 + [1] * 6, 2)])
+                                             ([60] * 2 + [1] * 6, 2),
+                                             ([130, 129, 131], 1),
+                                             ([200, 10, 200], 1)])
 def test_auto_skips_a_gemm_that_cannot_get_work(counts, launches):
     """Under the automatic choice the GEMM is launched only when the call
     has at least 4 rows per expert: 60 rows over 20 experts, or 99 over 40
     with one expert of 60, take the matvec alone (one launch); 80 rows over
     10 experts launch the GEMM as well, which finds no expert above 16 rows;
-    126 over 8 give it the two experts of 60.  Same results either way."""
+    126 over 8 give it the two experts of 60.  From 128 rows per expert on
+    average the GEMM alone takes every expert (one launch), a 10-row
+    expert included.  Same results either way."""
     import torch
     p = hz.problem_with_counts(77, counts, 1536, 512, exact=True)
     d = hz.upload(p)
