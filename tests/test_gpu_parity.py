@@ -380,6 +380,17 @@ def test_parity_noncanonical_layout_and_pointer_table():
     _run_and_compare(p, ptr_table=True)
     _run_and_compare(p, kernel=q.KERNEL_GEMM, layout=L, stride_pad=8192)
     _run_and_compare(p, kernel=q.KERNEL_GEMM, ptr_table=True)
+    # weight sections 16 bytes past a 32-byte boundary: the tensor-core
+    # GEMM whose weight loads are 32 bytes wide is not taken, the other
+    # one (with or without the workspace) gives the same results
+    L16 = q.q4moe_layout_t()
+    L16.hidden_size, L16.intermediate_size = H, I
+    L16.up_s_offset = 0
+    L16.gate_s_offset = 4096
+    L16.up_w_offset = 8192 + 16
+    L16.gate_w_offset = 8192 + 16 + wb + 256
+    L16.slab_bytes = (L16.gate_w_offset + wb + 4095) // 4096 * 4096
+    _run_and_compare(p, kernel=q.KERNEL_GEMM, layout=L16, stride_pad=8192)
 
 
 def test_max_experts_and_empty_call():

@@ -10,7 +10,8 @@
 //           two blocks of 128 output rows of the one matrix) x up to 256 of
 //           the expert's grouped rows;
 //  A      = the tile's packed weights, each of 8 warps streaming its rows
-//           (one row of one matrix per thread) through a register ring four
+//           (one row of one matrix per thread, a 64-K block by one 256-bit
+//           load for nibbles, two for bytes) through a register ring four
 //           64-K blocks deep (two for bytes), dequantised (nibble - 8 or the
 //           signed byte, exact in bf16) into shared memory in the 128-byte
 //           swizzled K-major layout, 64 K per stage, four stages;
@@ -28,6 +29,10 @@
 //           rounding.
 //
 // Measured choices (prefill workload, traces of one CTA, steps in ms):
+//  * the weights come 32 bytes per load instruction (ld.global.nc.v8):
+//    Q4 0.895 -> 0.862, Q8 1.162 -> 0.998 against two 16-byte loads (half
+//    the load instructions, and half the L1 lookups for rows that each
+//    sit in their own line);
 //  * each dequantisation thread prefetches its row's line 4 blocks past
 //    its register ring into L2: the ring's loads then wait on L2, not HBM
 //    (0.977 -> 0.939; the bulk prefetch instead, queued on the TMA unit,
@@ -228,6 +233,16 @@ __device__ __forceinline__ uint4 bytes_bf16(uint32_t w0, uint32_t w1) {
                       byte_pair(__byte_perm(w0, 0x43434343u, 0x4342)),
                       byte_pair(__byte_perm(w1, 0x43434343u, 0x4140)),
                       byte_pair(__byte_perm(w1, 0x43434343u, 0x4342)));
+}
+
+// 32 bytes of weights (two uint4) by one 256-bit load; p must be 32-byte
+// aligned (gemm_tma_supported checks the sections; rows hold a whole
+// number of 64-K blocks, a multiple of 32 bytes).
+__device__ __forceinline__ void ldg_32(const uint4 *p, uint4 &lo, uint4 &hi) {
+    asm("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x),
+          "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+        : "l"(p));
 }
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
@@ -437,11 +452,17 @@ gemm_tma_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                 (m ? a.up_w_off : a.gate_w_off) + row * rb);
             uint4 ring[kDepth][kVecs];
 #pragma unroll
-            for (int d = 0; d < kDepth; ++d)
+            for (int d = 0; d < kDepth; ++d) {
 #pragma unroll
-                for (int v = 0; v < kVecs; ++v)
-                    ring[d][v] = (rok && d < KB) ? __ldg(src + kVecs * d + v)
-                                                 : kZero;
+                for (int v = 0; v < kVecs; v += 2) {
+                    if (rok && d < KB) {
+                        ldg_32(src + kVecs * d + v, ring[d][v], ring[d][v + 1]);
+                    } else {
+                        ring[d][v] = kZero;
+                        ring[d][v + 1] = kZero;
+                    }
+                }
+            }
             // two 64-K blocks per round (one proxy fence for both)
             for (int kb0 = 0; kb0 < KB && ok; kb0 += kDepth) {
 #pragma unroll
@@ -482,8 +503,9 @@ gemm_tma_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
                         const int kn = kb + q + kDepth;
                         if (kn < KB && rok) {
 #pragma unroll
-                            for (int v = 0; v < kVecs; ++v)
-                                ring[d + q][v] = __ldg(src + kVecs * kn + v);
+                            for (int v = 0; v < kVecs; v += 2)
+                                ldg_32(src + kVecs * kn + v, ring[d + q][v],
+                                       ring[d + q][v + 1]);
                         }
                         // the row's 128-byte line kPrefetch blocks past
                         // the ring into L2, so the ring's loads find it
@@ -673,11 +695,14 @@ cudaError_t launch_fmt(const GateUpArgs &a, const uint16_t *rows,
 }  // namespace
 
 // This GEMM takes slabs at base + e * stride whose weight rows hold a whole
-// number of 64-K stages, with 16-byte aligned weight sections.
+// number of 64-K stages, with 32-byte aligned weight sections (its weight
+// loads are 32 bytes wide; the slab base and stride are multiples of
+// Q4MOE_SLAB_ALIGNMENT).
 bool gemm_tma_supported(const GateUpArgs &a) {
+    static_assert(Q4MOE_SLAB_ALIGNMENT % 32 == 0, "32-byte weight loads");
     return a.slab_ptrs == nullptr && a.H % BK == 0 &&
-           a.gate_w_off % 16 == 0 && a.up_w_off % 16 == 0 &&
-           (reinterpret_cast<uintptr_t>(a.base) & 15) == 0 &&
+           a.gate_w_off % 32 == 0 && a.up_w_off % 32 == 0 &&
+           (reinterpret_cast<uintptr_t>(a.base) & 31) == 0 &&
            a.H < (1ll << 31) && a.I < (1ll << 31) &&
            smem_bytes(a.E) <= 227 * 1024 && tensor_map_encoder() != nullptr;
 }
