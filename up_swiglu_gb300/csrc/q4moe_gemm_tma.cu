@@ -33,10 +33,10 @@
 //    Q4 0.895 -> 0.862, Q8 1.162 -> 0.998 against two 16-byte loads (half
 //    the load instructions, and half the L1 lookups for rows that each
 //    sit in their own line);
-//  * each dequantisation thread prefetches its row's line 4 blocks past
+//  * each dequantisation thread prefetches its row's line 2 blocks past
 //    its register ring into L2: the ring's loads then wait on L2, not HBM
-//    (0.977 -> 0.939; the bulk prefetch instead, queued on the TMA unit,
-//    1.37-1.59);
+//    (0.977 -> 0.939 at 4 blocks with 16-byte loads; the bulk prefetch
+//    instead, queued on the TMA unit, 1.37-1.59);
 //  * the weights do not go through TMA: the SM's one TMA unit then also
 //    serves the token rows, and with the HBM-cold weight boxes in its queue
 //    the MMA thread waited ~800 cycles per stage for token rows (~100 with
@@ -433,7 +433,9 @@ gemm_tma_kernel(GateUpArgs a, const __grid_constant__ XgMaps xg_maps) {
         constexpr int kVecs = kQ8 ? 4 : 2;
         constexpr int kDepth = kQ8 ? 2 : 4;
         constexpr int kBlocksPerLine = 128 / (kVecs * 16);
-        constexpr int kPrefetch = 4;         // measured: 4 best of 4-32
+        // measured with 32-byte loads: 2 (Q4 0.8555 ms, Q8 0.991) against
+        // 4 (0.8587, 0.996) and 8 (0.862, 1.010)
+        constexpr int kPrefetch = 2;
         const int64_t rb = weight_row_bytes(a, a.H);
         const uint32_t z = kQ8 ? 0u : 0x88888888u;    // weight zero
         const uint4 kZero = make_uint4(z, z, z, z);
