@@ -32,7 +32,9 @@
 //  * the weights come 32 bytes per load instruction (ld.global.nc.v8):
 //    Q4 0.895 -> 0.862, Q8 1.162 -> 0.998 against two 16-byte loads (half
 //    the load instructions, and half the L1 lookups for rows that each
-//    sit in their own line);
+//    sit in their own line); and without allocating in L1, which then
+//    keeps the sigmoid table: Q4 0.855 -> ~0.81, Q8 0.990 -> ~0.89 (with
+//    16-byte loads the same hint had cost 0.93 -> 1.43);
 //  * each dequantisation thread prefetches its row's line 2 blocks past
 //    its register ring into L2: the ring's loads then wait on L2, not HBM
 //    (0.977 -> 0.939 at 4 blocks with 16-byte loads; the bulk prefetch
@@ -235,11 +237,13 @@ __device__ __forceinline__ uint4 bytes_bf16(uint32_t w0, uint32_t w1) {
                       byte_pair(__byte_perm(w1, 0x43434343u, 0x4342)));
 }
 
-// 32 bytes of weights (two uint4) by one 256-bit load; p must be 32-byte
-// aligned (gemm_tma_supported checks the sections; rows hold a whole
-// number of 64-K blocks, a multiple of 32 bytes).
+// 32 bytes of weights (two uint4) by one 256-bit load that leaves L1 to
+// the epilogue's sigmoid table (each 32-byte sector is read once); p must
+// be 32-byte aligned (gemm_tma_supported checks the sections; rows hold a
+// whole number of 64-K blocks, a multiple of 32 bytes).
 __device__ __forceinline__ void ldg_32(const uint4 *p, uint4 &lo, uint4 &hi) {
-    asm("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm("ld.global.nc.L1::no_allocate.v8.u32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x),
           "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
         : "l"(p));
