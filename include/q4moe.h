@@ -197,8 +197,11 @@ typedef struct q4moe_options {
                            q4moe_workspace_bytes(M, H) bytes, 256-byte
                            aligned, not overlapping any other argument.
                            With it the tensor-core GEMM reads the routed
-                           activations once, grouped, through TMA; without
-                           it the GEMM gathers them row by row.  Contents
+                           activations once, grouped, through TMA (its
+                           fast form also wants 32-byte aligned weight
+                           sections; a layout with sections only 16-byte
+                           aligned takes the row-by-row form); without it
+                           the GEMM gathers them row by row.  Contents
                            are undefined after the call; calls that share a
                            workspace must be ordered on one stream.       */
     int64_t workspace_bytes; /* size of workspace                         */
